@@ -1,0 +1,470 @@
+"""Benchmark of the paged-KV decode step on GB300.
+
+One step is the whole hot path over one batch: the new token of every
+sequence is written into the paged cache (pa_reshape_and_cache), then every
+sequence's query attends over its paged KV (pa_decode). The default workload
+is the Llama-8B-shaped batch: 64 sequences, 32 query / 8 KV heads, head dim
+128, bf16, 16-token blocks, context lengths uniform in [128, 4096], blocks
+shuffled over a pool 1.25x the need. Other workloads (--workload) are the
+shared-prefix, long-context and fp8 cases.
+
+Prints one JSON line (rank 0). ``value`` is whole-job KV GB/s: algorithmic
+bytes of all ranks' steps / max-over-ranks time, where the algorithmic bytes
+of a step are the KV rows of real tokens read by the decode, plus q, out,
+block-table entries and context lengths, plus the new tokens read and written
+by the cache write. Timing: CUDA events around every step on the launching
+stream, the L2 flushed (a 256 MiB write) between steps outside the events.
+
+``--impl reference`` times the fp64 CPU oracle on the same workload instead.
+"""
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "pa_decode KV GB/s and decode tokens/s per layer; % of GB300 HBM roofline"
+L2_FLUSH_BYTES = 256 << 20
+
+
+# ----------------------------------------------------------------------------
+# workloads and their algorithmic bytes
+
+
+def make_case(name, rank):
+    seed_shift = 10007 * rank  # each rank gets its own replica batch of the same shape
+    if name == "llama8b":
+        return workloads.llama8b(seed=1002 + seed_shift)
+    if name == "shared_prefix":
+        return workloads.shared_prefix(seed=1003 + seed_shift)
+    if name.startswith("long_context"):
+        bs = int(name.split("bs")[-1]) if "bs" in name else 16
+        return workloads.long_context(bs, seed=1004 + seed_shift)
+    if name == "fp8_layer":
+        return workloads.fp8_step_layer(0, seed=1005 + seed_shift)
+    raise ValueError(name)
+
+
+def elem(dtype):
+    return workloads.elem_bytes(dtype)
+
+
+def decode_bytes(case):
+    """Algorithmic bytes of one pa_decode: real KV rows, scales, q, out, tables, lengths."""
+    ctx = case.context_lens.astype(np.int64)
+    eb = elem(case.kv_dtype)
+    kv = int(ctx.sum()) * case.num_kv_heads * 2 * case.head_dim * eb
+    nblocks = int(sum(-(-int(c) // case.block_size) for c in ctx if c > 0))
+    scales = nblocks * case.num_kv_heads * 2 * 4 if case.kv_dtype == workloads.FP8_E4M3 else 0
+    qo = 2 * case.num_seqs * case.num_heads * case.head_dim * elem(case.q_dtype)
+    return kv + scales + qo + nblocks * 4 + case.num_seqs * 4
+
+
+def write_bytes(case):
+    """Algorithmic bytes of one pa_reshape_and_cache: sources read, cache rows written, slots."""
+    if case.new_key is None:
+        return 0
+    T = case.new_key.shape[0]
+    src = 2 * T * case.num_kv_heads * case.head_dim * elem(case.src_dtype)
+    dst = 2 * T * case.num_kv_heads * case.head_dim * elem(case.kv_dtype)
+    return src + dst + 8 * T
+
+
+# ----------------------------------------------------------------------------
+# clocks
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the GPU works."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.lines = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = [l for t, l in self.lines if t0 - 0.25 <= t <= t1 + 0.25] or [l for _, l in self.lines]
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            f = [x.strip() for x in r.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# the oracle on the host (cpu_baseline and --impl reference)
+
+
+def oracle_seconds(workload, seqs, reps, rank=0):
+    """Run the fp64 oracle decode on a sample, single-threaded, in a child process."""
+    code = f"""
+import sys, time, json
+sys.path.insert(0, {ROOT!r})
+import numpy as np
+import bench, workloads, oracle
+case = bench.make_case({workload!r}, {rank})
+sel = list(range({seqs}))
+kc, vc = case.k_cache, case.v_cache
+if case.kv_dtype == workloads.FP8_E4M3:
+    kc, vc = kc.copy(), vc.copy()
+    oracle.reshape_and_cache(case.new_key, case.new_value, kc, vc, case.slot_mapping,
+                             case.block_size, case.src_dtype, case.kv_dtype, case.k_scale, case.v_scale)
+times = []
+for r in range({reps}):
+    t = time.perf_counter()
+    oracle.paged_decode(case.q[sel], kc, vc, case.block_tables[sel], case.context_lens[sel],
+                        case.scale, case.block_size, case.q_dtype, case.kv_dtype,
+                        case.k_scale, case.v_scale)
+    times.append(time.perf_counter() - t)
+print(json.dumps(times))
+"""
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "NUMEXPR_NUM_THREADS"):
+        env[k] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                         cwd=ROOT)
+    if res.returncode != 0:
+        raise RuntimeError(res.stderr[-2000:])
+    return json.loads(res.stdout.strip().splitlines()[-1])
+
+
+def sample_case(case, seqs):
+    return workloads.DecodeCase(**{**case.__dict__, "q": case.q[:seqs],
+                                   "block_tables": case.block_tables[:seqs],
+                                   "context_lens": case.context_lens[:seqs], "num_seqs": seqs})
+
+
+def cpu_baseline(workload, case, target_s=12.0):
+    """The oracle on the whole batch, repeated to about target_s seconds of CPU work."""
+    probe = oracle_seconds(workload, case.num_seqs, 1)[0]
+    reps = max(1, min(50, int(math.ceil(target_s / max(probe, 1e-3)))))
+    if probe > target_s:
+        seqs = max(1, int(case.num_seqs * target_s / probe))
+        reps = 1
+    else:
+        seqs = case.num_seqs
+    times = oracle_seconds(workload, seqs, reps)
+    sub = sample_case(case, seqs)
+    gbs = decode_bytes(sub) * len(times) / sum(times) / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"fp64 numpy oracle pa_decode over {seqs} of {case.num_seqs} sequences, "
+                      f"{len(times)} repetitions, {sum(times):.1f} s, 1 thread"}
+
+
+# ----------------------------------------------------------------------------
+# the GPU arm
+
+
+def setup_dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_ours(args, world, rank, local):
+    import paged_kv_cache_288_gb300 as pa
+    from paged_kv_cache_288_gb300 import build
+
+    build.build_library()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    case = make_case(args.workload, rank)
+
+    def to_dev(bits, dtype):
+        a = np.ascontiguousarray(bits)
+        if dtype == workloads.FP8_E4M3:
+            return torch.from_numpy(a.view(np.uint8)).to(device)
+        t = torch.from_numpy(a.view(np.int16)).to(device)
+        return t.view(torch.float16 if dtype == workloads.F16 else torch.bfloat16)
+
+    q = to_dev(case.q, case.q_dtype)
+    kc = to_dev(case.k_cache, case.kv_dtype)
+    vc = to_dev(case.v_cache, case.kv_dtype)
+    tables = torch.from_numpy(case.block_tables).to(device)
+    lens = torch.from_numpy(case.context_lens).to(device)
+    ks = torch.from_numpy(case.k_scale).to(device) if case.k_scale is not None else None
+    vs = torch.from_numpy(case.v_scale).to(device) if case.v_scale is not None else None
+    nk = to_dev(case.new_key, case.src_dtype)
+    nv = to_dev(case.new_value, case.src_dtype)
+    slots = torch.from_numpy(case.slot_mapping).to(device)
+    if case.kv_dtype == workloads.FP8_E4M3:
+        # the fp8 pool starts empty: fill it once through the library (untimed)
+        pa.reshape_and_cache(nk, nv, kc, vc, slots, k_scale=ks, v_scale=vs)
+        T = min(case.num_seqs, nk.shape[0])
+        last = np.cumsum(case.context_lens.astype(np.int64)) - 1
+        nk, nv, slots = nk[last].contiguous(), nv[last].contiguous(), slots[last].contiguous()
+        case.new_key = case.new_key[last]
+        case.new_value = case.new_value[last]
+        del T
+    out = torch.empty_like(q)
+    max_ctx = int(case.context_lens.max())
+    part = args.partition_size
+    ws_bytes = pa.decode_workspace_size(case.num_seqs, case.num_heads, case.num_kv_heads,
+                                        case.head_dim, max_ctx, part)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    launches_before = pa.lib().pa_kernel_launch_count()
+
+    def step():
+        pa.reshape_and_cache(nk, nv, kc, vc, slots, k_scale=ks, v_scale=vs)
+
+    def dec():
+        pa.decode(out, q, kc, vc, tables, lens, case.scale, max_ctx, k_scale=ks, v_scale=vs,
+                  partition_size=part, workspace=ws)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+        dec()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    n0 = pa.lib().pa_kernel_launch_count()
+    t0 = time.time()
+    for k in range(K):
+        flush.zero_()
+        ev[k][0].record(stream)
+        step()
+        ev[k][1].record(stream)
+        dec()
+        ev[k][2].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier(world)
+    n1 = pa.lib().pa_kernel_launch_count()
+    sampler.stop()
+    step_ms = [ev[k][0].elapsed_time(ev[k][2]) for k in range(K)]
+    dec_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)]
+    total_ms = max_over_ranks(sum(step_ms), world, device)
+    dec_mean_ms = statistics.mean(dec_ms)
+
+    # end to end through the public API with host buffers: inputs H2D, output D2H
+    pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+    h_q, h_nk, h_nv, h_slots = pin(q), pin(nk), pin(nv), pin(slots)
+    h_tables, h_lens = pin(tables), pin(lens)
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    d_q, d_nk, d_nv = torch.empty_like(q), torch.empty_like(nk), torch.empty_like(nv)
+    d_slots, d_tables, d_lens = torch.empty_like(slots), torch.empty_like(tables), torch.empty_like(lens)
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_nk, h_nv, h_slots, h_tables, h_lens))
+    d2h = h_out.numel() * h_out.element_size()
+    Ke = max(1, min(K, 200))
+    eev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Ke)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for k in range(Ke):
+        flush.zero_()
+        eev[k][0].record(stream)
+        for dst, src in ((d_q, h_q), (d_nk, h_nk), (d_nv, h_nv), (d_slots, h_slots),
+                         (d_tables, h_tables), (d_lens, h_lens)):
+            dst.copy_(src, non_blocking=True)
+        pa.reshape_and_cache(d_nk, d_nv, kc, vc, d_slots, k_scale=ks, v_scale=vs)
+        pa.decode(out, d_q, kc, vc, d_tables, d_lens, case.scale, max_ctx, k_scale=ks,
+                  v_scale=vs, partition_size=part, workspace=ws)
+        h_out.copy_(out, non_blocking=True)
+        eev[k][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(sum(eev[k][0].elapsed_time(eev[k][1]) for k in range(Ke)), world,
+                            device)
+
+    bytes_step = decode_bytes(case) + write_bytes(case)
+    value = world * bytes_step * K / (total_ms / 1e3) / 1e9
+    e2e_value = world * bytes_step * Ke / (e2e_ms / 1e3) / 1e9
+    dbytes = decode_bytes(case)
+    achieved = dbytes / (dec_mean_ms / 1e3) / 1e9
+    peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(peaks_path):
+        peak = json.load(open(peaks_path))["hbm_gbs"]
+        peak_src = "measured"
+    else:
+        peak, peak_src = 6800.0, "fallback"
+    launches = n1 - n0
+    if rank != 0:
+        return None
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_ms / K, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if case.kv_dtype == workloads.BF16 else (
+            "f16" if case.kv_dtype == workloads.F16 else "fp8_e4m3 KV, bf16 q, f32 accumulate"),
+        "data": "synthetic (seeded N(0,1) K/V/q, shuffled physical blocks)",
+        "config": {
+            "workload": args.workload,
+            "num_seqs": case.num_seqs, "num_heads": case.num_heads,
+            "num_kv_heads": case.num_kv_heads, "head_dim": case.head_dim,
+            "block_size": case.block_size, "num_blocks": case.num_blocks,
+            "context_tokens": int(case.context_lens.sum()),
+            "max_context_len": max_ctx, "partition_size": part,
+            "l2": "flushed between steps (256 MiB write outside the timed events)",
+            "parallelism": f"{world} independent replica(s), one per GPU",
+        },
+        "tokens_per_s_per_layer": round(world * case.num_seqs * K / (total_ms / 1e3), 1),
+        "decode_us": round(dec_mean_ms * 1e3, 2),
+        "decode_bytes": dbytes,
+        "step_bytes": bytes_step,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": None, "kernel": "pa_decode"},
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": Ke},
+        "clocks": sampler.summary(t0, t1),
+        "gpu_launches": launches,
+        "launches_per_step": launches / K,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(args.workload, case)
+    del launches_before
+    return line
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return None
+    case = make_case(args.workload, 0)
+    seqs = max(1, min(case.num_seqs, args.reference_seqs))
+    times = oracle_seconds(args.workload, seqs, args.warmup + args.steps)
+    timed = times[args.warmup:]
+    sub = sample_case(case, seqs)
+    value = decode_bytes(sub) * len(timed) / sum(timed) / 1e9
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 5),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(1e3 * sum(timed) / len(timed), 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64 (oracle)",
+        "data": "synthetic (seeded N(0,1) K/V/q, shuffled physical blocks)",
+        "config": {"workload": args.workload, "num_seqs": case.num_seqs,
+                   "sample_seqs_per_step": seqs},
+        "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"fp64 numpy oracle pa_decode over {seqs} of {case.num_seqs} "
+                                   f"sequences per step, 1 thread"},
+        "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="llama8b")
+    ap.add_argument("--partition-size", type=int, default=0)
+    ap.add_argument("--reference-seqs", type=int, default=8)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+    world, rank, local = setup_dist()
+    if args.impl == "reference":
+        line = run_reference(args, world, rank)
+    else:
+        line = run_ours(args, world, rank, local)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

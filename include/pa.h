@@ -1,0 +1,182 @@
+/*
+ * pa.h - paged KV-cache attention decode for NVIDIA GB300 (sm_103a).
+ *
+ * The KV cache is a pool of fixed-size physical blocks. A sequence owns a
+ * block table that maps its logical block index to a physical block id, so
+ * its blocks need not be contiguous (serving-paged-attention, section
+ * "블록으로 쪼개고 표로 잇는다"; LLM의 Paged Attention, "Paged Attention의
+ * 핵심 원리" items 1-2). Decode attention reads each sequence's scattered
+ * blocks through its table.
+ *
+ * Conventions shared by every call:
+ *  - Tensor arguments are DEVICE pointers owned by the caller. The library
+ *    never allocates, frees or synchronises; it launches on `stream`
+ *    asynchronously and returns.
+ *  - Layouts are dense, row-major, with no padding:
+ *      k_cache, v_cache   [num_blocks, num_kv_heads, block_size, head_dim]
+ *      q, out             [num_seqs, num_heads, head_dim]
+ *      key, value (new)   [num_tokens, num_kv_heads, head_dim]
+ *      block_tables       int32 [num_seqs, max_blocks_per_seq]
+ *      context_lens       int32 [num_seqs]
+ *      slot_mapping       int64 [num_tokens]; slot = block*block_size+offset
+ *      k_scale, v_scale   float32 [num_blocks, num_kv_heads] (8-bit KV only)
+ *  - Query head h reads KV head h / (num_heads / num_kv_heads) (grouped-query
+ *    attention with contiguous groups).
+ *  - Every call returns a pa_status. Bad shapes, types, sizes, null or
+ *    misaligned pointers are rejected before anything is launched. Values
+ *    held in device memory (slots, table entries, context lengths) are
+ *    checked by the kernels themselves: an out-of-range value is skipped
+ *    (never dereferenced) and, when `debug_err` is non-NULL, the matching
+ *    PA_DEVERR_* bit is OR-ed into *debug_err. `debug_err` is a caller-owned
+ *    device int32, never cleared by the library.
+ *  - PA_ERR_CUDA reports a launch error from the CUDA runtime; the message
+ *    of the last failure on the calling thread is pa_last_error_message().
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PA_OK = 0,
+  PA_ERR_INVALID = 1,     /* a host-checked argument is wrong */
+  PA_ERR_UNSUPPORTED = 2, /* valid, but not a shape/type this build runs */
+  PA_ERR_CUDA = 3,        /* the CUDA runtime reported an error */
+  PA_ERR_WORKSPACE = 4    /* the workspace given is too small */
+} pa_status;
+
+typedef enum {
+  PA_F16 = 0,
+  PA_BF16 = 1,
+  PA_FP8_E4M3 = 2 /* OCP OFP8 E4M3: bias 7, max 448, no infinities */
+} pa_dtype;
+
+/* Bits OR-ed into *debug_err by the kernels. */
+#define PA_DEVERR_SLOT_RANGE 0x1    /* slot >= num_blocks * block_size */
+#define PA_DEVERR_BLOCK_RANGE 0x2   /* table entry or copy pair outside [0, num_blocks) */
+#define PA_DEVERR_CONTEXT_RANGE 0x4 /* context length above max_context_len or the table width */
+
+/* Library version, major*10000 + minor*100 + patch. */
+int pa_version(void);
+
+/* Human-readable name of a status code (static storage). */
+const char* pa_status_string(pa_status status);
+
+/* Detail of the last failed call on this thread ("" if none). */
+const char* pa_last_error_message(void);
+
+/* Number of kernels this library has launched in this process (all threads). */
+uint64_t pa_kernel_launch_count(void);
+
+/*
+ * pa_reshape_and_cache - write new tokens' K and V into their cache slots.
+ *
+ * For token t with s = slot_mapping[t] >= 0: block = s / block_size, offset
+ * = s % block_size, and for every KV head h the row key[t, h, :] goes to
+ * k_cache[block, h, offset, :] (value[t, h, :] to v_cache likewise). A slot
+ * of -1 is a padding token and is skipped. This is the token-to-slot table
+ * of vLLM의 핵심 이해: PagedAttention, section 6, applied to the block pool
+ * of serving-paged-attention, "블록으로 쪼개고 표로 잇는다".
+ *
+ * src_dtype must equal kv_dtype for 16-bit caches, which receive the source
+ * bits unchanged. For kv_dtype == PA_FP8_E4M3 (serving-paged-attention,
+ * "실무에서 만지는 지점": an 8-bit KV cache) the sources are f16 or bf16 and
+ * each stored code is e4m3(float(x) / scale[block, h]) with an IEEE float32
+ * division and round-to-nearest-even conversion that saturates at +-448.
+ * k_scale / v_scale are read only (NULL for 16-bit caches). head_dim must be
+ * a multiple of 8; every tensor pointer must be 16-byte aligned.
+ * Out-of-range slots set PA_DEVERR_SLOT_RANGE and are skipped.
+ */
+pa_status pa_reshape_and_cache(const void* key, const void* value, void* k_cache,
+                               void* v_cache, const int64_t* slot_mapping,
+                               int32_t num_tokens, int32_t num_kv_heads,
+                               int32_t head_dim, int32_t block_size,
+                               int32_t num_blocks, pa_dtype src_dtype,
+                               pa_dtype kv_dtype, const float* k_scale,
+                               const float* v_scale, int32_t* debug_err,
+                               cudaStream_t stream);
+
+/*
+ * pa_decode - single-query attention of every sequence over its paged KV.
+ *
+ * For sequence i with L = context_lens[i] and query head h, with g = h / G:
+ *   K, V = rows 0..L-1 of the sequence, gathered through block_tables[i]
+ *          (logical block j lives in physical block block_tables[i, j];
+ *          serving-paged-attention, "블록으로 쪼개고 표로 잇는다")
+ *   out[i, h, :] = softmax(scale * K q[i, h]) V
+ * computed with the online softmax (running max, running sum, rescaled
+ * accumulator) of LLM 추론 확장, 품질·비용 절충 필수, in float32. Entries of a
+ * table past ceil(L / block_size) and the unused tail of the last block are
+ * never read as data. L == 0 gives an all-zero output row.
+ *
+ * Types: q_dtype == kv_dtype for 16-bit caches; with kv_dtype ==
+ * PA_FP8_E4M3, q is f16 or bf16 and k_scale / v_scale give the per-(block,
+ * KV head) dequantisation factors. out has q's type.
+ *
+ * max_context_len is a host-known upper bound on every context_lens[i]
+ * (larger lengths are clamped to it and flag PA_DEVERR_CONTEXT_RANGE).
+ * partition_size = 0 lets the library schedule the work; > 0 forces the
+ * split-context path: partitions of that many tokens are attended
+ * separately into float32 partials in `workspace`, then merged by a reduce
+ * kernel (it must be a multiple of 16 and of block_size). The workspace is
+ * caller-owned device memory of at least pa_decode_workspace_size() bytes,
+ * 256-byte aligned; with partition_size = 0 and a smaller or NULL workspace
+ * the library uses a schedule that needs none.
+ *
+ * Supported: num_heads / num_kv_heads in {1, 2, 4, 8}; head_dim in {64, 128,
+ * 256}; block_size in {8, 16, 32, 64}.
+ */
+pa_status pa_decode(void* out, const void* q, const void* k_cache,
+                    const void* v_cache, const int32_t* block_tables,
+                    int32_t max_blocks_per_seq, const int32_t* context_lens,
+                    int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                    int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                    float scale, pa_dtype q_dtype, pa_dtype kv_dtype,
+                    const float* k_scale, const float* v_scale,
+                    int32_t max_context_len, int32_t partition_size,
+                    void* workspace, size_t workspace_bytes,
+                    int32_t* debug_err, cudaStream_t stream);
+
+/*
+ * Bytes of workspace pa_decode needs for these sizes on the current device
+ * (partition_size as passed to pa_decode; 0 = the library's own schedule).
+ */
+size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_heads,
+                                int32_t num_kv_heads, int32_t head_dim,
+                                int32_t max_context_len, int32_t partition_size);
+
+/*
+ * pa_copy_blocks - copy whole physical blocks, K and V, in every layer.
+ *
+ * For each pair p, src = block_mapping[2p], dst = block_mapping[2p+1], and
+ * each layer l: block dst of k_caches[l] and v_caches[l] becomes a byte copy
+ * of block src. This is the copy of copy-on-write: a request about to write
+ * into a block that other tables share gets its own copy first
+ * (serving-paged-attention, "공유는 표를 베끼는 일이 된다"; LLM의 Paged
+ * Attention, "Paged Attention의 핵심 원리" item 3); redirecting the table
+ * entry is the caller's job.
+ *
+ * k_caches / v_caches are DEVICE arrays of num_layers device pointers;
+ * block_mapping is a DEVICE int64 array [num_pairs, 2]. block_bytes is the
+ * size of one block of one cache (num_kv_heads * block_size * head_dim *
+ * element size), a multiple of 16; cache pointers must be 16-byte aligned.
+ * No dst may equal a src or another dst (one src may feed many dsts).
+ * Pairs outside [0, num_blocks) set PA_DEVERR_BLOCK_RANGE and are skipped.
+ */
+pa_status pa_copy_blocks(void* const* k_caches, void* const* v_caches,
+                         int32_t num_layers, const int64_t* block_mapping,
+                         int32_t num_pairs, int32_t num_blocks,
+                         size_t block_bytes, int32_t* debug_err,
+                         cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

@@ -51,7 +51,8 @@ def reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, block_size,
     serving-paged-attention, section "블록으로 쪼개고 표로 잇는다" (a request
     borrows one free block at a time): slot = block * block_size + offset,
     so block = slot // block_size and offset = slot % block_size. A slot of -1
-    marks a padding token that is not written.
+    marks a padding token that is not written. Slots of distinct tokens are
+    distinct (two tokens in one slot is a caller error).
 
     16-bit caches receive the source bits unchanged. An 8-bit cache
     (serving-paged-attention, "실무에서 만지는 지점": KV stored in 8 bits)
@@ -59,23 +60,23 @@ def reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, block_size,
     float32 and the encoding round-to-nearest-even with saturation; the scales
     belong to the caller and are only read.
     """
-    num_tokens, num_kv_heads, _ = key.shape
-    for t in range(num_tokens):
-        slot = int(slot_mapping[t])
-        if slot < 0:
-            continue
-        blk, off = divmod(slot, block_size)
-        for h in range(num_kv_heads):
-            if kv_dtype == FP8_E4M3:
-                ks = np.float32(k_scale[blk, h])
-                vs = np.float32(v_scale[blk, h])
-                k_cache[blk, h, off, :] = e4m3_encode(_bits_to_f32(key[t, h], src_dtype) / ks)
-                v_cache[blk, h, off, :] = e4m3_encode(_bits_to_f32(value[t, h], src_dtype) / vs)
-            else:
-                if src_dtype != kv_dtype:
-                    raise ValueError("16-bit caches take sources of the same type")
-                k_cache[blk, h, off, :] = key[t, h]
-                v_cache[blk, h, off, :] = value[t, h]
+    slots = np.asarray(slot_mapping, dtype=np.int64)
+    if kv_dtype != FP8_E4M3 and src_dtype != kv_dtype:
+        raise ValueError("16-bit caches take sources of the same type")
+    tokens = np.nonzero(slots >= 0)[0]
+    # tokens are independent (slots are distinct), so they are taken in chunks
+    for start in range(0, len(tokens), 4096):
+        t = tokens[start:start + 4096]
+        blk = slots[t] // block_size
+        off = slots[t] % block_size
+        if kv_dtype == FP8_E4M3:
+            ks = np.asarray(k_scale, dtype=np.float32)[blk][:, :, None]
+            vs = np.asarray(v_scale, dtype=np.float32)[blk][:, :, None]
+            k_cache[blk, :, off, :] = e4m3_encode(_bits_to_f32(key[t], src_dtype) / ks)
+            v_cache[blk, :, off, :] = e4m3_encode(_bits_to_f32(value[t], src_dtype) / vs)
+        else:
+            k_cache[blk, :, off, :] = key[t]
+            v_cache[blk, :, off, :] = value[t]
 
 
 def copy_blocks(k_caches, v_caches, block_mapping):

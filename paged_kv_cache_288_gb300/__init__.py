@@ -1,0 +1,32 @@
+"""Paged KV-cache attention decode for GB300 (sm_103a).
+
+The compute lives in ``libpa.so`` (hand-written CUDA kernels behind the C ABI
+of ``include/pa.h``); this package only marshals torch tensors into those
+calls. Build the library with ``python -m paged_kv_cache_288_gb300.build``.
+Importing the package does not load the library; the first call does, and
+raises if it has not been built.
+"""
+
+from ._binding import (
+    PaError,
+    F16,
+    BF16,
+    FP8_E4M3,
+    DEVERR_SLOT_RANGE,
+    DEVERR_BLOCK_RANGE,
+    DEVERR_CONTEXT_RANGE,
+    lib,
+    library_path,
+    reshape_and_cache,
+    decode,
+    decode_workspace_size,
+    copy_blocks,
+    pointer_array,
+)
+from .block_pool import BlockPool, OutOfBlocks
+
+__all__ = [
+    "PaError", "F16", "BF16", "FP8_E4M3", "DEVERR_SLOT_RANGE", "DEVERR_BLOCK_RANGE",
+    "DEVERR_CONTEXT_RANGE", "lib", "library_path", "reshape_and_cache", "decode",
+    "decode_workspace_size", "copy_blocks", "pointer_array", "BlockPool", "OutOfBlocks",
+]

@@ -1,0 +1,156 @@
+"""ctypes binding of libpa.so: argument marshalling only.
+
+Every function here derives sizes from torch tensor shapes, passes raw
+device pointers and the current CUDA stream to the C ABI of ``include/pa.h``
+and raises ``PaError`` on a non-zero status. No arithmetic of the method is
+done in Python and there is no fallback: without the compiled library the
+calls raise.
+"""
+
+import ctypes
+import os
+
+import torch
+
+F16, BF16, FP8_E4M3 = 0, 1, 2
+DEVERR_SLOT_RANGE = 0x1
+DEVERR_BLOCK_RANGE = 0x2
+DEVERR_CONTEXT_RANGE = 0x4
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libpa.so")
+_lib = None
+
+_c_int32 = ctypes.c_int32
+_c_ptr = ctypes.c_void_p
+_c_size = ctypes.c_size_t
+
+
+class PaError(RuntimeError):
+    def __init__(self, status, what):
+        self.status = status
+        super().__init__(f"{what}: {status_name(status)}: {last_error_message()}")
+
+
+def library_path():
+    return _LIB_PATH
+
+
+def lib():
+    """The loaded libpa.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"{_LIB_PATH} is missing: build it with "
+                               "`python -m paged_kv_cache_288_gb300.build`")
+        L = ctypes.CDLL(_LIB_PATH)
+        L.pa_version.restype = ctypes.c_int
+        L.pa_status_string.restype = ctypes.c_char_p
+        L.pa_status_string.argtypes = [ctypes.c_int]
+        L.pa_last_error_message.restype = ctypes.c_char_p
+        L.pa_kernel_launch_count.restype = ctypes.c_uint64
+        L.pa_reshape_and_cache.restype = ctypes.c_int
+        L.pa_reshape_and_cache.argtypes = [
+            _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int32, _c_int32, _c_int32, _c_int32,
+            _c_int32, ctypes.c_int, ctypes.c_int, _c_ptr, _c_ptr, _c_ptr, _c_ptr]
+        L.pa_decode.restype = ctypes.c_int
+        L.pa_decode.argtypes = [
+            _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int32, _c_ptr, _c_int32, _c_int32,
+            _c_int32, _c_int32, _c_int32, _c_int32, ctypes.c_float, ctypes.c_int, ctypes.c_int,
+            _c_ptr, _c_ptr, _c_int32, _c_int32, _c_ptr, _c_size, _c_ptr, _c_ptr]
+        L.pa_decode_workspace_size.restype = _c_size
+        L.pa_decode_workspace_size.argtypes = [_c_int32] * 6
+        L.pa_copy_blocks.restype = ctypes.c_int
+        L.pa_copy_blocks.argtypes = [_c_ptr, _c_ptr, _c_int32, _c_ptr, _c_int32, _c_int32,
+                                     _c_size, _c_ptr, _c_ptr]
+        _lib = L
+    return _lib
+
+
+def status_name(status):
+    return lib().pa_status_string(int(status)).decode()
+
+
+def last_error_message():
+    return lib().pa_last_error_message().decode()
+
+
+def _dtype_code(t):
+    if t == torch.float16:
+        return F16
+    if t == torch.bfloat16:
+        return BF16
+    if t in (torch.uint8, torch.float8_e4m3fn):
+        return FP8_E4M3
+    raise TypeError(f"unsupported dtype {t}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(status, what):
+    if status != 0:
+        raise PaError(status, what)
+
+
+def reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, k_scale=None, v_scale=None,
+                      debug_err=None, stream=None):
+    """Write new tokens' K/V ([T, Hkv, d]) into the caches ([Nb, Hkv, bs, d]) at their slots."""
+    T, Hkv, d = key.shape
+    Nb, Hkv2, bs, d2 = k_cache.shape
+    if (Hkv, d) != (Hkv2, d2) or value.shape != key.shape or v_cache.shape != k_cache.shape:
+        raise ValueError("shape mismatch between new tokens and caches")
+    if slot_mapping.dtype != torch.int64 or slot_mapping.numel() != T:
+        raise ValueError("slot_mapping must be int64 [num_tokens]")
+    _check(lib().pa_reshape_and_cache(
+        _ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping), T, Hkv, d, bs,
+        Nb, _dtype_code(key.dtype), _dtype_code(k_cache.dtype), _ptr(k_scale), _ptr(v_scale),
+        _ptr(debug_err), _stream(stream)), "pa_reshape_and_cache")
+
+
+def decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, max_context_len,
+                          partition_size=0):
+    return int(lib().pa_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim,
+                                              max_context_len, partition_size))
+
+
+def decode(out, q, k_cache, v_cache, block_tables, context_lens, scale, max_context_len,
+           k_scale=None, v_scale=None, partition_size=0, workspace=None, debug_err=None,
+           stream=None):
+    """out[B, Hq, d] = paged single-query attention of q[B, Hq, d] over the caches."""
+    B, Hq, d = q.shape
+    Nb, Hkv, bs, d2 = k_cache.shape
+    if d2 != d or out.shape != q.shape or v_cache.shape != k_cache.shape:
+        raise ValueError("shape mismatch")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise ValueError("block_tables and context_lens must be int32")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or context_lens.numel() != B:
+        raise ValueError("block_tables must be [num_seqs, max_blocks]; context_lens [num_seqs]")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().pa_decode(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+        block_tables.shape[1], _ptr(context_lens), B, Hq, Hkv, d, bs, Nb, float(scale),
+        _dtype_code(q.dtype), _dtype_code(k_cache.dtype), _ptr(k_scale), _ptr(v_scale),
+        int(max_context_len), int(partition_size), _ptr(workspace), ws_bytes, _ptr(debug_err),
+        _stream(stream)), "pa_decode")
+
+
+def pointer_array(tensors, device):
+    """Device int64 array of the tensors' data pointers (for copy_blocks)."""
+    return torch.tensor([t.data_ptr() for t in tensors], dtype=torch.int64, device=device)
+
+
+def copy_blocks(k_ptrs, v_ptrs, block_mapping, num_blocks, block_bytes, debug_err=None,
+                stream=None):
+    """Copy blocks (src, dst) = block_mapping[p] in every layer; *_ptrs from pointer_array."""
+    if block_mapping.dtype != torch.int64 or block_mapping.dim() != 2 or block_mapping.shape[1] != 2:
+        raise ValueError("block_mapping must be int64 [num_pairs, 2]")
+    _check(lib().pa_copy_blocks(
+        _ptr(k_ptrs), _ptr(v_ptrs), k_ptrs.numel(), _ptr(block_mapping), block_mapping.shape[0],
+        int(num_blocks), int(block_bytes), _ptr(debug_err), _stream(stream)), "pa_copy_blocks")

@@ -1,0 +1,274 @@
+// General paged decode on the CUDA cores.
+//
+// One CTA of 4 warps handles one (partition, KV head, sequence). The warps
+// take the partition's blocks round-robin. Lane l owns head_dim/32
+// consecutive elements of every row, so a K or V row is one coalesced
+// warp-wide load; q.k is a per-lane partial dot product finished with
+// xor-shuffles. Each warp keeps the online-softmax state (running max m,
+// running sum l, accumulator acc rescaled by exp(m_old - m_new)) for the G
+// query heads of its KV head, four tokens at a time; the four warp states
+// are merged through shared memory at the end. With a single partition the
+// CTA writes the output row; otherwise it writes a normalised float32
+// partial plus (m, l) and reduce_partitions_kernel merges them.
+#include "common.cuh"
+#include "internal.h"
+
+namespace pa {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kChunk = 4;  // tokens per online-softmax update
+
+template <typename QT, typename KT, int D, int G>
+__global__ void __launch_bounds__(kWarps * 32)
+decode_simt_kernel(const DecodeParams p) {
+  constexpr int EPL = D / 32;  // elements per lane
+  constexpr bool kFp8 = is_fp8<KT>::value;
+  const int part = blockIdx.x;
+  const int kvh = blockIdx.y;
+  const int seq = blockIdx.z;
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  const int ctx = clamp_context(p, seq);
+  const int tok_begin = part * p.partition_size;
+  const int tok_end = min(ctx, tok_begin + p.partition_size);
+  const bool single = p.num_partitions == 1;
+  if (tok_begin >= tok_end && !(single && part == 0)) return;  // partition past the end
+
+  // query rows of this KV head's group, widened to float
+  float qf[G][EPL];
+  const QT* q = static_cast<const QT*>(p.q);
+#pragma unroll
+  for (int j = 0; j < G; ++j)
+    load_float<QT, EPL>(q + (static_cast<int64_t>(seq) * p.num_heads + kvh * G + j) * D + lane * EPL,
+                        qf[j]);
+
+  float m[G], l[G], acc[G][EPL];
+#pragma unroll
+  for (int j = 0; j < G; ++j) {
+    m[j] = -INFINITY;
+    l[j] = 0.f;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) acc[j][e] = 0.f;
+  }
+
+  const KT* kc = static_cast<const KT*>(p.k_cache);
+  const KT* vc = static_cast<const KT*>(p.v_cache);
+  const int bs = p.block_size;
+  const int32_t* table = p.block_tables + static_cast<int64_t>(seq) * p.max_blocks_per_seq;
+  const int blk_begin = tok_begin / bs;
+  const int blk_end = (tok_end + bs - 1) / bs;
+
+  for (int b = blk_begin + warp; b < blk_end; b += kWarps) {
+    const int phys = table[b];
+    if (phys < 0 || phys >= p.num_blocks) {
+      if (lane == 0) flag_error(p.debug_err, PA_DEVERR_BLOCK_RANGE);
+      continue;
+    }
+    const int valid = min(bs, tok_end - b * bs);
+    const int64_t row0 = (static_cast<int64_t>(phys) * p.num_kv_heads + kvh) * bs;
+    float kscale = 1.f, vscale = 1.f;
+    if constexpr (kFp8) {
+      kscale = p.k_scale[static_cast<int64_t>(phys) * p.num_kv_heads + kvh];
+      vscale = p.v_scale[static_cast<int64_t>(phys) * p.num_kv_heads + kvh];
+    }
+    for (int t0 = 0; t0 < valid; t0 += kChunk) {
+      float kf[kChunk][EPL];
+#pragma unroll
+      for (int u = 0; u < kChunk; ++u) {
+        if (t0 + u < valid) {
+          load_float<KT, EPL>(kc + (row0 + t0 + u) * D + lane * EPL, kf[u]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) kf[u][e] = 0.f;
+        }
+      }
+      float s[kChunk][G];
+#pragma unroll
+      for (int u = 0; u < kChunk; ++u)
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+          float d = 0.f;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) d = fmaf(qf[j][e], kf[u][e], d);
+          s[u][j] = d;
+        }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+        for (int u = 0; u < kChunk; ++u)
+#pragma unroll
+          for (int j = 0; j < G; ++j) s[u][j] += __shfl_xor_sync(0xffffffffu, s[u][j], off);
+
+      float vf[kChunk][EPL];
+#pragma unroll
+      for (int u = 0; u < kChunk; ++u) {
+        if (t0 + u < valid) {
+          load_float<KT, EPL>(vc + (row0 + t0 + u) * D + lane * EPL, vf[u]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) vf[u][e] = 0.f;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < G; ++j) {
+        float cmax = -INFINITY;
+#pragma unroll
+        for (int u = 0; u < kChunk; ++u) {
+          s[u][j] = (t0 + u < valid) ? s[u][j] * (p.scale_log2 * kscale) : -INFINITY;
+          cmax = fmaxf(cmax, s[u][j]);
+        }
+        const float m_new = fmaxf(m[j], cmax);
+        const float alpha = exp2f(m[j] - m_new);  // 0 when m[j] is -inf
+        m[j] = m_new;
+        float psum = 0.f;
+        float pu[kChunk];
+#pragma unroll
+        for (int u = 0; u < kChunk; ++u) {
+          pu[u] = exp2f(s[u][j] - m_new);
+          psum += pu[u];
+        }
+        l[j] = l[j] * alpha + psum;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+          float a = acc[j][e] * alpha;
+#pragma unroll
+          for (int u = 0; u < kChunk; ++u) a = fmaf(pu[u] * vscale, vf[u][e], a);
+          acc[j][e] = a;
+        }
+      }
+    }
+  }
+
+  // merge the warps' states
+  __shared__ float sm_m[kWarps][G];
+  __shared__ float sm_l[kWarps][G];
+  __shared__ float sm_acc[kWarps][G][D];
+  if (lane == 0) {
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      sm_m[warp][j] = m[j];
+      sm_l[warp][j] = l[j];
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < G; ++j)
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) sm_acc[warp][j][lane * EPL + e] = acc[j][e];
+  __syncthreads();
+
+  for (int idx = threadIdx.x; idx < G * D; idx += kWarps * 32) {
+    const int j = idx / D;
+    const int e = idx % D;
+    float mt = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) mt = fmaxf(mt, sm_m[w][j]);
+    float lt = 0.f, at = 0.f;
+    if (mt != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float f = exp2f(sm_m[w][j] - mt);
+        lt += sm_l[w][j] * f;
+        at += sm_acc[w][j][e] * f;
+      }
+    }
+    const float o = lt > 0.f ? at / lt : 0.f;
+    const int h = kvh * G + j;
+    if (single) {
+      QT* out = static_cast<QT*>(p.out);
+      out[(static_cast<int64_t>(seq) * p.num_heads + h) * D + e] = from_float(o, static_cast<QT*>(nullptr));
+    } else {
+      const int64_t slot = (static_cast<int64_t>(seq) * p.num_heads + h) * p.num_partitions + part;
+      p.ws_acc[slot * D + e] = o;
+      if (e == 0) {
+        p.ws_ml[slot * 2] = mt;
+        p.ws_ml[slot * 2 + 1] = lt;
+      }
+    }
+  }
+}
+
+// Merge the partitions of one (sequence, query head): with M = max_p m_p and
+// w_p = 2^(m_p - M) * l_p, out = sum_p w_p * o_p / sum_p w_p.
+template <typename QT, int D>
+__global__ void __launch_bounds__(128) reduce_partitions_kernel(const DecodeParams p) {
+  const int h = blockIdx.x;
+  const int seq = blockIdx.y;
+  const int ctx = clamp_context(p, seq);
+  const int nparts = (ctx + p.partition_size - 1) / p.partition_size;
+  const int64_t base = (static_cast<int64_t>(seq) * p.num_heads + h) * p.num_partitions;
+  extern __shared__ float sm_w[];  // [num_partitions]
+  __shared__ float sm_max, sm_sum;
+  if (threadIdx.x < 32) {
+    float mt = -INFINITY;
+    for (int q = threadIdx.x; q < nparts; q += 32) mt = fmaxf(mt, p.ws_ml[(base + q) * 2]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
+    float st = 0.f;
+    for (int q = threadIdx.x; q < nparts; q += 32) {
+      const float w = (mt == -INFINITY) ? 0.f : exp2f(p.ws_ml[(base + q) * 2] - mt) * p.ws_ml[(base + q) * 2 + 1];
+      sm_w[q] = w;
+      st += w;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) st += __shfl_xor_sync(0xffffffffu, st, off);
+    if (threadIdx.x == 0) {
+      sm_max = mt;
+      sm_sum = st;
+    }
+  }
+  __syncthreads();
+  QT* out = static_cast<QT*>(p.out);
+  const float inv = sm_sum > 0.f ? 1.f / sm_sum : 0.f;
+  for (int e = threadIdx.x; e < D; e += blockDim.x) {
+    float a = 0.f;
+    for (int q = 0; q < nparts; ++q) a = fmaf(sm_w[q], p.ws_acc[(base + q) * D + e], a);
+    out[(static_cast<int64_t>(seq) * p.num_heads + h) * D + e] = from_float(a * inv, static_cast<QT*>(nullptr));
+  }
+}
+
+template <typename QT, typename KT, int D>
+cudaError_t launch_d(const DecodeParams& p, int group, cudaStream_t stream) {
+  dim3 grid(p.num_partitions, p.num_kv_heads, p.num_seqs);
+  switch (group) {
+    case 1: decode_simt_kernel<QT, KT, D, 1><<<grid, kWarps * 32, 0, stream>>>(p); break;
+    case 2: decode_simt_kernel<QT, KT, D, 2><<<grid, kWarps * 32, 0, stream>>>(p); break;
+    case 4: decode_simt_kernel<QT, KT, D, 4><<<grid, kWarps * 32, 0, stream>>>(p); break;
+    case 8: decode_simt_kernel<QT, KT, D, 8><<<grid, kWarps * 32, 0, stream>>>(p); break;
+    default: return cudaErrorInvalidValue;
+  }
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  note_launches(1);
+  if (p.num_partitions == 1) return err;
+  dim3 rgrid(p.num_heads, p.num_seqs);
+  reduce_partitions_kernel<QT, D><<<rgrid, 128, p.num_partitions * sizeof(float), stream>>>(p);
+  err = cudaGetLastError();
+  if (err == cudaSuccess) note_launches(1);
+  return err;
+}
+
+template <typename QT, typename KT>
+cudaError_t launch_t(const DecodeParams& p, int head_dim, int group, cudaStream_t stream) {
+  switch (head_dim) {
+    case 64: return launch_d<QT, KT, 64>(p, group, stream);
+    case 128: return launch_d<QT, KT, 128>(p, group, stream);
+    case 256: return launch_d<QT, KT, 256>(p, group, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_decode_simt(const DecodeParams& p, int head_dim, pa_dtype q_dtype,
+                               pa_dtype kv_dtype, cudaStream_t stream) {
+  if (p.num_seqs == 0) return cudaSuccess;
+  const int group = p.num_heads / p.num_kv_heads;
+  if (kv_dtype == PA_F16) return launch_t<f16, f16>(p, head_dim, group, stream);
+  if (kv_dtype == PA_BF16) return launch_t<bf16, bf16>(p, head_dim, group, stream);
+  if (q_dtype == PA_F16) return launch_t<f16, fp8>(p, head_dim, group, stream);
+  return launch_t<bf16, fp8>(p, head_dim, group, stream);
+}
+
+}  // namespace pa

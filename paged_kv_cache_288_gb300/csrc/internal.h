@@ -1,0 +1,32 @@
+// Launchers shared between the translation units of the library. These are
+// C++ (namespace pa); the C-ABI lives in pa_api.cu.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pa.h"
+
+namespace pa {
+
+struct DecodeParams;
+
+// Adds n to the process-wide count of kernels launched by this library.
+void note_launches(int n);
+
+cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* k_cache,
+                                     void* v_cache, const int64_t* slot_mapping, int num_tokens,
+                                     int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                     pa_dtype src_dtype, pa_dtype kv_dtype, const float* k_scale,
+                                     const float* v_scale, int32_t* debug_err, cudaStream_t stream);
+
+cudaError_t launch_copy_blocks(void* const* k_caches, void* const* v_caches, int num_layers,
+                               const int64_t* block_mapping, int num_pairs, int num_blocks,
+                               size_t block_bytes, int32_t* debug_err, cudaStream_t stream);
+
+// CUDA-core decode: grid (num_partitions, num_kv_heads, num_seqs), plus the
+// partition reduce when num_partitions > 1.
+cudaError_t launch_decode_simt(const DecodeParams& p, int head_dim, pa_dtype q_dtype,
+                               pa_dtype kv_dtype, cudaStream_t stream);
+
+}  // namespace pa

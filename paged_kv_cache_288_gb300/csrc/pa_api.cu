@@ -1,0 +1,230 @@
+// The C ABI of the library: argument checks, schedule choice, launches.
+#include <atomic>
+#include <cmath>
+#include <cstdio>
+#include <cstdarg>
+#include <string>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+std::atomic<uint64_t> g_launches{0};
+
+pa_status fail(pa_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+pa_status from_cuda(cudaError_t err, const char* what) {
+  if (err == cudaSuccess) return PA_OK;
+  return fail(PA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(err));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool is_16bit(pa_dtype t) { return t == PA_F16 || t == PA_BF16; }
+bool valid_dtype(pa_dtype t) { return t == PA_F16 || t == PA_BF16 || t == PA_FP8_E4M3; }
+bool supported_block_size(int bs) { return bs == 8 || bs == 16 || bs == 32 || bs == 64; }
+bool supported_group(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
+bool supported_head_dim(int d) { return d == 64 || d == 128 || d == 256; }
+
+constexpr int kAutoPartition = 512;
+
+int num_partitions_for(int max_context_len, int partition_size) {
+  return max_context_len <= 0 ? 1 : (max_context_len + partition_size - 1) / partition_size;
+}
+
+size_t split_workspace_bytes(int num_seqs, int num_heads, int head_dim, int nparts) {
+  const size_t slots = static_cast<size_t>(num_seqs) * num_heads * nparts;
+  const size_t acc = ((slots * head_dim * sizeof(float)) + 255) / 256 * 256;
+  const size_t ml = ((slots * 2 * sizeof(float)) + 255) / 256 * 256;
+  return acc + ml;
+}
+
+// The split schedule the library picks by itself, or 0 for a single pass.
+int auto_partition(int max_context_len) {
+  return max_context_len > kAutoPartition ? kAutoPartition : 0;
+}
+
+}  // namespace
+
+namespace pa {
+void note_launches(int n) { g_launches.fetch_add(static_cast<uint64_t>(n), std::memory_order_relaxed); }
+}  // namespace pa
+
+extern "C" {
+
+uint64_t pa_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int pa_version(void) { return 100; }
+
+const char* pa_status_string(pa_status status) {
+  switch (status) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_INVALID: return "PA_ERR_INVALID";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA";
+    case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE";
+  }
+  return "PA_ERR_UNKNOWN";
+}
+
+const char* pa_last_error_message(void) { return g_last_error.c_str(); }
+
+pa_status pa_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
+                               const int64_t* slot_mapping, int32_t num_tokens,
+                               int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                               int32_t num_blocks, pa_dtype src_dtype, pa_dtype kv_dtype,
+                               const float* k_scale, const float* v_scale, int32_t* debug_err,
+                               cudaStream_t stream) {
+  if (num_tokens < 0) return fail(PA_ERR_INVALID, "num_tokens < 0");
+  if (num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0)
+    return fail(PA_ERR_INVALID, "sizes must be positive");
+  if (head_dim % 8 != 0) return fail(PA_ERR_INVALID, "head_dim must be a multiple of 8");
+  if (!valid_dtype(src_dtype) || !valid_dtype(kv_dtype)) return fail(PA_ERR_INVALID, "bad dtype");
+  if (!is_16bit(src_dtype)) return fail(PA_ERR_INVALID, "sources must be f16 or bf16");
+  if (is_16bit(kv_dtype) && src_dtype != kv_dtype)
+    return fail(PA_ERR_INVALID, "a 16-bit cache takes sources of its own type");
+  if (kv_dtype == PA_FP8_E4M3 && (k_scale == nullptr || v_scale == nullptr))
+    return fail(PA_ERR_INVALID, "an 8-bit cache needs k_scale and v_scale");
+  if (num_tokens == 0) return PA_OK;
+  if (!key || !value || !k_cache || !v_cache || !slot_mapping)
+    return fail(PA_ERR_INVALID, "null tensor pointer");
+  if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache))
+    return fail(PA_ERR_INVALID, "tensor pointers must be 16-byte aligned");
+  return from_cuda(pa::launch_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping,
+                                                num_tokens, num_kv_heads, head_dim, block_size,
+                                                num_blocks, src_dtype, kv_dtype, k_scale, v_scale,
+                                                debug_err, stream),
+                   "reshape_and_cache launch");
+}
+
+size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                                int32_t head_dim, int32_t max_context_len,
+                                int32_t partition_size) {
+  (void)num_kv_heads;
+  if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || max_context_len <= 0) return 0;
+  const int part = partition_size > 0 ? partition_size : auto_partition(max_context_len);
+  if (part == 0) return 0;
+  return split_workspace_bytes(num_seqs, num_heads, head_dim,
+                               num_partitions_for(max_context_len, part));
+}
+
+pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* block_tables, int32_t max_blocks_per_seq,
+                    const int32_t* context_lens, int32_t num_seqs, int32_t num_heads,
+                    int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                    int32_t num_blocks, float scale, pa_dtype q_dtype, pa_dtype kv_dtype,
+                    const float* k_scale, const float* v_scale, int32_t max_context_len,
+                    int32_t partition_size, void* workspace, size_t workspace_bytes,
+                    int32_t* debug_err, cudaStream_t stream) {
+  if (num_seqs < 0) return fail(PA_ERR_INVALID, "num_seqs < 0");
+  if (num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+      num_blocks <= 0 || max_blocks_per_seq <= 0)
+    return fail(PA_ERR_INVALID, "sizes must be positive");
+  if (num_heads % num_kv_heads != 0)
+    return fail(PA_ERR_INVALID, "num_heads must be a multiple of num_kv_heads");
+  if (head_dim % 8 != 0) return fail(PA_ERR_INVALID, "head_dim must be a multiple of 8");
+  if (!valid_dtype(q_dtype) || !valid_dtype(kv_dtype)) return fail(PA_ERR_INVALID, "bad dtype");
+  if (!is_16bit(q_dtype)) return fail(PA_ERR_INVALID, "q must be f16 or bf16");
+  if (is_16bit(kv_dtype) && q_dtype != kv_dtype)
+    return fail(PA_ERR_INVALID, "q and a 16-bit cache must have the same type");
+  if (kv_dtype == PA_FP8_E4M3 && (k_scale == nullptr || v_scale == nullptr))
+    return fail(PA_ERR_INVALID, "an 8-bit cache needs k_scale and v_scale");
+  if (!std::isfinite(scale)) return fail(PA_ERR_INVALID, "scale must be finite");
+  if (max_context_len < 0) return fail(PA_ERR_INVALID, "max_context_len < 0");
+  if (static_cast<int64_t>(max_context_len) > static_cast<int64_t>(max_blocks_per_seq) * block_size)
+    return fail(PA_ERR_INVALID, "max_context_len exceeds max_blocks_per_seq * block_size");
+  if (partition_size < 0) return fail(PA_ERR_INVALID, "partition_size < 0");
+  if (partition_size > 0 && (partition_size % 16 != 0 || partition_size % block_size != 0))
+    return fail(PA_ERR_INVALID, "partition_size must be a multiple of 16 and of block_size");
+  if (!supported_block_size(block_size))
+    return fail(PA_ERR_UNSUPPORTED, "block_size %d not in {8,16,32,64}", block_size);
+  if (!supported_group(num_heads / num_kv_heads))
+    return fail(PA_ERR_UNSUPPORTED, "num_heads/num_kv_heads %d not in {1,2,4,8}",
+                num_heads / num_kv_heads);
+  if (!supported_head_dim(head_dim))
+    return fail(PA_ERR_UNSUPPORTED, "head_dim %d not in {64,128,256}", head_dim);
+  if (num_seqs == 0) return PA_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
+    return fail(PA_ERR_INVALID, "null tensor pointer");
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return fail(PA_ERR_INVALID, "tensor pointers must be 16-byte aligned");
+  if (workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(PA_ERR_INVALID, "workspace must be 256-byte aligned");
+
+  pa::DecodeParams p{};
+  p.out = out;
+  p.q = q;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.debug_err = debug_err;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.num_seqs = num_seqs;
+  p.num_heads = num_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.block_size = block_size;
+  p.num_blocks = num_blocks;
+  p.max_context_len = max_context_len;
+  p.scale_log2 = scale * pa::kLog2e;
+
+  int part = partition_size;
+  if (part > 0) {
+    const size_t need = split_workspace_bytes(num_seqs, num_heads, head_dim,
+                                              num_partitions_for(max_context_len, part));
+    if (workspace == nullptr || workspace_bytes < need)
+      return fail(PA_ERR_WORKSPACE, "split decode needs %zu workspace bytes, got %zu", need,
+                  workspace_bytes);
+  } else {
+    part = auto_partition(max_context_len);
+    if (part > 0) {
+      const size_t need = split_workspace_bytes(num_seqs, num_heads, head_dim,
+                                                num_partitions_for(max_context_len, part));
+      if (workspace == nullptr || workspace_bytes < need) part = 0;
+    }
+  }
+  if (part > 0) {
+    p.partition_size = part;
+    p.num_partitions = num_partitions_for(max_context_len, part);
+    const size_t slots = static_cast<size_t>(num_seqs) * num_heads * p.num_partitions;
+    p.ws_acc = static_cast<float*>(workspace);
+    p.ws_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                       ((slots * head_dim * sizeof(float)) + 255) / 256 * 256);
+  } else {
+    // one pass over the whole sequence
+    p.partition_size = max_context_len > 0 ? ((max_context_len + block_size - 1) / block_size) * block_size
+                                           : block_size;
+    p.num_partitions = 1;
+  }
+  return from_cuda(pa::launch_decode_simt(p, head_dim, q_dtype, kv_dtype, stream),
+                   "decode launch");
+}
+
+pa_status pa_copy_blocks(void* const* k_caches, void* const* v_caches, int32_t num_layers,
+                         const int64_t* block_mapping, int32_t num_pairs, int32_t num_blocks,
+                         size_t block_bytes, int32_t* debug_err, cudaStream_t stream) {
+  if (num_layers < 0 || num_pairs < 0) return fail(PA_ERR_INVALID, "negative count");
+  if (num_blocks <= 0) return fail(PA_ERR_INVALID, "num_blocks must be positive");
+  if (block_bytes == 0 || block_bytes % 16 != 0)
+    return fail(PA_ERR_INVALID, "block_bytes must be a positive multiple of 16");
+  if (num_layers == 0 || num_pairs == 0) return PA_OK;
+  if (num_layers > 65535) return fail(PA_ERR_UNSUPPORTED, "more than 65535 layers");
+  if (!k_caches || !v_caches || !block_mapping) return fail(PA_ERR_INVALID, "null pointer");
+  return from_cuda(pa::launch_copy_blocks(k_caches, v_caches, num_layers, block_mapping,
+                                          num_pairs, num_blocks, block_bytes, debug_err, stream),
+                   "copy_blocks launch");
+}
+
+}  // extern "C"

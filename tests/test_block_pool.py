@@ -1,0 +1,111 @@
+"""Host block pool: free list, on-demand growth, sharing, copy-on-write."""
+
+import numpy as np
+import pytest
+
+import oracle
+from paged_kv_cache_288_gb300 import BlockPool, OutOfBlocks
+
+
+def test_grows_one_block_at_a_time():
+    pool = BlockPool(10, 16)
+    slots = pool.add_sequence("a", 5)
+    assert pool.used_blocks() == 1 and len(slots) == 5
+    b0 = pool.tables["a"][0]
+    assert slots == [b0 * 16 + i for i in range(5)]
+    s, cow = pool.append("a", 11)
+    assert pool.used_blocks() == 1 and not cow
+    s, cow = pool.append("a", 1)  # token 17 opens a second block
+    assert pool.used_blocks() == 2 and s == [pool.tables["a"][1] * 16]
+
+
+def test_tail_waste_matches_closed_form():
+    rng = np.random.default_rng(3)
+    pool = BlockPool(100000, 16)
+    for i, n in enumerate(rng.integers(1, 3000, 300)):
+        pool.add_sequence(i, int(n))
+        assert pool.tail_waste(i) == oracle.paged_tail_waste_tokens(int(n), 16) <= 15
+
+
+def test_free_blocks_are_reused_by_anyone():
+    pool = BlockPool(4, 8)
+    pool.add_sequence("a", 16)
+    pool.add_sequence("b", 16)
+    with pytest.raises(OutOfBlocks):
+        pool.add_sequence("c", 1)
+    pool.free_sequence("a")
+    assert pool.num_free == 2
+    pool.add_sequence("c", 9)  # any two free blocks fit, wherever they are
+    assert pool.num_free == 0
+
+
+def test_capacity_rule_on_a_full_pool():
+    pool = BlockPool(8192, 16)
+    n = 0
+    while True:
+        try:
+            pool.add_sequence(n, 512)
+        except OutOfBlocks:
+            break
+        n += 1
+    assert n == oracle.concurrent_capacity(8192, 16, 512) == 256
+
+
+def test_fork_shares_then_copies_on_write():
+    pool = BlockPool(20, 16)
+    pool.add_sequence("p", 24)           # blocks: full, half full
+    pool.fork("p", "c")
+    a, b = pool.tables["p"]
+    assert pool.tables["c"] == [a, b] and pool.refcount[a] == 2 and pool.refcount[b] == 2
+    slots, cow = pool.append("c", 1)     # writes into the shared half-full block
+    assert len(cow) == 1 and cow[0][0] == b
+    new = cow[0][1]
+    assert pool.tables["c"] == [a, new] and pool.refcount[b] == 1 and pool.refcount[new] == 1
+    assert slots == [new * 16 + 8]
+    slots, cow = pool.append("p", 1)     # the parent now owns b alone: no copy
+    assert not cow and slots == [b * 16 + 8]
+
+
+def test_prefix_sharing_pattern_of_one_hundred_requests():
+    """100 requests over one 1016-token prompt: 64 shared blocks, 100 copies of the last."""
+    pool = BlockPool(4000, 16)
+    pool.add_sequence("prompt", 1016)
+    total_cow = []
+    for i in range(100):
+        pool.fork("prompt", i)
+        _, cow = pool.append(i, 40)
+        total_cow += cow
+    shared = pool.tables["prompt"]
+    assert len(shared) == 64
+    assert len(total_cow) == 100 and all(src == shared[-1] for src, _ in total_cow)
+    for b in shared[:-1]:
+        assert pool.refcount[b] == 101
+    # the sharing saves what the closed form says
+    per_token = oracle.kv_cache_bytes(32, 8, 128, 1, 2)
+    private = 100 * (1016 + 40)
+    used = pool.used_blocks() * 16
+    assert used < private
+    assert (private - used) * per_token > 0
+
+
+def test_beam_pruning_frees_only_unshared_blocks():
+    pool = BlockPool(20, 4)
+    pool.add_sequence("root", 8)
+    pool.fork("root", "beam1")
+    pool.fork("root", "beam2")
+    pool.append("beam1", 3)
+    pool.append("beam2", 3)
+    before = pool.num_free
+    pool.free_sequence("beam2")
+    assert pool.num_free == before + 1  # only beam2's own block returns
+    assert all(pool.refcount[b] == 2 for b in pool.tables["root"])
+
+
+def test_block_table_array_padding():
+    pool = BlockPool(10, 4)
+    pool.add_sequence(0, 9)
+    pool.add_sequence(1, 2)
+    t = pool.block_table_array([0, 1], width=4, pad=7)
+    assert t.dtype == np.int32 and t.shape == (2, 4)
+    assert list(t[1, 1:]) == [7, 7, 7]
+    assert list(pool.context_lens([0, 1])) == [9, 2]

@@ -1,0 +1,215 @@
+"""GPU parity of pa_decode against the fp64 oracle on small and edge cases."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from workloads import F16, BF16, FP8_E4M3
+from gpu_helpers import (DeviceCase, assert_close, dev, host_bits, oracle_decode, run_decode,
+                         to_f64)
+import paged_kv_cache_288_gb300 as pa
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(case, partition_size=0, workspace=True):
+    dc = DeviceCase(case)
+    out = run_decode(pa, dc, partition_size=partition_size, workspace=workspace)
+    ref = oracle_decode(case)
+    torch.cuda.synchronize()
+    assert dc.debug_err.item() == 0
+    return assert_close(out, ref, case.q_dtype, case.kv_dtype, case.name), out, dc
+
+
+def test_tiny_decode_append_decode():
+    """Lengths 5/17/33/64, GQA 2, d 64, fp16; append one token each, decode again."""
+    before, step = workloads.tiny()
+    _check(before)
+    dc = DeviceCase(before)
+    # append through the library, then decode at the new lengths
+    dstep = DeviceCase(step)
+    pa.reshape_and_cache(dstep.new_key, dstep.new_value, dc.k_cache, dc.v_cache,
+                         dstep.slot_mapping, debug_err=dc.debug_err)
+    kc, vc = before.k_cache.copy(), before.v_cache.copy()
+    oracle.reshape_and_cache(step.new_key, step.new_value, kc, vc, step.slot_mapping, 16, F16, F16)
+    torch.cuda.synchronize()
+    assert np.array_equal(host_bits(dc.k_cache), kc)
+    assert np.array_equal(host_bits(dc.v_cache), vc)
+    out = run_decode(pa, dstep, k_cache=dc.k_cache, v_cache=dc.v_cache)
+    ref = oracle_decode(step, k_cache=kc, v_cache=vc)
+    assert_close(out, ref, F16, F16, "tiny after append")
+    assert dc.debug_err.item() == 0 and dstep.debug_err.item() == 0
+
+
+SWEEP = [
+    # (group, Hkv, d, bs, dtype)
+    (1, 4, 128, 16, BF16), (2, 2, 64, 8, F16), (4, 2, 128, 32, BF16), (8, 1, 128, 64, F16),
+    (4, 8, 128, 16, F16), (2, 3, 256, 16, BF16), (8, 2, 64, 16, BF16), (1, 1, 64, 64, F16),
+    (4, 2, 256, 8, F16),
+]
+
+
+@pytest.mark.parametrize("group,Hkv,d,bs,dtype", SWEEP)
+def test_random_shapes(group, Hkv, d, bs, dtype):
+    seed = group * 10000 + Hkv * 1000 + d + bs
+    case = workloads.random_small_case(seed, num_seqs=7, group=group, num_kv_heads=Hkv,
+                                       head_dim=d, block_size=bs, dtype=dtype, max_ctx=700)
+    _check(case)
+
+
+@pytest.mark.parametrize("bs", [8, 16, 32, 64])
+def test_lengths_around_block_boundaries(bs):
+    lengths = [1, 2, bs - 1, bs, bs + 1, 2 * bs - 1, 2 * bs, 2 * bs + 1, 5 * bs + 3]
+    case = workloads.paged_case(500 + bs, lengths, 8, 2, 128, bs, BF16, name=f"edges{bs}")
+    _check(case)
+
+
+@pytest.mark.parametrize("partition_size", [16, 64, 512])
+@pytest.mark.parametrize("bs", [8, 16, 32])
+def test_split_path_matches_oracle_and_single_pass(partition_size, bs):
+    if partition_size % bs:
+        pytest.skip("partition must be a multiple of the block size")
+    lengths = [1, 15, 16, 17, 511, 512, 513, 1300, 2048]
+    case = workloads.paged_case(600 + bs, lengths, 16, 4, 128, bs, BF16, name="split")
+    (_, _), out_split, dc = _check(case, partition_size=partition_size)
+    out_single = run_decode(pa, dc, partition_size=0, workspace=False)
+    a, b = to_f64(out_split, BF16), to_f64(out_single, BF16)
+    # two float32 evaluation orders, each rounded to bf16: at most a couple of ulps apart
+    assert np.all(np.abs(a - b) <= 2 ** -7 * np.abs(b) + 1e-6)
+
+
+def test_empty_and_single_token_sequences():
+    lengths = [0, 1, 0, 3, 1]
+    case = workloads.paged_case(700, lengths, 4, 2, 64, 16, F16, name="empty")
+    (_, _), out, dc = _check(case)
+    got = to_f64(out, F16)
+    assert np.all(got[0] == 0) and np.all(got[2] == 0)
+    # a single token: the output is that token's value row, rounded to fp16
+    for i in (1, 4):
+        blk = case.block_tables[i, 0]
+        for h in range(4):
+            want = oracle.bits_to_f64(case.v_cache[blk, h // 2, 0], F16)
+            assert np.array_equal(got[i, h], want)
+
+
+def test_no_workspace_still_correct():
+    case = workloads.paged_case(701, [3000, 100, 4096], 32, 8, 128, 16, BF16, name="nows")
+    _check(case, workspace=False)
+
+
+def test_split_without_workspace_is_rejected():
+    case = workloads.paged_case(702, [100], 4, 2, 64, 16, F16)
+    dc = DeviceCase(case)
+    with pytest.raises(pa.PaError):
+        run_decode(pa, dc, partition_size=64, workspace=False)
+
+
+def test_physical_permutation_gives_bit_identical_output():
+    case = workloads.paged_case(703, [900, 37, 2000, 16], 32, 8, 128, 16, BF16, name="perm")
+    dc = DeviceCase(case)
+    out1 = run_decode(pa, dc)
+    rng = np.random.default_rng(0)
+    Nb2 = case.num_blocks + 33
+    new_id = rng.permutation(Nb2)[:case.num_blocks]
+    kc = np.full((Nb2,) + case.k_cache.shape[1:], workloads.NAN_BITS[BF16], np.uint16)
+    vc = kc.copy()
+    kc[new_id] = case.k_cache
+    vc[new_id] = case.v_cache
+    tables = torch.from_numpy(new_id[case.block_tables].astype(np.int32)).cuda()
+    out2 = run_decode(pa, dc, k_cache=dev(kc, BF16), v_cache=dev(vc, BF16), block_tables=tables)
+    torch.cuda.synchronize()
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+
+
+def test_shared_prefix_equals_private_copies_bit_identical():
+    case = workloads.shared_prefix(seed=7, num_seqs=6, prefix_len=300, suffix_lo=5, suffix_hi=90)
+    dc = DeviceCase(case)
+    pa.copy_blocks(pa.pointer_array([dc.k_cache], "cuda"), pa.pointer_array([dc.v_cache], "cuda"),
+                   dc.cow_pairs, case.num_blocks, 8 * 16 * 128 * 2)
+    pa.reshape_and_cache(dc.new_key, dc.new_value, dc.k_cache, dc.v_cache, dc.slot_mapping)
+    out_shared = run_decode(pa, dc)
+    # private copies of every shared prefix block, one set per sequence
+    kc, vc = host_bits(dc.k_cache), host_bits(dc.v_cache)
+    shared = case.meta["shared_blocks"][:-1]
+    extra_k, extra_v, tables = [], [], case.block_tables.copy()
+    for i in range(case.num_seqs):
+        for j, b in enumerate(shared):
+            tables[i, j] = kc.shape[0] + len(extra_k)
+            extra_k.append(kc[b])
+            extra_v.append(vc[b])
+    kc2 = np.concatenate([kc, np.stack(extra_k)])
+    vc2 = np.concatenate([vc, np.stack(extra_v)])
+    out_private = run_decode(pa, dc, k_cache=dev(kc2, F16), v_cache=dev(vc2, F16),
+                             block_tables=torch.from_numpy(tables).cuda())
+    torch.cuda.synchronize()
+    assert torch.equal(out_shared.view(torch.int16), out_private.view(torch.int16))
+    ref = oracle.paged_decode(case.q, kc, vc, case.block_tables, case.context_lens, case.scale,
+                              16, F16, F16)
+    assert_close(out_shared, ref, F16, F16, "shared prefix")
+
+
+def test_bad_table_entries_are_flagged_and_skipped():
+    case = workloads.paged_case(704, [40, 40], 4, 2, 64, 16, F16, name="badtable")
+    tables = case.block_tables.copy()
+    tables[0, 1] = case.num_blocks + 5   # out of range
+    tables[1, 0] = -3
+    dc = DeviceCase(case)
+    out = run_decode(pa, dc, block_tables=torch.from_numpy(tables).cuda())
+    torch.cuda.synchronize()
+    assert dc.debug_err.item() & pa.DEVERR_BLOCK_RANGE
+    assert torch.isfinite(out.float()).all()
+    # the result equals attention over the remaining blocks only
+    keep = case.context_lens.copy()
+    ref = np.zeros((2, 4, 64))
+    for i, drop in ((0, 1), (1, 0)):
+        for h in range(4):
+            rows_k, rows_v = [], []
+            for j in range(3):
+                if j == drop:
+                    continue
+                n = min(16, int(keep[i]) - 16 * j)
+                b = case.block_tables[i, j]
+                rows_k.append(oracle.bits_to_f64(case.k_cache[b, h // 2, :n], F16))
+                rows_v.append(oracle.bits_to_f64(case.v_cache[b, h // 2, :n], F16))
+            K, V = np.concatenate(rows_k), np.concatenate(rows_v)
+            s = case.scale * K @ oracle.bits_to_f64(case.q[i, h], F16)
+            w = np.exp(s - s.max())
+            ref[i, h] = w @ V / w.sum()
+    assert_close(out, ref, F16, F16, "skipped blocks")
+
+
+def test_context_above_bound_is_flagged_and_clamped():
+    case = workloads.paged_case(705, [64, 20], 4, 2, 64, 16, F16, name="clamp")
+    dc = DeviceCase(case)
+    ws = torch.empty(1, dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(dc.q)
+    pa.decode(out, dc.q, dc.k_cache, dc.v_cache, dc.block_tables, dc.context_lens, case.scale,
+              32, debug_err=dc.debug_err)
+    torch.cuda.synchronize()
+    assert dc.debug_err.item() & pa.DEVERR_CONTEXT_RANGE
+    ref = oracle_decode(case, context_lens=np.array([32, 20], np.int32))
+    assert_close(out, ref, F16, F16, "clamped")
+    del ws
+
+
+@pytest.mark.parametrize("q_dtype", [BF16, F16])
+@pytest.mark.parametrize("bs", [8, 16, 64])
+def test_fp8_kv_decode(q_dtype, bs):
+    lengths = [1, 7, 16, 33, 250, 777]
+    case = workloads.fp8_layer(800 + bs, lengths, num_heads=16, num_kv_heads=4, head_dim=128,
+                               block_size=bs, src_dtype=q_dtype, name=f"fp8_bs{bs}")
+    dc = DeviceCase(case)
+    pa.reshape_and_cache(dc.new_key, dc.new_value, dc.k_cache, dc.v_cache, dc.slot_mapping,
+                         k_scale=dc.k_scale, v_scale=dc.v_scale, debug_err=dc.debug_err)
+    kc, vc = case.k_cache.copy(), case.v_cache.copy()
+    oracle.reshape_and_cache(case.new_key, case.new_value, kc, vc, case.slot_mapping, bs, q_dtype,
+                             FP8_E4M3, case.k_scale, case.v_scale)
+    for part in (0, 64):
+        out = run_decode(pa, dc, partition_size=part)
+        ref = oracle_decode(case, k_cache=kc, v_cache=vc)
+        torch.cuda.synchronize()
+        assert_close(out, ref, q_dtype, FP8_E4M3, f"fp8 part={part}")
+    assert dc.debug_err.item() == 0
+    assert np.array_equal(host_bits(dc.k_cache), kc)

@@ -175,6 +175,42 @@ pa_status pa_copy_blocks(void* const* k_caches, void* const* v_caches,
                          size_t block_bytes, int32_t* debug_err,
                          cudaStream_t stream);
 
+/*
+ * pa_decode_split_noalloc - pa_decode's split-context path without a
+ * caller-provided workspace. (The source pages have no counterpart; this is
+ * an interface for callers, not a step of the method.)
+ *
+ * For callers that cannot allocate device memory: a plugin inside a host
+ * framework that owns every device allocation and gives its plugins none, or
+ * a runtime whose device memory is fixed at start-up (real-time and
+ * certified deployments forbid allocating afterwards). The partial
+ * results of the partitions go to a scratch array built into the library
+ * (16 MiB, a file-scope __device__ array that every GPU loading the library
+ * holds until the process exits). Nothing is allocated or freed by this call.
+ *
+ * Arguments and results are those of pa_decode with the split path forced
+ * (partition_size 0 means 512 tokens). Sizes whose partials would not fit
+ * the 16 MiB (pa_decode_workspace_size() above 16 MiB) are rejected with
+ * PA_ERR_WORKSPACE and a message giving both sizes.
+ *
+ * The first call on a device looks up the scratch array's device address
+ * (cudaGetSymbolAddress, with that device current) and keeps it; make that
+ * first call before any stream capture. All calls share the one array, which
+ * keeps the last call's contents: each call writes every partial it reads, so
+ * nothing needs clearing, but calls whose kernels overlap on the GPU (on
+ * different streams, or from different threads) race on the array and must
+ * be serialised by the caller.
+ */
+pa_status pa_decode_split_noalloc(void* out, const void* q, const void* k_cache,
+                                  const void* v_cache, const int32_t* block_tables,
+                                  int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                  int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                  float scale, pa_dtype q_dtype, pa_dtype kv_dtype,
+                                  const float* k_scale, const float* v_scale,
+                                  int32_t max_context_len, int32_t partition_size,
+                                  int32_t* debug_err, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

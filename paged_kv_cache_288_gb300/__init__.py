@@ -20,6 +20,7 @@ from ._binding import (
     reshape_and_cache,
     decode,
     decode_workspace_size,
+    decode_split_noalloc,
     copy_blocks,
     pointer_array,
 )
@@ -28,5 +29,5 @@ from .block_pool import BlockPool, OutOfBlocks
 __all__ = [
     "PaError", "F16", "BF16", "FP8_E4M3", "DEVERR_SLOT_RANGE", "DEVERR_BLOCK_RANGE",
     "DEVERR_CONTEXT_RANGE", "lib", "library_path", "reshape_and_cache", "decode",
-    "decode_workspace_size", "copy_blocks", "pointer_array", "BlockPool", "OutOfBlocks",
+    "decode_workspace_size", "decode_split_noalloc", "copy_blocks", "pointer_array", "BlockPool", "OutOfBlocks",
 ]

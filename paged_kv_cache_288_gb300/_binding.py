@@ -60,6 +60,11 @@ def lib():
             _c_ptr, _c_ptr, _c_int32, _c_int32, _c_ptr, _c_size, _c_ptr, _c_ptr]
         L.pa_decode_workspace_size.restype = _c_size
         L.pa_decode_workspace_size.argtypes = [_c_int32] * 6
+        L.pa_decode_split_noalloc.restype = ctypes.c_int
+        L.pa_decode_split_noalloc.argtypes = [
+            _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int32, _c_ptr, _c_int32, _c_int32,
+            _c_int32, _c_int32, _c_int32, _c_int32, ctypes.c_float, ctypes.c_int, ctypes.c_int,
+            _c_ptr, _c_ptr, _c_int32, _c_int32, _c_ptr, _c_ptr]
         L.pa_copy_blocks.restype = ctypes.c_int
         L.pa_copy_blocks.argtypes = [_c_ptr, _c_ptr, _c_int32, _c_ptr, _c_int32, _c_int32,
                                      _c_size, _c_ptr, _c_ptr]
@@ -139,6 +144,28 @@ def decode(out, q, k_cache, v_cache, block_tables, context_lens, scale, max_cont
         _dtype_code(q.dtype), _dtype_code(k_cache.dtype), _ptr(k_scale), _ptr(v_scale),
         int(max_context_len), int(partition_size), _ptr(workspace), ws_bytes, _ptr(debug_err),
         _stream(stream)), "pa_decode")
+
+
+def decode_split_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                         max_context_len, k_scale=None, v_scale=None, partition_size=0,
+                         debug_err=None, stream=None):
+    """Split-path decode whose partials live in the library's own scratch array.
+
+    For callers that cannot allocate device memory; see pa_decode_split_noalloc
+    in include/pa.h for the size limit and the rule that overlapping calls race.
+    """
+    B, Hq, d = q.shape
+    Nb, Hkv, bs, d2 = k_cache.shape
+    if d2 != d or out.shape != q.shape or v_cache.shape != k_cache.shape:
+        raise ValueError("shape mismatch")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise ValueError("block_tables and context_lens must be int32")
+    _check(lib().pa_decode_split_noalloc(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+        block_tables.shape[1], _ptr(context_lens), B, Hq, Hkv, d, bs, Nb, float(scale),
+        _dtype_code(q.dtype), _dtype_code(k_cache.dtype), _ptr(k_scale), _ptr(v_scale),
+        int(max_context_len), int(partition_size), _ptr(debug_err), _stream(stream)),
+        "pa_decode_split_noalloc")
 
 
 def pointer_array(tensors, device):

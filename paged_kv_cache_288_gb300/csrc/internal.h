@@ -14,6 +14,9 @@ struct DecodeParams;
 // Adds n to the process-wide count of kernels launched by this library.
 void note_launches(int n);
 
+// Sets the message pa_last_error_message() returns on this thread.
+void set_last_error(const char* fmt, ...);
+
 cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* k_cache,
                                      void* v_cache, const int64_t* slot_mapping, int num_tokens,
                                      int num_kv_heads, int head_dim, int block_size, int num_blocks,

@@ -16,6 +16,7 @@ F16, BF16, FP8_E4M3 = 0, 1, 2
 DEVERR_SLOT_RANGE = 0x1
 DEVERR_BLOCK_RANGE = 0x2
 DEVERR_CONTEXT_RANGE = 0x4
+DEVERR_TIMEOUT = 0x8
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libpa.so")

@@ -12,6 +12,7 @@
 // partial plus (m, l) and reduce_partitions_kernel merges them.
 #include "common.cuh"
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace pa {
 namespace {
@@ -193,6 +194,7 @@ decode_simt_kernel(const DecodeParams p) {
 // w_p = 2^(m_p - M) * l_p, out = sum_p w_p * o_p / sum_p w_p.
 template <typename QT, int D>
 __global__ void __launch_bounds__(128) reduce_partitions_kernel(const DecodeParams p) {
+  griddep_wait();
   const int h = blockIdx.x;
   const int seq = blockIdx.y;
   const int ctx = clamp_context(p, seq);
@@ -249,6 +251,23 @@ cudaError_t launch_d(const DecodeParams& p, int group, cudaStream_t stream) {
   return err;
 }
 
+template <typename QT, int D>
+cudaError_t launch_reduce_pdl(const DecodeParams& p, bool pdl, cudaStream_t stream) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.num_heads, p.num_seqs);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = p.num_partitions * sizeof(float);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  cudaError_t err = cudaLaunchKernelEx(&cfg, reduce_partitions_kernel<QT, D>, p);
+  if (err == cudaSuccess) note_launches(1);
+  return err;
+}
+
 template <typename QT, typename KT>
 cudaError_t launch_t(const DecodeParams& p, int head_dim, int group, cudaStream_t stream) {
   switch (head_dim) {
@@ -260,6 +279,17 @@ cudaError_t launch_t(const DecodeParams& p, int head_dim, int group, cudaStream_
 }
 
 }  // namespace
+
+cudaError_t launch_reduce_partitions(const DecodeParams& p, int head_dim, pa_dtype q_dtype,
+                                     bool pdl, cudaStream_t stream) {
+  const bool b = q_dtype == PA_BF16;
+  switch (head_dim) {
+    case 64: return b ? launch_reduce_pdl<bf16, 64>(p, pdl, stream) : launch_reduce_pdl<f16, 64>(p, pdl, stream);
+    case 128: return b ? launch_reduce_pdl<bf16, 128>(p, pdl, stream) : launch_reduce_pdl<f16, 128>(p, pdl, stream);
+    case 256: return b ? launch_reduce_pdl<bf16, 256>(p, pdl, stream) : launch_reduce_pdl<f16, 256>(p, pdl, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
 
 cudaError_t launch_decode_simt(const DecodeParams& p, int head_dim, pa_dtype q_dtype,
                                pa_dtype kv_dtype, cudaStream_t stream) {

@@ -1,0 +1,838 @@
+// Paged decode on the tensor cores, for GQA groups of 2, 4 or 8 query heads.
+//
+// Work. The context of every (sequence, KV head) is cut into 16-token tiles;
+// all tiles of the batch form one flat list ordered (sequence, KV head,
+// tile). Each warp of a persistent grid (8 warps per CTA, one CTA per SM)
+// takes an equal contiguous share of that list, so every warp streams the
+// same number of KV bytes whatever the mix of context lengths. A warp's share
+// is a run of "pieces", one per (sequence, KV head) it touches; only the
+// first and last piece can be partial. A warp that holds a whole (sequence,
+// KV head) writes its output rows; partial pieces leave their online-softmax
+// state (running max, running sum, unnormalised accumulator) in the
+// workspace and tc_merge_kernel combines them. With a forced partition size
+// the list is cut at partition boundaries instead, every piece is one whole
+// partition, and the partition reduce of the split path combines them.
+//
+// Data movement. Each warp owns a ring of shared-memory slots, one 16-token
+// K tile plus V tile per slot. It fetches its own tiles with 3-D TMA loads
+// (box = 128 bytes of a row x up to 16 rows of one block of one KV head, 128B
+// swizzle), completing on one mbarrier per slot, and runs as many tiles ahead
+// as it has slots. Physical block ids come from the block table through a
+// 32-entry window held one entry per lane.
+//
+// Math. With G query heads per KV head, S^T = K Q^T is a 16x16 by 16x8
+// product per 16 d-columns (tokens in M, heads in N, G of the 8 columns
+// used), issued as mma.sync m16n8k16 with float accumulators; P^T is moved
+// from the accumulator layout into the B-operand layout with movmatrix; then
+// O^T = V^T P^T, again m16n8k16, with V^T fragments read by ldmatrix.trans.
+// The online softmax runs in log2 units on the accumulator fragments. E4M3
+// tiles are widened to f16 in registers (K through a consistent permutation
+// of the contraction index, V through one of the d rows) and their block
+// scales are applied to S and to P.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <type_traits>
+
+#include "common.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace pa {
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kTile = 16;      // tokens per tile = MMA M
+constexpr int kMaxG = 8;       // MMA N
+constexpr uint32_t kFull = 0xffffffffu;
+
+template <typename KT, int D>
+struct Geom {
+  static constexpr int kElem = int(sizeof(KT));
+  static constexpr int kRowBytes = D * kElem;
+  static constexpr int kBoxW = 128 / kElem;        // elements in one 128-byte box row
+  static constexpr int kBoxes = kRowBytes / 128;   // boxes across a row
+  static constexpr int kTileBytes = kTile * kRowBytes;
+  static constexpr int kSlotBytes = 2 * kTileBytes;
+  static constexpr int kSlots = kSlotBytes >= 8192 ? 3 : 6;
+  static constexpr int kSteps = D / 16;            // 16-column steps of QK^T and PV
+};
+
+struct SlotMeta {
+  uint32_t mask;  // bit t: token t of the tile holds data
+  float ks0, ks1; // E4M3 K scale of tokens 0-7 and 8-15
+  float vs0, vs1; // E4M3 V scale
+  uint32_t pad[3];
+};
+
+struct TcParams {
+  DecodeParams p;
+  int32_t* ws_prefix;  // [num_seqs + 1] tile prefix, written by CTA 0 (auto schedule)
+  float* ws_slots;     // [2 * num_warps][kMaxG * (D + 2)] partial states (auto schedule)
+  int32_t num_warps;   // warps that share the work
+  int32_t part_tiles;  // tiles per partition (split path); 0 = auto schedule
+  int32_t group;       // query heads per KV head
+};
+
+// Byte address of 16-byte chunk `chunk` of row `row` in a tile: 128-byte boxes
+// of 16 rows (8-row boxes stack to the same layout), chunks XOR-swizzled by
+// row % 8 as the TMA 128B swizzle stores them.
+__device__ __forceinline__ uint32_t tile_addr(uint32_t base, int row, int chunk) {
+  return base + (chunk >> 3) * 2048 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+  __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes & 0xffffu),
+                                             __NV_E4M3);
+  return static_cast<uint32_t>(r.x) | (static_cast<uint32_t>(r.y) << 16);
+}
+
+// Keep the 16-bit halves of a (token t, token t+1) register whose token holds data.
+__device__ __forceinline__ uint32_t keep_tokens(uint32_t v, uint32_t mask, int t) {
+  const uint32_t lo = (mask >> t) & 1u ? 0x0000ffffu : 0u;
+  const uint32_t hi = (mask >> (t + 1)) & 1u ? 0xffff0000u : 0u;
+  return v & (lo | hi);
+}
+
+// Position in the flat tile list, walked tile by tile.
+struct Cursor {
+  int64_t f;  // flat index
+  int seq, kvh, t, tiles;
+};
+
+__device__ __forceinline__ int find_seq(const int* pref, int B, int Hkv, int64_t f) {
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (static_cast<int64_t>(pref[mid]) * Hkv <= f) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ void cursor_at(Cursor& c, int64_t f, const int* prefT, int B, int Hkv) {
+  c.f = f;
+  c.seq = find_seq(prefT, B, Hkv, f);
+  c.tiles = prefT[c.seq + 1] - prefT[c.seq];
+  const int64_t r = f - static_cast<int64_t>(prefT[c.seq]) * Hkv;
+  c.kvh = static_cast<int>(r / c.tiles);
+  c.t = static_cast<int>(r % c.tiles);
+}
+
+__device__ __forceinline__ void cursor_next(Cursor& c, const int* prefT, int B, int Hkv) {
+  ++c.f;
+  if (++c.t < c.tiles) return;
+  c.t = 0;
+  if (++c.kvh < Hkv) return;
+  c.kvh = 0;
+  do {
+    ++c.seq;
+  } while (c.seq < B && prefT[c.seq + 1] == prefT[c.seq]);
+  if (c.seq < B) c.tiles = prefT[c.seq + 1] - prefT[c.seq];
+}
+
+template <typename QT, typename KT, int D>
+__global__ void __launch_bounds__(kThreads, 1)
+decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                 const __grid_constant__ CUtensorMap tmap_v, const TcParams tp) {
+  using Gm = Geom<KT, D>;
+  constexpr bool kFp8 = is_fp8<KT>::value;
+  constexpr int NS = Gm::kSlots;
+  const DecodeParams& p = tp.p;
+  const int B = p.num_seqs;
+  const int Hkv = p.num_kv_heads;
+  const int G = tp.group;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2;   // MMA group id: accumulator row, B-operand column
+  const int tig = lane & 3;  // thread in group
+
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* slots = smem;
+  SlotMeta* meta = reinterpret_cast<SlotMeta*>(slots + kWarps * NS * Gm::kSlotBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(meta + kWarps * NS);
+  int* s_ctx = reinterpret_cast<int*>(bars + kWarps * NS);
+  int* s_prefT = s_ctx + B;
+  int* s_prefP = s_prefT + B + 1;
+  __shared__ int s_warp_sum[kWarps][2];
+
+  if (threadIdx.x < kWarps * NS) mbar_init(smem_u32(&bars[threadIdx.x]), 1);
+  mbar_init_fence();
+  griddep_wait();
+
+  // ---- per-sequence tile and partition counts, and their exclusive prefix --
+  const int per = (B + kThreads - 1) / kThreads;
+  const int i0 = min(B, static_cast<int>(threadIdx.x) * per);
+  const int i1 = min(B, i0 + per);
+  int sum_t = 0, sum_p = 0;
+  for (int i = i0; i < i1; ++i) {
+    const int ctx = clamp_context(p, i);
+    s_ctx[i] = ctx;
+    const int tl = (ctx + kTile - 1) / kTile;
+    sum_t += tl;
+    if (tp.part_tiles) sum_p += (tl + tp.part_tiles - 1) / tp.part_tiles;
+  }
+  int inc_t = sum_t, inc_p = sum_p;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int a = __shfl_up_sync(kFull, inc_t, off);
+    const int b = __shfl_up_sync(kFull, inc_p, off);
+    if (lane >= off) {
+      inc_t += a;
+      inc_p += b;
+    }
+  }
+  if (lane == 31) {
+    s_warp_sum[warp][0] = inc_t;
+    s_warp_sum[warp][1] = inc_p;
+  }
+  __syncthreads();
+  int run_t = inc_t - sum_t, run_p = inc_p - sum_p;
+  for (int w = 0; w < warp; ++w) {
+    run_t += s_warp_sum[w][0];
+    run_p += s_warp_sum[w][1];
+  }
+  for (int i = i0; i < i1; ++i) {
+    s_prefT[i] = run_t;
+    s_prefP[i] = run_p;
+    const int tl = (s_ctx[i] + kTile - 1) / kTile;
+    run_t += tl;
+    if (tp.part_tiles) run_p += (tl + tp.part_tiles - 1) / tp.part_tiles;
+  }
+  if (threadIdx.x == kThreads - 1) {
+    s_prefT[B] = run_t;
+    s_prefP[B] = run_p;
+  }
+  __syncthreads();
+  if (blockIdx.x == 0 && tp.ws_prefix != nullptr)
+    for (int i = threadIdx.x; i <= B; i += kThreads) tp.ws_prefix[i] = s_prefT[i];
+  griddep_launch_dependents();
+
+  // ---- this warp's share of the tile list --------------------------------
+  const int64_t W = tp.num_warps;
+  const int64_t wid = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
+  if (wid >= W) return;
+  const int64_t U = static_cast<int64_t>(s_prefT[B]) * Hkv;
+  int64_t f0, f1;
+  if (tp.part_tiles == 0) {
+    f0 = wid * U / W;
+    f1 = (wid + 1) * U / W;
+  } else {
+    // whole partitions: convert partition indices to tile indices
+    const int64_t US = static_cast<int64_t>(s_prefP[B]) * Hkv;
+    auto part_to_tile = [&](int64_t s) -> int64_t {
+      if (s >= US) return U;
+      const int seq = find_seq(s_prefP, B, Hkv, s);
+      const int np = s_prefP[seq + 1] - s_prefP[seq];
+      const int64_t r = s - static_cast<int64_t>(s_prefP[seq]) * Hkv;
+      const int kvh = static_cast<int>(r / np);
+      const int pi = static_cast<int>(r % np);
+      const int tiles = s_prefT[seq + 1] - s_prefT[seq];
+      return static_cast<int64_t>(s_prefT[seq]) * Hkv + static_cast<int64_t>(kvh) * tiles +
+             static_cast<int64_t>(pi) * tp.part_tiles;
+    };
+    f0 = part_to_tile(wid * US / W);
+    f1 = part_to_tile((wid + 1) * US / W);
+  }
+  if (f0 >= f1) return;
+
+  const int bs = p.block_size;
+  const int width = p.max_blocks_per_seq;
+  const int Hq = p.num_heads;
+  const uint32_t slot_base0 = smem_u32(slots) + warp * NS * Gm::kSlotBytes;
+  SlotMeta* my_meta = meta + warp * NS;
+  const uint32_t bar_base = smem_u32(bars + warp * NS);
+
+  // block-table window: lane l holds entry win_base + l of sequence win_seq
+  int win_seq = -1, win_base = 0, win_val = -1;
+  auto table_entry = [&](int seq, int j) -> int {
+    if (seq != win_seq || j < win_base || j >= win_base + 32) {
+      win_seq = seq;
+      win_base = j;
+      const int jj = j + lane;
+      win_val = jj < width ? p.block_tables[static_cast<int64_t>(seq) * width + jj] : -1;
+    }
+    return __shfl_sync(kFull, win_val, j - win_base);
+  };
+
+  // Issue the TMA loads of the tile under `c` into slot `s` (whole warp).
+  auto issue = [&](const Cursor& c, int s) {
+    const int ctx = s_ctx[c.seq];
+    const int tok0 = c.t * kTile;
+    const int valid = min(kTile, ctx - tok0);
+    const uint32_t kdst = slot_base0 + s * Gm::kSlotBytes;
+    const uint32_t vdst = kdst + Gm::kTileBytes;
+    const uint32_t bar = bar_base + s * 8;
+    uint32_t mask = 0, tx = 0;
+    int phys[2] = {-1, -1};
+    int rows[2] = {0, 0};
+    int off[2] = {0, 0};
+    if (bs >= kTile) {
+      phys[0] = table_entry(c.seq, tok0 / bs);
+      rows[0] = kTile;
+      off[0] = tok0 % bs;
+    } else {  // block size 8: two blocks per tile
+      phys[0] = table_entry(c.seq, tok0 / bs);
+      rows[0] = bs;
+      if (valid > bs) {
+        phys[1] = table_entry(c.seq, tok0 / bs + 1);
+        rows[1] = bs;
+      }
+    }
+    float ks[2] = {1.f, 1.f}, vs[2] = {1.f, 1.f};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      if (rows[h] == 0) continue;
+      const int first = h * bs;  // first token of this half in the tile
+      const int nvalid = min(rows[h], valid - first);
+      if (phys[h] < 0 || phys[h] >= p.num_blocks) {
+        if (lane == 0) flag_error(p.debug_err, PA_DEVERR_BLOCK_RANGE);
+        phys[h] = -1;
+        continue;
+      }
+      mask |= ((1u << nvalid) - 1u) << first;
+      tx += 2u * rows[h] * Gm::kRowBytes;
+      if constexpr (kFp8) {
+        const int64_t si = static_cast<int64_t>(phys[h]) * Hkv + c.kvh;
+        ks[h] = p.k_scale[si];
+        vs[h] = p.v_scale[si];
+      }
+    }
+    if (lane == 0) {
+      SlotMeta& m = my_meta[s];
+      m.mask = mask;
+      m.ks0 = ks[0];
+      m.vs0 = vs[0];
+      m.ks1 = (bs >= kTile) ? ks[0] : ks[1];
+      m.vs1 = (bs >= kTile) ? vs[0] : vs[1];
+      mbar_arrive_expect_tx(bar, tx);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (phys[h] < 0) continue;
+        const int z = phys[h] * Hkv + c.kvh;
+        const uint32_t half = h * bs * 128;  // 8-row boxes of the second block sit after the first
+#pragma unroll
+        for (int b = 0; b < Gm::kBoxes; ++b) {
+          tma_load_3d(kdst + b * 2048 + half, &tmap_k, b * Gm::kBoxW, off[h], z, bar);
+          tma_load_3d(vdst + b * 2048 + half, &tmap_v, b * Gm::kBoxW, off[h], z, bar);
+        }
+      }
+    }
+  };
+
+  // q of one (sequence, KV head) as MMA B fragments: column g = query head
+  // kvh*G + g (zero for g >= G); 16-bit caches contract d in order, E4M3
+  // caches in the permuted order their K fragments arrive in.
+  uint32_t qb[Gm::kSteps][2];
+  auto load_q = [&](int seq, int kvh) {
+    const QT* qrow = static_cast<const QT*>(p.q) + (static_cast<int64_t>(seq) * Hq + kvh * G + g) * D;
+#pragma unroll
+    for (int k = 0; k < Gm::kSteps; ++k) {
+      if (g >= G) {
+        qb[k][0] = qb[k][1] = 0u;
+      } else if constexpr (!kFp8) {
+        qb[k][0] = *reinterpret_cast<const uint32_t*>(qrow + 16 * k + 2 * tig);
+        qb[k][1] = *reinterpret_cast<const uint32_t*>(qrow + 16 * k + 8 + 2 * tig);
+      } else {
+        float f[4];
+        load_float<QT, 4>(qrow + 16 * k + 4 * tig, f);
+        qb[k][0] = pack_f16(f[0], f[1]);
+        qb[k][1] = pack_f16(f[2], f[3]);
+      }
+    }
+  };
+
+  // online-softmax state of the current piece: this lane's two heads
+  // (columns 2*tig, 2*tig+1) and its 16 d rows per 16-row step
+  float m0, m1, l0, l1;
+  float o[Gm::kSteps][4];
+  auto reset = [&]() {
+    m0 = m1 = -INFINITY;
+    l0 = l1 = 0.f;
+#pragma unroll
+    for (int k = 0; k < Gm::kSteps; ++k) o[k][0] = o[k][1] = o[k][2] = o[k][3] = 0.f;
+  };
+
+  // d index held in accumulator row r (0..15) of 16-row step k
+  auto d_of = [&](int k, int upper) -> int {
+    if constexpr (kFp8) return 16 * k + 2 * g + upper;
+    else return 16 * k + g + 8 * upper;
+  };
+
+  // Write the finished piece: output rows, a partition partial, or a
+  // per-warp partial state for the merge.
+  auto flush = [&](int seq, int kvh, int part, bool whole, int64_t slot_index) {
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l0 += __shfl_xor_sync(kFull, l0, off);
+      l1 += __shfl_xor_sync(kFull, l1, off);
+    }
+    const int h0 = 2 * tig, h1 = 2 * tig + 1;
+    if (whole && tp.part_tiles == 0) {
+      QT* out = static_cast<QT*>(p.out);
+      const float i0 = l0 > 0.f ? 1.f / l0 : 0.f;
+      const float i1 = l1 > 0.f ? 1.f / l1 : 0.f;
+      QT* r0 = out + (static_cast<int64_t>(seq) * Hq + kvh * G + h0) * D;
+      QT* r1 = r0 + D;
+#pragma unroll
+      for (int k = 0; k < Gm::kSteps; ++k) {
+        if constexpr (kFp8) {
+          // rows d and d+1 are adjacent: one 32-bit store per head
+          const int d = d_of(k, 0);
+          if (h0 < G) {
+            if constexpr (std::is_same<QT, bf16>::value)
+              *reinterpret_cast<uint32_t*>(r0 + d) = pack_bf16(o[k][0] * i0, o[k][2] * i0);
+            else
+              *reinterpret_cast<uint32_t*>(r0 + d) = pack_f16(o[k][0] * i0, o[k][2] * i0);
+          }
+          if (h1 < G) {
+            if constexpr (std::is_same<QT, bf16>::value)
+              *reinterpret_cast<uint32_t*>(r1 + d) = pack_bf16(o[k][1] * i1, o[k][3] * i1);
+            else
+              *reinterpret_cast<uint32_t*>(r1 + d) = pack_f16(o[k][1] * i1, o[k][3] * i1);
+          }
+        } else {
+          const int da = d_of(k, 0), db = d_of(k, 1);
+          if (h0 < G) {
+            r0[da] = from_float(o[k][0] * i0, static_cast<QT*>(nullptr));
+            r0[db] = from_float(o[k][2] * i0, static_cast<QT*>(nullptr));
+          }
+          if (h1 < G) {
+            r1[da] = from_float(o[k][1] * i1, static_cast<QT*>(nullptr));
+            r1[db] = from_float(o[k][3] * i1, static_cast<QT*>(nullptr));
+          }
+        }
+      }
+    } else if (tp.part_tiles != 0) {
+      // one whole partition: normalised partial plus (max, sum) for the reduce
+      const int NP = p.num_partitions;
+      const float i0 = l0 > 0.f ? 1.f / l0 : 0.f;
+      const float i1 = l1 > 0.f ? 1.f / l1 : 0.f;
+      const int64_t s0 = (static_cast<int64_t>(seq) * Hq + kvh * G + h0) * NP + part;
+      const int64_t s1 = s0 + NP;
+#pragma unroll
+      for (int k = 0; k < Gm::kSteps; ++k) {
+        const int da = d_of(k, 0), db = d_of(k, 1);
+        if (h0 < G) {
+          p.ws_acc[s0 * D + da] = o[k][0] * i0;
+          p.ws_acc[s0 * D + db] = o[k][2] * i0;
+        }
+        if (h1 < G) {
+          p.ws_acc[s1 * D + da] = o[k][1] * i1;
+          p.ws_acc[s1 * D + db] = o[k][3] * i1;
+        }
+      }
+      if (g == 0) {
+        if (h0 < G) {
+          p.ws_ml[s0 * 2] = m0;
+          p.ws_ml[s0 * 2 + 1] = l0;
+        }
+        if (h1 < G) {
+          p.ws_ml[s1 * 2] = m1;
+          p.ws_ml[s1 * 2 + 1] = l1;
+        }
+      }
+    } else {
+      // part of a (sequence, KV head) shared with other warps
+      float* base = tp.ws_slots + slot_index * (kMaxG * (D + 2));
+#pragma unroll
+      for (int k = 0; k < Gm::kSteps; ++k) {
+        const int da = d_of(k, 0), db = d_of(k, 1);
+        if (h0 < G) {
+          base[h0 * D + da] = o[k][0];
+          base[h0 * D + db] = o[k][2];
+        }
+        if (h1 < G) {
+          base[h1 * D + da] = o[k][1];
+          base[h1 * D + db] = o[k][3];
+        }
+      }
+      if (g == 0) {
+        if (h0 < G) {
+          base[kMaxG * D + h0] = m0;
+          base[kMaxG * D + kMaxG + h0] = l0;
+        }
+        if (h1 < G) {
+          base[kMaxG * D + h1] = m1;
+          base[kMaxG * D + kMaxG + h1] = l1;
+        }
+      }
+    }
+  };
+
+  // ---- the warp's pipeline ----------------------------------------------
+  Cursor pc, cc;
+  cursor_at(pc, f0, s_prefT, B, Hkv);
+  cc = pc;
+  int pending = 0;
+  for (int s = 0; s < NS && pc.f < f1; ++s) {
+    issue(pc, s);
+    cursor_next(pc, s_prefT, B, Hkv);
+    ++pending;
+  }
+  load_q(cc.seq, cc.kvh);
+  reset();
+  int piece_t0 = cc.t;
+  bool first_piece = true;
+  uint32_t parity = 0;
+  int s = 0;
+  while (cc.f < f1) {
+    const bool ok = mbar_wait_bounded(bar_base + s * 8, (parity >> s) & 1u);
+    if (!__all_sync(kFull, ok)) {
+      if (lane == 0) flag_error(p.debug_err, PA_DEVERR_TIMEOUT);
+      // give copies still in flight a short while to land, then leave
+      for (int q = 0; q < NS; ++q) mbar_wait_bounded(bar_base + q * 8, (parity >> q) & 1u, 10000000ull);
+      return;
+    }
+    parity ^= 1u << s;
+    --pending;
+    const SlotMeta mt = my_meta[s];
+    const uint32_t kbase = slot_base0 + s * Gm::kSlotBytes;
+    const uint32_t vbase = kbase + Gm::kTileBytes;
+
+    // S^T = K Q^T: rows = the tile's 16 tokens, columns = query heads
+    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+    if constexpr (!kFp8) {
+#pragma unroll
+      for (int k = 0; k < Gm::kSteps; ++k) {
+        uint32_t a[4];
+        ldsm_x4(tile_addr(kbase, lane & 15, 2 * k + (lane >> 4)), a[0], a[1], a[2], a[3]);
+        if constexpr (std::is_same<KT, bf16>::value) mma_bf16((k & 1) ? sb : sa, a, qb[k][0], qb[k][1]);
+        else mma_f16((k & 1) ? sb : sa, a, qb[k][0], qb[k][1]);
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < Gm::kSteps; k += 2) {
+        uint32_t r[4];
+        ldsm_x4(tile_addr(kbase, lane & 15, k + (lane >> 4)), r[0], r[1], r[2], r[3]);
+        const uint32_t a0[4] = {e4m3x2_to_f16x2(r[0]), e4m3x2_to_f16x2(r[1]),
+                                e4m3x2_to_f16x2(r[0] >> 16), e4m3x2_to_f16x2(r[1] >> 16)};
+        const uint32_t a1[4] = {e4m3x2_to_f16x2(r[2]), e4m3x2_to_f16x2(r[3]),
+                                e4m3x2_to_f16x2(r[2] >> 16), e4m3x2_to_f16x2(r[3] >> 16)};
+        mma_f16(sa, a0, qb[k][0], qb[k][1]);
+        mma_f16(sb, a1, qb[k + 1][0], qb[k + 1][1]);
+      }
+    }
+    const float sc0 = p.scale_log2 * mt.ks0, sc1 = p.scale_log2 * mt.ks1;
+    float s0 = (sa[0] + sb[0]) * sc0, s1 = (sa[1] + sb[1]) * sc0;
+    float s2 = (sa[2] + sb[2]) * sc1, s3 = (sa[3] + sb[3]) * sc1;
+    const uint32_t mask = mt.mask;
+    if (!((mask >> g) & 1u)) s0 = s1 = -INFINITY;
+    if (!((mask >> (g + 8)) & 1u)) s2 = s3 = -INFINITY;
+
+    // online softmax (log2 units), per head column
+    float x0 = fmaxf(s0, s2), x1 = fmaxf(s1, s3);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      x0 = fmaxf(x0, __shfl_xor_sync(kFull, x0, off));
+      x1 = fmaxf(x1, __shfl_xor_sync(kFull, x1, off));
+    }
+    const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
+    if (__any_sync(kFull, n0 > m0 || n1 > m1)) {
+      const float a0 = exp2f(m0 - n0), a1 = exp2f(m1 - n1);  // 0 while m is -inf
+      m0 = n0;
+      m1 = n1;
+      l0 *= a0;
+      l1 *= a1;
+#pragma unroll
+      for (int k = 0; k < Gm::kSteps; ++k) {
+        o[k][0] *= a0;
+        o[k][1] *= a1;
+        o[k][2] *= a0;
+        o[k][3] *= a1;
+      }
+    }
+    const float b0 = m0 == -INFINITY ? 0.f : m0, b1 = m1 == -INFINITY ? 0.f : m1;
+    const float p0 = exp2f(s0 - b0), p1 = exp2f(s1 - b1);
+    const float p2 = exp2f(s2 - b0), p3 = exp2f(s3 - b1);
+    l0 += p0 + p2;
+    l1 += p1 + p3;
+
+    // P^T as the B operand: transpose the accumulator-layout rows
+    uint32_t pb0, pb1;
+    if constexpr (std::is_same<KT, bf16>::value) {
+      pb0 = movmatrix_trans(pack_bf16(p0, p1));
+      pb1 = movmatrix_trans(pack_bf16(p2, p3));
+    } else if constexpr (!kFp8) {
+      pb0 = movmatrix_trans(pack_f16(p0, p1));
+      pb1 = movmatrix_trans(pack_f16(p2, p3));
+    } else {
+      pb0 = movmatrix_trans(pack_f16(p0 * mt.vs0, p1 * mt.vs0));
+      pb1 = movmatrix_trans(pack_f16(p2 * mt.vs1, p3 * mt.vs1));
+    }
+
+    // O^T += V^T P^T, one 16-row step of d at a time
+    const bool partial = mask != 0xffffu;
+    if constexpr (!kFp8) {
+#pragma unroll
+      for (int k = 0; k < Gm::kSteps; ++k) {
+        uint32_t a[4];
+        ldsm_x4_trans(tile_addr(vbase, (lane & 7) + ((lane >> 4) << 3), 2 * k + ((lane >> 3) & 1)),
+                      a[0], a[1], a[2], a[3]);
+        if (partial) {
+          a[0] = keep_tokens(a[0], mask, 2 * tig);
+          a[1] = keep_tokens(a[1], mask, 2 * tig);
+          a[2] = keep_tokens(a[2], mask, 2 * tig + 8);
+          a[3] = keep_tokens(a[3], mask, 2 * tig + 8);
+        }
+        if constexpr (std::is_same<KT, bf16>::value) mma_bf16(o[k], a, pb0, pb1);
+        else mma_f16(o[k], a, pb0, pb1);
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < Gm::kSteps; k += 2) {
+        uint32_t r[4];
+        ldsm_x4_trans(tile_addr(vbase, lane & 15, k + (lane >> 4)), r[0], r[1], r[2], r[3]);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t lo = r[2 * h], hi = r[2 * h + 1];  // tokens 0-7 / 8-15 of chunk k+h
+          uint32_t a[4] = {e4m3x2_to_f16x2(__byte_perm(lo, 0, 0x0020)),
+                           e4m3x2_to_f16x2(__byte_perm(lo, 0, 0x0031)),
+                           e4m3x2_to_f16x2(__byte_perm(hi, 0, 0x0020)),
+                           e4m3x2_to_f16x2(__byte_perm(hi, 0, 0x0031))};
+          if (partial) {
+            a[0] = keep_tokens(a[0], mask, 2 * tig);
+            a[1] = keep_tokens(a[1], mask, 2 * tig);
+            a[2] = keep_tokens(a[2], mask, 2 * tig + 8);
+            a[3] = keep_tokens(a[3], mask, 2 * tig + 8);
+          }
+          mma_f16(o[k + h], a, pb0, pb1);
+        }
+      }
+    }
+
+    // the slot is free again: refill it with the tile NS ahead
+    __syncwarp();
+    fence_proxy_async_smem();
+    if (pc.f < f1) {
+      issue(pc, s);
+      cursor_next(pc, s_prefT, B, Hkv);
+      ++pending;
+    }
+    s = (s + 1 == NS) ? 0 : s + 1;
+
+    // end of a piece?
+    const int seq = cc.seq, kvh = cc.kvh, t = cc.t, tiles = cc.tiles;
+    cursor_next(cc, s_prefT, B, Hkv);
+    const bool new_segment = cc.t == 0 || (tp.part_tiles != 0 && cc.t % tp.part_tiles == 0);
+    if (cc.f == f1 || new_segment) {
+      const int seg_t0 = tp.part_tiles ? (t / tp.part_tiles) * tp.part_tiles : 0;
+      const int seg_t1 = tp.part_tiles ? min(tiles, seg_t0 + tp.part_tiles) : tiles;
+      const bool whole = piece_t0 == seg_t0 && t + 1 == seg_t1;
+      flush(seq, kvh, tp.part_tiles ? t / tp.part_tiles : 0, whole, first_piece ? 2 * wid : 2 * wid + 1);
+      first_piece = false;
+      if (cc.f < f1) {
+        reset();
+        piece_t0 = cc.t;
+        if (cc.seq != seq || cc.kvh != kvh) load_q(cc.seq, cc.kvh);
+      }
+    }
+  }
+  (void)pending;
+}
+
+// Combine the partial states of every (sequence, KV head) that several warps
+// shared: with M = max_c m_c, out = sum_c 2^(m_c-M) acc_c / sum_c 2^(m_c-M) l_c.
+// Sequences with no context get zero rows here.
+template <typename QT, int D>
+__global__ void __launch_bounds__(128) tc_merge_kernel(const TcParams tp) {
+  griddep_wait();
+  const DecodeParams& p = tp.p;
+  const int kvh = blockIdx.x;
+  const int seq = blockIdx.y;
+  const int G = tp.group;
+  const int Hkv = p.num_kv_heads;
+  const int B = p.num_seqs;
+  QT* out = static_cast<QT*>(p.out) + (static_cast<int64_t>(seq) * p.num_heads + kvh * G) * D;
+  const int tiles = tp.ws_prefix[seq + 1] - tp.ws_prefix[seq];
+  if (tiles == 0) {
+    for (int i = threadIdx.x; i < G * D; i += blockDim.x) out[i] = from_float(0.f, static_cast<QT*>(nullptr));
+    return;
+  }
+  const int64_t U = static_cast<int64_t>(tp.ws_prefix[B]) * Hkv;
+  const int64_t W = tp.num_warps;
+  const int64_t seg0 = static_cast<int64_t>(tp.ws_prefix[seq]) * Hkv + static_cast<int64_t>(kvh) * tiles;
+  const int64_t seg1 = seg0 + tiles;
+  auto owner = [&](int64_t x) { return ((x + 1) * W - 1) / U; };
+  const int64_t w0 = owner(seg0), w1 = owner(seg1 - 1);
+  if (w0 == w1) return;  // one warp held it and wrote the rows
+  const float* slots = tp.ws_slots;
+  const int stride = kMaxG * (D + 2);
+  // warp w holds [w*U/W, (w+1)*U/W); warps whose range is empty wrote nothing
+  auto start = [&](int64_t w) { return w * U / W; };
+  auto slot_of = [&](int64_t w) -> int64_t {
+    return (w == w0 && start(w0) < seg0) ? 2 * w0 + 1 : 2 * w;
+  };
+  for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
+    const int h = i / D;
+    float mx = -INFINITY;
+    for (int64_t w = w0; w <= w1; ++w) {
+      if (start(w) == start(w + 1)) continue;
+      mx = fmaxf(mx, slots[slot_of(w) * stride + kMaxG * D + h]);
+    }
+    float num = 0.f, den = 0.f;
+    if (mx != -INFINITY) {
+      for (int64_t w = w0; w <= w1; ++w) {
+        if (start(w) == start(w + 1)) continue;
+        const int64_t sl = slot_of(w);
+        const float f = exp2f(slots[sl * stride + kMaxG * D + h] - mx);
+        den += f * slots[sl * stride + kMaxG * D + kMaxG + h];
+        num += f * slots[sl * stride + i];
+      }
+    }
+    out[i] = from_float(den > 0.f ? num / den : 0.f, static_cast<QT*>(nullptr));
+  }
+}
+
+// ---- host side ----------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    cudaDriverEntryPointQueryResult q;
+    void* ptr = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// 3-D view of a cache: (d, token in block, block x KV head), boxes of 128
+// bytes x min(block_size, 16) rows x 1, 128-byte swizzle.
+bool make_cache_map(CUtensorMap* map, const void* base, int head_dim, int elem, int block_size,
+                    int64_t blocks_x_heads) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(block_size),
+                        static_cast<cuuint64_t>(blocks_x_heads)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * elem,
+                           static_cast<cuuint64_t>(head_dim) * elem * block_size};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elem),
+                       static_cast<cuuint32_t>(block_size < kTile ? block_size : kTile), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, elem == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 3,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <typename QT, typename KT, int D>
+size_t smem_bytes(int num_seqs) {
+  using Gm = Geom<KT, D>;
+  return 1024 + static_cast<size_t>(kWarps) * Gm::kSlots * (Gm::kSlotBytes + sizeof(SlotMeta) + 8) +
+         (3 * static_cast<size_t>(num_seqs) + 2) * sizeof(int);
+}
+
+template <typename QT, typename KT, int D>
+cudaError_t launch_typed(const TcParams& tp, const void* k_cache, const void* v_cache, int num_sms,
+                         cudaStream_t stream) {
+  const DecodeParams& p = tp.p;
+  CUtensorMap mk, mv;
+  const int64_t bxh = static_cast<int64_t>(p.num_blocks) * p.num_kv_heads;
+  if (!make_cache_map(&mk, k_cache, D, int(sizeof(KT)), p.block_size, bxh) ||
+      !make_cache_map(&mv, v_cache, D, int(sizeof(KT)), p.block_size, bxh))
+    return cudaErrorInvalidValue;
+  auto kernel = decode_tc_kernel<QT, KT, D>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem_bytes<QT, KT, D>(kTcMaxSeqs)));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int grid = (tp.num_warps + kWarps - 1) / kWarps;
+  (void)num_sms;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem_bytes<QT, KT, D>(p.num_seqs);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t err = cudaLaunchKernelEx(&cfg, kernel, mk, mv, tp);
+  if (err != cudaSuccess) return err;
+  note_launches(1);
+  if (tp.part_tiles != 0)
+    return launch_reduce_partitions(p, D, std::is_same<QT, bf16>::value ? PA_BF16 : PA_F16,
+                                    /*pdl=*/true, stream);
+  cudaLaunchConfig_t mcfg = cfg;
+  mcfg.gridDim = dim3(p.num_kv_heads, p.num_seqs);
+  mcfg.blockDim = dim3(128);
+  mcfg.dynamicSmemBytes = 0;
+  err = cudaLaunchKernelEx(&mcfg, tc_merge_kernel<QT, D>, tp);
+  if (err == cudaSuccess) note_launches(1);
+  return err;
+}
+
+}  // namespace
+
+bool tc_supported(int group, int head_dim, pa_dtype kv_dtype, int num_seqs) {
+  if (group != 2 && group != 4 && group != 8) return false;
+  if (num_seqs > kTcMaxSeqs) return false;
+  if (kv_dtype == PA_FP8_E4M3) return head_dim == 128;
+  return head_dim == 64 || head_dim == 128;
+}
+
+int tc_num_warps(int num_sms, int64_t max_units) {
+  int64_t w = static_cast<int64_t>(num_sms) * kWarps;
+  if (max_units < w) w = max_units;
+  return static_cast<int>(w < 1 ? 1 : w);
+}
+
+size_t tc_auto_workspace_bytes(int num_seqs, int head_dim, int num_sms) {
+  const size_t prefix = ((static_cast<size_t>(num_seqs) + 1) * sizeof(int32_t) + 255) / 256 * 256;
+  const size_t slots = 2 * static_cast<size_t>(num_sms) * kWarps * kMaxG * (head_dim + 2) * sizeof(float);
+  return prefix + slots;
+}
+
+cudaError_t launch_decode_tc(const DecodeParams& p, int head_dim, pa_dtype q_dtype,
+                             pa_dtype kv_dtype, int part_tiles, void* workspace, int num_sms,
+                             cudaStream_t stream) {
+  TcParams tp{};
+  tp.p = p;
+  tp.group = p.num_heads / p.num_kv_heads;
+  tp.part_tiles = part_tiles;
+  const int64_t tiles_max = (static_cast<int64_t>(p.max_context_len) + kTile - 1) / kTile;
+  if (part_tiles == 0) {
+    tp.num_warps = tc_num_warps(num_sms, static_cast<int64_t>(p.num_seqs) * p.num_kv_heads * tiles_max);
+    tp.ws_prefix = static_cast<int32_t*>(workspace);
+    tp.ws_slots = reinterpret_cast<float*>(
+        static_cast<char*>(workspace) +
+        ((static_cast<size_t>(p.num_seqs) + 1) * sizeof(int32_t) + 255) / 256 * 256);
+  } else {
+    const int64_t parts_max = (tiles_max + part_tiles - 1) / part_tiles;
+    tp.num_warps = tc_num_warps(num_sms, static_cast<int64_t>(p.num_seqs) * p.num_kv_heads * parts_max);
+  }
+  const void* kc = p.k_cache;
+  const void* vc = p.v_cache;
+  if (kv_dtype == PA_BF16) {
+    if (head_dim == 128) return launch_typed<bf16, bf16, 128>(tp, kc, vc, num_sms, stream);
+    return launch_typed<bf16, bf16, 64>(tp, kc, vc, num_sms, stream);
+  }
+  if (kv_dtype == PA_F16) {
+    if (head_dim == 128) return launch_typed<f16, f16, 128>(tp, kc, vc, num_sms, stream);
+    return launch_typed<f16, f16, 64>(tp, kc, vc, num_sms, stream);
+  }
+  if (q_dtype == PA_BF16) return launch_typed<bf16, fp8, 128>(tp, kc, vc, num_sms, stream);
+  return launch_typed<f16, fp8, 128>(tp, kc, vc, num_sms, stream);
+}
+
+}  // namespace pa

@@ -32,4 +32,20 @@ cudaError_t launch_copy_blocks(void* const* k_caches, void* const* v_caches, int
 cudaError_t launch_decode_simt(const DecodeParams& p, int head_dim, pa_dtype q_dtype,
                                pa_dtype kv_dtype, cudaStream_t stream);
 
+// Merge of the split path's per-partition partials into the output rows;
+// with pdl the launch may overlap the tail of the kernel before it.
+cudaError_t launch_reduce_partitions(const DecodeParams& p, int head_dim, pa_dtype q_dtype,
+                                     bool pdl, cudaStream_t stream);
+
+// Tensor-core decode (GQA groups of 2/4/8). part_tiles = 0: balanced schedule
+// over all warps of the GPU with partial states merged by a second kernel
+// (workspace of tc_auto_workspace_bytes); part_tiles > 0: split path with
+// partitions of part_tiles * 16 tokens into p.ws_acc / p.ws_ml.
+constexpr int kTcMaxSeqs = 2048;
+bool tc_supported(int group, int head_dim, pa_dtype kv_dtype, int num_seqs);
+size_t tc_auto_workspace_bytes(int num_seqs, int head_dim, int num_sms);
+cudaError_t launch_decode_tc(const DecodeParams& p, int head_dim, pa_dtype q_dtype,
+                             pa_dtype kv_dtype, int part_tiles, void* workspace, int num_sms,
+                             cudaStream_t stream);
+
 }  // namespace pa

@@ -54,6 +54,13 @@ int auto_partition(int max_context_len) {
   return max_context_len > kAutoPartition ? kAutoPartition : 0;
 }
 
+int current_sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return sms;
+}
+
 }  // namespace
 
 namespace pa {
@@ -121,10 +128,21 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t num
                                 int32_t partition_size) {
   (void)num_kv_heads;
   if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || max_context_len <= 0) return 0;
-  const int part = partition_size > 0 ? partition_size : auto_partition(max_context_len);
-  if (part == 0) return 0;
-  return split_workspace_bytes(num_seqs, num_heads, head_dim,
-                               num_partitions_for(max_context_len, part));
+  if (partition_size > 0)
+    return split_workspace_bytes(num_seqs, num_heads, head_dim,
+                                 num_partitions_for(max_context_len, partition_size));
+  // the library's own schedule: the tensor-core schedule's partial states, or
+  // the CUDA-core split path, whichever needs more
+  size_t need = 0;
+  const int sms = current_sm_count();
+  if (sms > 0) need = pa::tc_auto_workspace_bytes(num_seqs, head_dim, sms);
+  const int part = auto_partition(max_context_len);
+  if (part > 0) {
+    const size_t simt = split_workspace_bytes(num_seqs, num_heads, head_dim,
+                                              num_partitions_for(max_context_len, part));
+    if (simt > need) need = simt;
+  }
+  return need;
 }
 
 pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
@@ -189,20 +207,43 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
   p.max_context_len = max_context_len;
   p.scale_log2 = scale * pa::kLog2e;
 
-  int part = partition_size;
-  if (part > 0) {
-    const size_t need = split_workspace_bytes(num_seqs, num_heads, head_dim,
-                                              num_partitions_for(max_context_len, part));
+  const int group = num_heads / num_kv_heads;
+  const bool tc = pa::tc_supported(group, head_dim, kv_dtype, num_seqs);
+  const int sms = current_sm_count();
+  if (sms <= 0) return fail(PA_ERR_CUDA, "no current CUDA device");
+
+  if (partition_size > 0) {
+    const int nparts = num_partitions_for(max_context_len, partition_size);
+    const size_t need = split_workspace_bytes(num_seqs, num_heads, head_dim, nparts);
     if (workspace == nullptr || workspace_bytes < need)
       return fail(PA_ERR_WORKSPACE, "split decode needs %zu workspace bytes, got %zu", need,
                   workspace_bytes);
-  } else {
-    part = auto_partition(max_context_len);
-    if (part > 0) {
-      const size_t need = split_workspace_bytes(num_seqs, num_heads, head_dim,
-                                                num_partitions_for(max_context_len, part));
-      if (workspace == nullptr || workspace_bytes < need) part = 0;
-    }
+    p.partition_size = partition_size;
+    p.num_partitions = nparts;
+    const size_t slots = static_cast<size_t>(num_seqs) * num_heads * nparts;
+    p.ws_acc = static_cast<float*>(workspace);
+    p.ws_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                       ((slots * head_dim * sizeof(float)) + 255) / 256 * 256);
+    if (tc)
+      return from_cuda(pa::launch_decode_tc(p, head_dim, q_dtype, kv_dtype, partition_size / 16,
+                                            nullptr, sms, stream),
+                       "decode launch");
+    return from_cuda(pa::launch_decode_simt(p, head_dim, q_dtype, kv_dtype, stream),
+                     "decode launch");
+  }
+
+  if (tc && workspace != nullptr &&
+      workspace_bytes >= pa::tc_auto_workspace_bytes(num_seqs, head_dim, sms)) {
+    p.partition_size = 0;
+    p.num_partitions = 1;
+    return from_cuda(pa::launch_decode_tc(p, head_dim, q_dtype, kv_dtype, 0, workspace, sms, stream),
+                     "decode launch");
+  }
+  int part = auto_partition(max_context_len);
+  if (part > 0) {
+    const size_t need = split_workspace_bytes(num_seqs, num_heads, head_dim,
+                                              num_partitions_for(max_context_len, part));
+    if (workspace == nullptr || workspace_bytes < need) part = 0;
   }
   if (part > 0) {
     p.partition_size = part;

@@ -66,18 +66,23 @@ def test_lengths_around_block_boundaries(bs):
     _check(case)
 
 
-@pytest.mark.parametrize("partition_size", [16, 64, 512])
-@pytest.mark.parametrize("bs", [8, 16, 32])
-def test_split_path_matches_oracle_and_single_pass(partition_size, bs):
-    if partition_size % bs:
-        pytest.skip("partition must be a multiple of the block size")
+SPLIT_CASES = [(ps, bs) for ps in (16, 64, 512) for bs in (8, 16, 32) if ps % bs == 0]
+
+
+@pytest.mark.parametrize("partition_size,bs", SPLIT_CASES)
+def test_split_path_matches_oracle_and_other_schedules(partition_size, bs):
     lengths = [1, 15, 16, 17, 511, 512, 513, 1300, 2048]
     case = workloads.paged_case(600 + bs, lengths, 16, 4, 128, bs, BF16, name="split")
     (_, _), out_split, dc = _check(case, partition_size=partition_size)
-    out_single = run_decode(pa, dc, partition_size=0, workspace=False)
-    a, b = to_f64(out_split, BF16), to_f64(out_single, BF16)
-    # two float32 evaluation orders, each rounded to bf16: at most a couple of ulps apart
-    assert np.all(np.abs(a - b) <= 2 ** -7 * np.abs(b) + 1e-6)
+    ref = oracle_decode(case)
+    # the library's own schedule and the no-workspace schedule meet the same bound
+    for ws in (True, False):
+        other = run_decode(pa, dc, partition_size=0, workspace=ws)
+        assert_close(other, ref, BF16, BF16, f"schedule workspace={ws}")
+    # different schedules round P and the merges differently, never by more
+    # than the parity tolerance between them
+    a, b = to_f64(out_split, BF16), to_f64(run_decode(pa, dc), BF16)
+    assert np.all(np.abs(a - b) <= 2e-3 + 1e-2 * np.abs(b))
 
 
 def test_empty_and_single_token_sequences():

@@ -643,9 +643,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
 
 // Combine the partial states of every (sequence, KV head) that several warps
 // shared: with M = max_c m_c, out = sum_c 2^(m_c-M) acc_c / sum_c 2^(m_c-M) l_c.
-// Sequences with no context get zero rows here.
+// Sequences with no context get zero rows here. The contributors (the warps
+// whose tile ranges meet the segment) are taken in chunks of one per thread:
+// their slots and per-head weights go to shared memory, then every thread
+// accumulates its elements over the chunk with independent loads.
+constexpr int kMergeThreads = 128;
+
 template <typename QT, int D>
-__global__ void __launch_bounds__(128) tc_merge_kernel(const TcParams tp) {
+__global__ void __launch_bounds__(kMergeThreads) tc_merge_kernel(const TcParams tp) {
   griddep_wait();
   const DecodeParams& p = tp.p;
   const int kvh = blockIdx.x;
@@ -656,41 +661,115 @@ __global__ void __launch_bounds__(128) tc_merge_kernel(const TcParams tp) {
   QT* out = static_cast<QT*>(p.out) + (static_cast<int64_t>(seq) * p.num_heads + kvh * G) * D;
   const int tiles = tp.ws_prefix[seq + 1] - tp.ws_prefix[seq];
   if (tiles == 0) {
-    for (int i = threadIdx.x; i < G * D; i += blockDim.x) out[i] = from_float(0.f, static_cast<QT*>(nullptr));
+    for (int i = threadIdx.x; i < G * D; i += kMergeThreads) out[i] = from_float(0.f, static_cast<QT*>(nullptr));
     return;
   }
   const int64_t U = static_cast<int64_t>(tp.ws_prefix[B]) * Hkv;
   const int64_t W = tp.num_warps;
   const int64_t seg0 = static_cast<int64_t>(tp.ws_prefix[seq]) * Hkv + static_cast<int64_t>(kvh) * tiles;
   const int64_t seg1 = seg0 + tiles;
-  auto owner = [&](int64_t x) { return ((x + 1) * W - 1) / U; };
-  const int64_t w0 = owner(seg0), w1 = owner(seg1 - 1);
+  // warp w holds [w*U/W, (w+1)*U/W): the owner of tile x is ceil((x+1)W/U) - 1
+  const int64_t w0 = ((seg0 + 1) * W - 1) / U;
+  const int64_t w1 = (seg1 * W - 1) / U;
   if (w0 == w1) return;  // one warp held it and wrote the rows
+  const int nc = static_cast<int>(w1 - w0 + 1);
+
+  __shared__ float s_w[kMergeThreads][kMaxG];
+  __shared__ int s_slot[kMergeThreads];
+  __shared__ float s_red[kMergeThreads / 32][kMaxG];
+  __shared__ float s_max[kMaxG], s_inv[kMaxG];
   const float* slots = tp.ws_slots;
-  const int stride = kMaxG * (D + 2);
-  // warp w holds [w*U/W, (w+1)*U/W); warps whose range is empty wrote nothing
-  auto start = [&](int64_t w) { return w * U / W; };
-  auto slot_of = [&](int64_t w) -> int64_t {
-    return (w == w0 && start(w0) < seg0) ? 2 * w0 + 1 : 2 * w;
+  constexpr int stride = kMaxG * (D + 2);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // slot of contributor c; -1 for a warp whose range is empty (it wrote nothing)
+  auto slot_of = [&](int c) -> int {
+    const int64_t w = w0 + c;
+    const int64_t st = w * U / W, en = (w + 1) * U / W;
+    return st == en ? -1 : static_cast<int>((c == 0 && st < seg0) ? 2 * w + 1 : 2 * w);
   };
-  for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
-    const int h = i / D;
-    float mx = -INFINITY;
-    for (int64_t w = w0; w <= w1; ++w) {
-      if (start(w) == start(w + 1)) continue;
-      mx = fmaxf(mx, slots[slot_of(w) * stride + kMaxG * D + h]);
+
+  // pass 1: the largest max of each head over all contributors
+  float mx[kMaxG];
+#pragma unroll
+  for (int h = 0; h < kMaxG; ++h) mx[h] = -INFINITY;
+  for (int c = threadIdx.x; c < nc; c += kMergeThreads) {
+    const int slot = slot_of(c);
+    if (slot < 0) continue;
+#pragma unroll
+    for (int h = 0; h < kMaxG; ++h)
+      if (h < G) mx[h] = fmaxf(mx[h], slots[int64_t(slot) * stride + kMaxG * D + h]);
+  }
+#pragma unroll
+  for (int h = 0; h < kMaxG; ++h) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], off));
+    if (lane == 0) s_red[warp][h] = mx[h];
+  }
+  __syncthreads();
+  if (threadIdx.x < kMaxG) {
+    float m = s_red[0][threadIdx.x];
+    for (int w = 1; w < kMergeThreads / 32; ++w) m = fmaxf(m, s_red[w][threadIdx.x]);
+    s_max[threadIdx.x] = m;
+  }
+  __syncthreads();
+
+  // pass 2, one chunk of kMergeThreads contributors at a time: weights
+  // 2^(m_c - M), the denominator, and the weighted rows; a thread owns the
+  // elements threadIdx.x + k * kMergeThreads of the G x D block
+  constexpr int kPer = (kMaxG * D + kMergeThreads - 1) / kMergeThreads;
+  const int n = G * D;
+  float acc[kPer];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) acc[k] = 0.f;
+  float den[kMaxG];
+#pragma unroll
+  for (int h = 0; h < kMaxG; ++h) den[h] = 0.f;
+  for (int cb = 0; cb < nc; cb += kMergeThreads) {
+    const int c = cb + threadIdx.x;
+    const int slot = c < nc ? slot_of(c) : -1;
+    s_slot[threadIdx.x] = slot;
+#pragma unroll
+    for (int h = 0; h < kMaxG; ++h) {
+      float f = 0.f;
+      if (slot >= 0 && h < G && s_max[h] != -INFINITY) {
+        const float* sl = slots + int64_t(slot) * stride + kMaxG * D;
+        f = exp2f(sl[h] - s_max[h]);
+        den[h] += f * sl[kMaxG + h];
+      }
+      s_w[threadIdx.x][h] = f;
     }
-    float num = 0.f, den = 0.f;
-    if (mx != -INFINITY) {
-      for (int64_t w = w0; w <= w1; ++w) {
-        if (start(w) == start(w + 1)) continue;
-        const int64_t sl = slot_of(w);
-        const float f = exp2f(slots[sl * stride + kMaxG * D + h] - mx);
-        den += f * slots[sl * stride + kMaxG * D + kMaxG + h];
-        num += f * slots[sl * stride + i];
+    __syncthreads();
+    const int nchunk = min(kMergeThreads, nc - cb);
+#pragma unroll 2
+    for (int j = 0; j < nchunk; ++j) {
+      const int sj = s_slot[j];
+      if (sj < 0) continue;
+      const float* sl = slots + int64_t(sj) * stride;
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int i = threadIdx.x + k * kMergeThreads;
+        if (i < n) acc[k] += s_w[j][i / D] * sl[i];
       }
     }
-    out[i] = from_float(den > 0.f ? num / den : 0.f, static_cast<QT*>(nullptr));
+    __syncthreads();
+  }
+#pragma unroll
+  for (int h = 0; h < kMaxG; ++h) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) den[h] += __shfl_xor_sync(0xffffffffu, den[h], off);
+    if (lane == 0) s_red[warp][h] = den[h];
+  }
+  __syncthreads();
+  if (threadIdx.x < kMaxG) {
+    float d = 0.f;
+    for (int w = 0; w < kMergeThreads / 32; ++w) d += s_red[w][threadIdx.x];
+    s_inv[threadIdx.x] = d > 0.f ? 1.f / d : 0.f;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int i = threadIdx.x + k * kMergeThreads;
+    if (i < n) out[i] = from_float(acc[k] * s_inv[i / D], static_cast<QT*>(nullptr));
   }
 }
 
@@ -775,7 +854,7 @@ cudaError_t launch_typed(const TcParams& tp, const void* k_cache, const void* v_
                                     /*pdl=*/true, stream);
   cudaLaunchConfig_t mcfg = cfg;
   mcfg.gridDim = dim3(p.num_kv_heads, p.num_seqs);
-  mcfg.blockDim = dim3(128);
+  mcfg.blockDim = dim3(kMergeThreads);
   mcfg.dynamicSmemBytes = 0;
   err = cudaLaunchKernelEx(&mcfg, tc_merge_kernel<QT, D>, tp);
   if (err == cudaSuccess) note_launches(1);

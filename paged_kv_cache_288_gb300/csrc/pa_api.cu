@@ -209,15 +209,19 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
 
   const int group = num_heads / num_kv_heads;
   const bool tc = pa::tc_supported(group, head_dim, kv_dtype, num_seqs);
-  const int sms = current_sm_count();
-  if (sms <= 0) return fail(PA_ERR_CUDA, "no current CUDA device");
-
   if (partition_size > 0) {
     const int nparts = num_partitions_for(max_context_len, partition_size);
     const size_t need = split_workspace_bytes(num_seqs, num_heads, head_dim, nparts);
     if (workspace == nullptr || workspace_bytes < need)
       return fail(PA_ERR_WORKSPACE, "split decode needs %zu workspace bytes, got %zu", need,
                   workspace_bytes);
+  }
+  // every argument is checked: from here on the device is queried and used
+  const int sms = current_sm_count();
+  if (sms <= 0) return fail(PA_ERR_CUDA, "no current CUDA device");
+
+  if (partition_size > 0) {
+    const int nparts = num_partitions_for(max_context_len, partition_size);
     p.partition_size = partition_size;
     p.num_partitions = nparts;
     const size_t slots = static_cast<size_t>(num_seqs) * num_heads * nparts;

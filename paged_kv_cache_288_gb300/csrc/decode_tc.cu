@@ -32,6 +32,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
+#include <mutex>
 #include <type_traits>
 
 #include "common.cuh"
@@ -69,11 +71,33 @@ struct SlotMeta {
 struct TcParams {
   DecodeParams p;
   int32_t* ws_prefix;  // [num_seqs + 1] tile prefix, written by CTA 0 (auto schedule)
-  float* ws_slots;     // [2 * num_warps][kMaxG * (D + 2)] partial states (auto schedule)
+  float* ws_slots;     // [6 * num_warps][group * (D + 2)] partial states (auto schedule)
+  int32_t* claim;      // chunk counter of the auto schedule: 0 on entry, reset by the merge
   int32_t num_warps;   // warps that share the work
   int32_t part_tiles;  // tiles per partition (split path); 0 = auto schedule
   int32_t group;       // query heads per KV head
 };
+
+// The auto schedule: the first kStatic256/256 of the U tiles are split
+// evenly over the W warps (warp w: [w*S/W, (w+1)*S/W)); the rest are chunks
+// of C >= kMinChunk tiles that warps claim from a counter when their share is
+// done, so SMs that stream faster take more of them. At most 2W chunks.
+constexpr int kStatic256 = 192;
+constexpr int64_t kMinChunk = 8;
+
+struct Sched {
+  int64_t S, C, K;
+};
+
+__device__ __forceinline__ Sched make_sched(int64_t U, int64_t W) {
+  Sched sc;
+  sc.S = U * kStatic256 / 256;
+  const int64_t rest = U - sc.S;
+  int64_t c = (rest + 2 * W - 1) / (2 * W);
+  sc.C = c < kMinChunk ? kMinChunk : c;
+  sc.K = (rest + sc.C - 1) / sc.C;
+  return sc;
+}
 
 // Byte address of 16-byte chunk `chunk` of row `row` in a tile: 128-byte boxes
 // of 16 rows (8-row boxes stack to the same layout), chunks XOR-swizzled by
@@ -224,9 +248,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
   if (wid >= W) return;
   const int64_t U = static_cast<int64_t>(s_prefT[B]) * Hkv;
   int64_t f0, f1;
+  int64_t S = U, C = 1, K = 0;  // static tiles, chunk size, chunks
   if (tp.part_tiles == 0) {
-    f0 = wid * U / W;
-    f1 = (wid + 1) * U / W;
+    const Sched sc = make_sched(U, W);
+    S = sc.S;
+    C = sc.C;
+    K = sc.K;
+    f0 = wid * S / W;
+    f1 = (wid + 1) * S / W;
   } else {
     // whole partitions: convert partition indices to tile indices
     const int64_t US = static_cast<int64_t>(s_prefP[B]) * Hkv;
@@ -244,7 +273,20 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     f0 = part_to_tile(wid * US / W);
     f1 = part_to_tile((wid + 1) * US / W);
   }
-  if (f0 >= f1) return;
+  // claim the next chunk of the shared tail: its tile range and first slot
+  auto claim = [&](int64_t& r0, int64_t& r1, int64_t& slot0) -> bool {
+    if (K == 0) return false;
+    int k = 0;
+    if (lane == 0) k = atomicAdd(tp.claim, 1);
+    k = __shfl_sync(kFull, k, 0);
+    if (k >= K) return false;
+    r0 = S + static_cast<int64_t>(k) * C;
+    r1 = r0 + C < U ? r0 + C : U;
+    slot0 = 2 * W + 2 * static_cast<int64_t>(k);
+    return true;
+  };
+  int64_t cr0 = f0, cr1 = f1, cslot = 2 * wid;  // the consumer's current range
+  if (cr0 >= cr1 && !claim(cr0, cr1, cslot)) return;
 
   const int bs = p.block_size;
   const int width = p.max_blocks_per_seq;
@@ -444,7 +486,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
       }
     } else {
       // part of a (sequence, KV head) shared with other warps
-      float* base = tp.ws_slots + slot_index * (kMaxG * (D + 2));
+      float* base = tp.ws_slots + slot_index * (G * (D + 2));
 #pragma unroll
       for (int k = 0; k < Gm::kSteps; ++k) {
         const int da = d_of(k, 0), db = d_of(k, 1);
@@ -459,25 +501,48 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
       }
       if (g == 0) {
         if (h0 < G) {
-          base[kMaxG * D + h0] = m0;
-          base[kMaxG * D + kMaxG + h0] = l0;
+          base[G * D + h0] = m0;
+          base[G * D + G + h0] = l0;
         }
         if (h1 < G) {
-          base[kMaxG * D + h1] = m1;
-          base[kMaxG * D + kMaxG + h1] = l1;
+          base[G * D + h1] = m1;
+          base[G * D + G + h1] = l1;
         }
       }
     }
   };
 
   // ---- the warp's pipeline ----------------------------------------------
+  // The producer side runs up to NS tiles ahead of the consumer side; when it
+  // reaches the end of its range it claims the next chunk, which the consumer
+  // takes over when it reaches the same point (chunks are longer than NS
+  // tiles, so at most one claimed range waits).
   Cursor pc, cc;
-  cursor_at(pc, f0, s_prefT, B, Hkv);
+  cursor_at(pc, cr0, s_prefT, B, Hkv);
   cc = pc;
-  int pending = 0;
-  for (int s = 0; s < NS && pc.f < f1; ++s) {
-    issue(pc, s);
+  int64_t pr1 = cr1;
+  int64_t nr0 = 0, nr1 = 0, nslot = 0;
+  bool have_next = false, prod_done = false;
+  auto advance_producer = [&]() {
     cursor_next(pc, s_prefT, B, Hkv);
+    if (pc.f == pr1) {
+      int64_t a, b, sl;
+      if (claim(a, b, sl)) {
+        nr0 = a;
+        nr1 = b;
+        nslot = sl;
+        have_next = true;
+        pr1 = b;
+        cursor_at(pc, a, s_prefT, B, Hkv);
+      } else {
+        prod_done = true;
+      }
+    }
+  };
+  int pending = 0;
+  for (int s = 0; s < NS && !prod_done; ++s) {
+    issue(pc, s);
+    advance_producer();
     ++pending;
   }
   load_q(cc.seq, cc.kvh);
@@ -486,7 +551,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
   bool first_piece = true;
   uint32_t parity = 0;
   int s = 0;
-  while (cc.f < f1) {
+  while (true) {
     const bool ok = mbar_wait_bounded(bar_base + s * 8, (parity >> s) & 1u);
     if (!__all_sync(kFull, ok)) {
       if (lane == 0) flag_error(p.debug_err, PA_DEVERR_TIMEOUT);
@@ -614,9 +679,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     // the slot is free again: refill it with the tile NS ahead
     __syncwarp();
     fence_proxy_async_smem();
-    if (pc.f < f1) {
+    if (!prod_done) {
       issue(pc, s);
-      cursor_next(pc, s_prefT, B, Hkv);
+      advance_producer();
       ++pending;
     }
     s = (s + 1 == NS) ? 0 : s + 1;
@@ -624,18 +689,26 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     // end of a piece?
     const int seq = cc.seq, kvh = cc.kvh, t = cc.t, tiles = cc.tiles;
     cursor_next(cc, s_prefT, B, Hkv);
+    const bool range_end = cc.f == cr1;
     const bool new_segment = cc.t == 0 || (tp.part_tiles != 0 && cc.t % tp.part_tiles == 0);
-    if (cc.f == f1 || new_segment) {
+    if (range_end || new_segment) {
       const int seg_t0 = tp.part_tiles ? (t / tp.part_tiles) * tp.part_tiles : 0;
       const int seg_t1 = tp.part_tiles ? min(tiles, seg_t0 + tp.part_tiles) : tiles;
       const bool whole = piece_t0 == seg_t0 && t + 1 == seg_t1;
-      flush(seq, kvh, tp.part_tiles ? t / tp.part_tiles : 0, whole, first_piece ? 2 * wid : 2 * wid + 1);
+      flush(seq, kvh, tp.part_tiles ? t / tp.part_tiles : 0, whole, first_piece ? cslot : cslot + 1);
       first_piece = false;
-      if (cc.f < f1) {
-        reset();
-        piece_t0 = cc.t;
-        if (cc.seq != seq || cc.kvh != kvh) load_q(cc.seq, cc.kvh);
+      if (range_end) {
+        if (!have_next) break;
+        cr0 = nr0;
+        cr1 = nr1;
+        cslot = nslot;
+        have_next = false;
+        first_piece = true;
+        cursor_at(cc, cr0, s_prefT, B, Hkv);
       }
+      reset();
+      piece_t0 = cc.t;
+      if (range_end || cc.seq != seq || cc.kvh != kvh) load_q(cc.seq, cc.kvh);
     }
   }
   (void)pending;
@@ -652,6 +725,8 @@ constexpr int kMergeThreads = 128;
 template <typename QT, int D>
 __global__ void __launch_bounds__(kMergeThreads) tc_merge_kernel(const TcParams tp) {
   griddep_wait();
+  // the decode grid is complete: rearm its chunk counter for the next call
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *tp.claim = 0;
   const DecodeParams& p = tp.p;
   const int kvh = blockIdx.x;
   const int seq = blockIdx.y;
@@ -668,24 +743,45 @@ __global__ void __launch_bounds__(kMergeThreads) tc_merge_kernel(const TcParams 
   const int64_t W = tp.num_warps;
   const int64_t seg0 = static_cast<int64_t>(tp.ws_prefix[seq]) * Hkv + static_cast<int64_t>(kvh) * tiles;
   const int64_t seg1 = seg0 + tiles;
-  // warp w holds [w*U/W, (w+1)*U/W): the owner of tile x is ceil((x+1)W/U) - 1
-  const int64_t w0 = ((seg0 + 1) * W - 1) / U;
-  const int64_t w1 = (seg1 * W - 1) / U;
-  if (w0 == w1) return;  // one warp held it and wrote the rows
-  const int nc = static_cast<int>(w1 - w0 + 1);
+  const Sched sc = make_sched(U, W);
+  const int64_t S = sc.S, C = sc.C;
+  // static shares meeting [seg0, min(seg1, S)): warp w holds [w*S/W, (w+1)*S/W),
+  // so the owner of tile x < S is ceil((x+1)W/S) - 1
+  int64_t ws0 = 0, nstat = 0;
+  if (seg0 < S) {
+    const int64_t e = seg1 < S ? seg1 : S;
+    ws0 = ((seg0 + 1) * W - 1) / S;
+    nstat = (e * W - 1) / S - ws0 + 1;
+  }
+  // chunks meeting [max(seg0, S), seg1)
+  int64_t k0 = 0, ndyn = 0;
+  if (seg1 > S) {
+    const int64_t a = seg0 > S ? seg0 : S;
+    k0 = (a - S) / C;
+    ndyn = (seg1 - 1 - S) / C - k0 + 1;
+  }
+  const int nc = static_cast<int>(nstat + ndyn);
+  if (nc == 1) return;  // one range held the whole segment and wrote the rows
 
   __shared__ float s_w[kMergeThreads][kMaxG];
   __shared__ int s_slot[kMergeThreads];
   __shared__ float s_red[kMergeThreads / 32][kMaxG];
   __shared__ float s_max[kMaxG], s_inv[kMaxG];
   const float* slots = tp.ws_slots;
-  constexpr int stride = kMaxG * (D + 2);
+  const int stride = G * (D + 2);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // slot of contributor c; -1 for a warp whose range is empty (it wrote nothing)
+  // slot of contributor c: static shares first, then chunks; a range that
+  // starts before the segment left it in its second slot; -1 for a warp
+  // whose static share is empty (it wrote nothing)
   auto slot_of = [&](int c) -> int {
-    const int64_t w = w0 + c;
-    const int64_t st = w * U / W, en = (w + 1) * U / W;
-    return st == en ? -1 : static_cast<int>((c == 0 && st < seg0) ? 2 * w + 1 : 2 * w);
+    if (c < nstat) {
+      const int64_t w = ws0 + c;
+      const int64_t st = w * S / W, en = (w + 1) * S / W;
+      return st == en ? -1 : static_cast<int>((c == 0 && st < seg0) ? 2 * w + 1 : 2 * w);
+    }
+    const int64_t k = k0 + (c - nstat);
+    const int64_t st = S + k * C;
+    return static_cast<int>(2 * W + 2 * k + ((c == nstat && st < seg0) ? 1 : 0));
   };
 
   // pass 1: the largest max of each head over all contributors
@@ -697,7 +793,7 @@ __global__ void __launch_bounds__(kMergeThreads) tc_merge_kernel(const TcParams 
     if (slot < 0) continue;
 #pragma unroll
     for (int h = 0; h < kMaxG; ++h)
-      if (h < G) mx[h] = fmaxf(mx[h], slots[int64_t(slot) * stride + kMaxG * D + h]);
+      if (h < G) mx[h] = fmaxf(mx[h], slots[int64_t(slot) * stride + G * D + h]);
   }
 #pragma unroll
   for (int h = 0; h < kMaxG; ++h) {
@@ -732,9 +828,9 @@ __global__ void __launch_bounds__(kMergeThreads) tc_merge_kernel(const TcParams 
     for (int h = 0; h < kMaxG; ++h) {
       float f = 0.f;
       if (slot >= 0 && h < G && s_max[h] != -INFINITY) {
-        const float* sl = slots + int64_t(slot) * stride + kMaxG * D;
+        const float* sl = slots + int64_t(slot) * stride + G * D;
         f = exp2f(sl[h] - s_max[h]);
-        den[h] += f * sl[kMaxG + h];
+        den[h] += f * sl[G + h];
       }
       s_w[threadIdx.x][h] = f;
     }
@@ -774,6 +870,31 @@ __global__ void __launch_bounds__(kMergeThreads) tc_merge_kernel(const TcParams 
 }
 
 // ---- host side ----------------------------------------------------------
+
+// Chunk counters of the auto schedule, one per call in flight (calls take
+// them round robin). Module memory is zero when the library loads on a
+// device and every call's merge kernel sets its counter back to zero, so the
+// schedule needs nothing from the caller's memory.
+constexpr int kClaimSlots = 256;
+constexpr int kClaimDevices = 64;
+__device__ int32_t g_claim_counters[kClaimSlots];
+std::mutex g_claim_mutex;
+int32_t* g_claim_base[kClaimDevices] = {};
+std::atomic<unsigned> g_claim_next{0};
+
+int32_t* next_claim_counter() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kClaimDevices) return nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_claim_mutex);
+    if (g_claim_base[dev] == nullptr) {
+      void* ptr = nullptr;
+      if (cudaGetSymbolAddress(&ptr, g_claim_counters) != cudaSuccess) return nullptr;
+      g_claim_base[dev] = static_cast<int32_t*>(ptr);
+    }
+  }
+  return g_claim_base[dev] + (g_claim_next.fetch_add(1, std::memory_order_relaxed) % kClaimSlots);
+}
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -857,7 +978,11 @@ cudaError_t launch_typed(const TcParams& tp, const void* k_cache, const void* v_
   mcfg.blockDim = dim3(kMergeThreads);
   mcfg.dynamicSmemBytes = 0;
   err = cudaLaunchKernelEx(&mcfg, tc_merge_kernel<QT, D>, tp);
-  if (err == cudaSuccess) note_launches(1);
+  if (err == cudaSuccess) {
+    note_launches(1);
+  } else {
+    cudaMemsetAsync(tp.claim, 0, sizeof(int32_t), stream);  // rearm the counter ourselves
+  }
   return err;
 }
 
@@ -876,9 +1001,11 @@ int tc_num_warps(int num_sms, int64_t max_units) {
   return static_cast<int>(w < 1 ? 1 : w);
 }
 
-size_t tc_auto_workspace_bytes(int num_seqs, int head_dim, int num_sms) {
+size_t tc_auto_workspace_bytes(int num_seqs, int head_dim, int group, int num_sms) {
   const size_t prefix = ((static_cast<size_t>(num_seqs) + 1) * sizeof(int32_t) + 255) / 256 * 256;
-  const size_t slots = 2 * static_cast<size_t>(num_sms) * kWarps * kMaxG * (head_dim + 2) * sizeof(float);
+  // two partial states per static share and per chunk (at most 2W chunks)
+  const size_t W = static_cast<size_t>(num_sms) * kWarps;
+  const size_t slots = 6 * W * static_cast<size_t>(group) * (head_dim + 2) * sizeof(float);
   return prefix + slots;
 }
 
@@ -891,6 +1018,8 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int head_dim, pa_dtype q_dty
   tp.part_tiles = part_tiles;
   const int64_t tiles_max = (static_cast<int64_t>(p.max_context_len) + kTile - 1) / kTile;
   if (part_tiles == 0) {
+    tp.claim = next_claim_counter();
+    if (tp.claim == nullptr) return cudaErrorInvalidDevice;
     tp.num_warps = tc_num_warps(num_sms, static_cast<int64_t>(p.num_seqs) * p.num_kv_heads * tiles_max);
     tp.ws_prefix = static_cast<int32_t*>(workspace);
     tp.ws_slots = reinterpret_cast<float*>(

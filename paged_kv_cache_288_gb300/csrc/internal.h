@@ -43,7 +43,7 @@ cudaError_t launch_reduce_partitions(const DecodeParams& p, int head_dim, pa_dty
 // partitions of part_tiles * 16 tokens into p.ws_acc / p.ws_ml.
 constexpr int kTcMaxSeqs = 2048;
 bool tc_supported(int group, int head_dim, pa_dtype kv_dtype, int num_seqs);
-size_t tc_auto_workspace_bytes(int num_seqs, int head_dim, int num_sms);
+size_t tc_auto_workspace_bytes(int num_seqs, int head_dim, int group, int num_sms);
 cudaError_t launch_decode_tc(const DecodeParams& p, int head_dim, pa_dtype q_dtype,
                              pa_dtype kv_dtype, int part_tiles, void* workspace, int num_sms,
                              cudaStream_t stream);

@@ -836,15 +836,28 @@ __global__ void __launch_bounds__(kMergeThreads) tc_merge_kernel(const TcParams 
     }
     __syncthreads();
     const int nchunk = min(kMergeThreads, nc - cb);
-#pragma unroll 2
-    for (int j = 0; j < nchunk; ++j) {
-      const int sj = s_slot[j];
-      if (sj < 0) continue;
-      const float* sl = slots + int64_t(sj) * stride;
+    // eight contributors per step, all their loads issued before any use
+    for (int j0 = 0; j0 < nchunk; j0 += 8) {
+      float v[8][kPer];
 #pragma unroll
-      for (int k = 0; k < kPer; ++k) {
-        const int i = threadIdx.x + k * kMergeThreads;
-        if (i < n) acc[k] += s_w[j][i / D] * sl[i];
+      for (int u = 0; u < 8; ++u) {
+        const int j = j0 + u;
+        const int sj = j < nchunk ? s_slot[j] : -1;
+        const float* sl = slots + int64_t(sj < 0 ? 0 : sj) * stride;
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+          const int i = threadIdx.x + k * kMergeThreads;
+          v[u][k] = (sj >= 0 && i < n) ? sl[i] : 0.f;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int j = j0 + u < nchunk ? j0 + u : 0;
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+          const int i = threadIdx.x + k * kMergeThreads;
+          if (i < n) acc[k] += s_w[j][i / D] * v[u][k];
+        }
       }
     }
     __syncthreads();

@@ -511,68 +511,36 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     for (int h = 0; h < kMaxG; ++h)
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) den[h] += __shfl_xor_sync(kFull, den[h], off);
-    // rows: lane owns float4 groups lane + 32 q of the G x D block (q < G*D/128);
-    // contributors go 32 at a time, lane j holding contributor j's slot and
-    // weights, broadcast by shuffles; four contributors' loads per step
-    constexpr int kQ = kMaxG * D / 128;
-    const int nq = G * D / 128;
-    float4 acc[kQ];
+    QT* out = static_cast<QT*>(p.out) + (static_cast<int64_t>(seq) * Hq + kvh * G) * D;
+    const int n = G * D;
+    constexpr int kGroup = 8;  // elements per lane per pass
+    for (int e0 = 0; e0 < n; e0 += 32 * kGroup) {
+      float acc[kGroup];
 #pragma unroll
-    for (int q = 0; q < kQ; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int64_t r = 0; r < nc; r += 32) {
-      const int64_t c = r + lane;
-      int sl = -1;
-      float w[kMaxG];
+      for (int j = 0; j < kGroup; ++j) acc[j] = 0.f;
+#pragma unroll 2
+      for (int64_t c = 0; c < nc; ++c) {
+        const int64_t sl = slot_of(ct, seg0, c);
+        if (sl < 0) continue;
+        const float* base = tp.ws_slots + sl * stride;
 #pragma unroll
-      for (int h = 0; h < kMaxG; ++h) w[h] = 0.f;
-      if (c < nc) {
-        sl = static_cast<int>(slot_of(ct, seg0, c));
-        if (sl >= 0) {
-#pragma unroll
-          for (int h = 0; h < kMaxG; ++h)
-            if (h < G && mx[h] != -INFINITY)
-              w[h] = exp2f(__ldcg(tp.ws_slots + int64_t(sl) * stride + G * D + h) - mx[h]);
-        }
-      }
-      const int nr = static_cast<int>(nc - r < 32 ? nc - r : 32);
-#pragma unroll 4
-      for (int j = 0; j < nr; ++j) {
-        const int slj = __shfl_sync(kFull, sl, j);
-        float wj[kMaxG];
-#pragma unroll
-        for (int h = 0; h < kMaxG; ++h) wj[h] = __shfl_sync(kFull, w[h], j);
-        if (slj < 0) continue;
-        const float4* base = reinterpret_cast<const float4*>(tp.ws_slots + int64_t(slj) * stride);
-#pragma unroll
-        for (int q = 0; q < kQ; ++q) {
-          if (q < nq) {
-            const int e4 = lane + 32 * q;
-            const float wt = pick8(wj, (4 * e4) / D);
-            const float4 v = __ldcg(base + e4);
-            acc[q].x += wt * v.x;
-            acc[q].y += wt * v.y;
-            acc[q].z += wt * v.z;
-            acc[q].w += wt * v.w;
+        for (int j = 0; j < kGroup; ++j) {
+          const int e = e0 + lane + 32 * j;
+          if (e < n) {
+            const int h = e / D;
+            const float mh = pick8(mx, h);
+            const float f = mh == -INFINITY ? 0.f : exp2f(__ldcg(base + G * D + h) - mh);
+            acc[j] += f * __ldcg(base + e);
           }
         }
       }
-    }
-    QT* out = static_cast<QT*>(p.out) + (static_cast<int64_t>(seq) * Hq + kvh * G) * D;
 #pragma unroll
-    for (int q = 0; q < kQ; ++q) {
-      if (q < nq) {
-        const int e = 4 * (lane + 32 * q);
-        const float d = pick8(den, e / D);
-        const float inv = d > 0.f ? 1.f / d : 0.f;
-        uint2 pk;
-        if constexpr (std::is_same<QT, bf16>::value) {
-          pk.x = pack_bf16(acc[q].x * inv, acc[q].y * inv);
-          pk.y = pack_bf16(acc[q].z * inv, acc[q].w * inv);
-        } else {
-          pk.x = pack_f16(acc[q].x * inv, acc[q].y * inv);
-          pk.y = pack_f16(acc[q].z * inv, acc[q].w * inv);
+      for (int j = 0; j < kGroup; ++j) {
+        const int e = e0 + lane + 32 * j;
+        if (e < n) {
+          const float d = pick8(den, e / D);
+          out[e] = from_float(d > 0.f ? acc[j] / d : 0.f, static_cast<QT*>(nullptr));
         }
-        *reinterpret_cast<uint2*>(out + e) = pk;
       }
     }
   };

@@ -68,20 +68,11 @@ struct SlotMeta {
   uint32_t pad[3];
 };
 
-// Per-call counters of the auto schedule, in module memory: all zero when a
-// call starts (zero at load, and the last warp of every call rearms them).
-struct CallState {
-  int32_t claim;   // next tail chunk to hand out
-  int32_t arrive;  // CTAs that have cleared their share of the piece counters
-  int32_t done;    // warps that have finished
-  int32_t pad;
-};
-
 struct TcParams {
   DecodeParams p;
-  int32_t* ws_count;   // [num_seqs * num_kv_heads] pieces finished per (sequence, KV head)
+  int32_t* ws_prefix;  // [num_seqs + 1] tile prefix, written by CTA 0 (auto schedule)
   float* ws_slots;     // [6 * num_warps][group * (D + 2)] partial states (auto schedule)
-  CallState* state;    // auto schedule only
+  int32_t* claim;      // chunk counter of the auto schedule: 0 on entry, reset by the merge
   int32_t num_warps;   // warps that share the work
   int32_t part_tiles;  // tiles per partition (split path); 0 = auto schedule
   int32_t group;       // query heads per KV head
@@ -127,14 +118,6 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
   __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes & 0xffffu),
                                              __NV_E4M3);
   return static_cast<uint32_t>(r.x) | (static_cast<uint32_t>(r.y) << 16);
-}
-
-// a[h] for a runtime h < 8, without indexing a register array
-__device__ __forceinline__ float pick8(const float (&a)[8], int h) {
-  float r = a[0];
-#pragma unroll
-  for (int i = 1; i < 8; ++i) r = (h == i) ? a[i] : r;
-  return r;
 }
 
 // Keep the 16-bit halves of a (token t, token t+1) register whose token holds data.
@@ -255,28 +238,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     s_prefP[B] = run_p;
   }
   __syncthreads();
-  const int Hq = p.num_heads;
-  if (tp.part_tiles == 0) {
-    // clear this CTA's share of the piece counters, write the zero rows of
-    // sequences without context, then announce the CTA
-    for (int i = blockIdx.x * kThreads + threadIdx.x; i < B * Hkv; i += gridDim.x * kThreads)
-      tp.ws_count[i] = 0;
-    QT* out = static_cast<QT*>(p.out);
-    for (int seq = blockIdx.x; seq < B; seq += gridDim.x)
-      if (s_ctx[seq] == 0)
-        for (int i = threadIdx.x; i < Hq * D; i += kThreads)
-          out[static_cast<int64_t>(seq) * Hq * D + i] = from_float(0.f, static_cast<QT*>(nullptr));
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) atomicAdd(&tp.state->arrive, 1);
-  }
+  if (blockIdx.x == 0 && tp.ws_prefix != nullptr)
+    for (int i = threadIdx.x; i <= B; i += kThreads) tp.ws_prefix[i] = s_prefT[i];
   griddep_launch_dependents();
 
   // ---- this warp's share of the tile list --------------------------------
   const int64_t W = tp.num_warps;
   const int64_t wid = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
-  bool all_arrived = false;
-  auto body = [&]() {
   if (wid >= W) return;
   const int64_t U = static_cast<int64_t>(s_prefT[B]) * Hkv;
   int64_t f0, f1;
@@ -309,7 +277,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
   auto claim = [&](int64_t& r0, int64_t& r1, int64_t& slot0) -> bool {
     if (K == 0) return false;
     int k = 0;
-    if (lane == 0) k = atomicAdd(&tp.state->claim, 1);
+    if (lane == 0) k = atomicAdd(tp.claim, 1);
     k = __shfl_sync(kFull, k, 0);
     if (k >= K) return false;
     r0 = S + static_cast<int64_t>(k) * C;
@@ -322,6 +290,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
 
   const int bs = p.block_size;
   const int width = p.max_blocks_per_seq;
+  const int Hq = p.num_heads;
   const uint32_t slot_base0 = smem_u32(slots) + warp * NS * Gm::kSlotBytes;
   SlotMeta* my_meta = meta + warp * NS;
   const uint32_t bar_base = smem_u32(bars + warp * NS);
@@ -442,109 +411,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     else return 16 * k + g + 8 * upper;
   };
 
-  // The ranges that meet (sequence, KV head) [seg0, seg1): static shares
-  // ws0.. (warp w holds [w*S/W, (w+1)*S/W), owner of x < S is
-  // ceil((x+1)W/S) - 1), then tail chunks k0..; each left its state in its
-  // first slot, or its second if it started before the segment. Static
-  // shares that are empty wrote nothing (slot -1).
-  struct Contrib {
-    int64_t ws0, nstat, k0, ndyn;
-  };
-  auto contributors = [&](int64_t seg0, int64_t seg1) {
-    Contrib ct{0, 0, 0, 0};
-    if (seg0 < S) {
-      const int64_t e = seg1 < S ? seg1 : S;
-      ct.ws0 = ((seg0 + 1) * W - 1) / S;
-      ct.nstat = (e * W - 1) / S - ct.ws0 + 1;
-    }
-    if (seg1 > S) {
-      const int64_t a = seg0 > S ? seg0 : S;
-      ct.k0 = (a - S) / C;
-      ct.ndyn = (seg1 - 1 - S) / C - ct.k0 + 1;
-    }
-    return ct;
-  };
-  auto slot_of = [&](const Contrib& ct, int64_t seg0, int64_t c) -> int64_t {
-    if (c < ct.nstat) {
-      const int64_t w = ct.ws0 + c;
-      const int64_t st = w * S / W, en = (w + 1) * S / W;
-      return st == en ? -1 : ((c == 0 && st < seg0) ? 2 * w + 1 : 2 * w);
-    }
-    const int64_t k = ct.k0 + (c - ct.nstat);
-    return 2 * W + 2 * k + ((c == ct.nstat && S + k * C < seg0) ? 1 : 0);
-  };
-
-  // The last piece of a shared (sequence, KV head) to finish combines all
-  // of them: with M = max_c m_c, out = sum_c 2^(m_c-M) acc_c / sum_c
-  // 2^(m_c-M) l_c. Lanes take contributors for the (max, sum) part and
-  // elements (lane + 32 j of the G x D block) for the rows.
-  auto merge_segment = [&](int seq, int kvh, int64_t seg0, const Contrib& ct) {
-    const int64_t nc = ct.nstat + ct.ndyn;
-    const int stride = G * (D + 2);
-    float mx[kMaxG], den[kMaxG];
-#pragma unroll
-    for (int h = 0; h < kMaxG; ++h) {
-      mx[h] = -INFINITY;
-      den[h] = 0.f;
-    }
-    for (int64_t c = lane; c < nc; c += 32) {
-      const int64_t sl = slot_of(ct, seg0, c);
-      if (sl < 0) continue;
-#pragma unroll
-      for (int h = 0; h < kMaxG; ++h)
-        if (h < G) mx[h] = fmaxf(mx[h], __ldcg(tp.ws_slots + sl * stride + G * D + h));
-    }
-#pragma unroll
-    for (int h = 0; h < kMaxG; ++h)
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) mx[h] = fmaxf(mx[h], __shfl_xor_sync(kFull, mx[h], off));
-    for (int64_t c = lane; c < nc; c += 32) {
-      const int64_t sl = slot_of(ct, seg0, c);
-      if (sl < 0) continue;
-#pragma unroll
-      for (int h = 0; h < kMaxG; ++h)
-        if (h < G && mx[h] != -INFINITY)
-          den[h] += exp2f(__ldcg(tp.ws_slots + sl * stride + G * D + h) - mx[h]) *
-                    __ldcg(tp.ws_slots + sl * stride + G * D + G + h);
-    }
-#pragma unroll
-    for (int h = 0; h < kMaxG; ++h)
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) den[h] += __shfl_xor_sync(kFull, den[h], off);
-    QT* out = static_cast<QT*>(p.out) + (static_cast<int64_t>(seq) * Hq + kvh * G) * D;
-    const int n = G * D;
-    constexpr int kGroup = 8;  // elements per lane per pass
-    for (int e0 = 0; e0 < n; e0 += 32 * kGroup) {
-      float acc[kGroup];
-#pragma unroll
-      for (int j = 0; j < kGroup; ++j) acc[j] = 0.f;
-#pragma unroll 2
-      for (int64_t c = 0; c < nc; ++c) {
-        const int64_t sl = slot_of(ct, seg0, c);
-        if (sl < 0) continue;
-        const float* base = tp.ws_slots + sl * stride;
-#pragma unroll
-        for (int j = 0; j < kGroup; ++j) {
-          const int e = e0 + lane + 32 * j;
-          if (e < n) {
-            const int h = e / D;
-            const float mh = pick8(mx, h);
-            const float f = mh == -INFINITY ? 0.f : exp2f(__ldcg(base + G * D + h) - mh);
-            acc[j] += f * __ldcg(base + e);
-          }
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < kGroup; ++j) {
-        const int e = e0 + lane + 32 * j;
-        if (e < n) {
-          const float d = pick8(den, e / D);
-          out[e] = from_float(d > 0.f ? acc[j] / d : 0.f, static_cast<QT*>(nullptr));
-        }
-      }
-    }
-  };
-
   // Write the finished piece: output rows, a partition partial, or a
   // per-warp partial state for the merge.
   auto flush = [&](int seq, int kvh, int part, bool whole, int64_t slot_index) {
@@ -642,41 +508,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
           base[G * D + h1] = m1;
           base[G * D + G + h1] = l1;
         }
-      }
-      // publish the state, then count the piece; the count's last increment
-      // belongs to the warp that merges
-      __threadfence();
-      __syncwarp();
-      const int tiles = s_prefT[seq + 1] - s_prefT[seq];
-      const int64_t seg0 = static_cast<int64_t>(s_prefT[seq]) * Hkv + static_cast<int64_t>(kvh) * tiles;
-      const Contrib ct = contributors(seg0, seg0 + tiles);
-      int64_t pieces = ct.ndyn;
-      for (int64_t c = 0; c < ct.nstat; ++c) pieces += slot_of(ct, seg0, c) >= 0 ? 1 : 0;
-      int last = 0;
-      if (lane == 0) {
-        bool ok = all_arrived;
-        if (!ok) {
-          // every CTA must have cleared its counters first (it does so at its
-          // start, microseconds before any piece ends)
-          const uint64_t t0 = globaltimer_ns();
-          while (!(ok = atomicAdd(&tp.state->arrive, 0) >= static_cast<int>(gridDim.x))) {
-            if (globaltimer_ns() - t0 > kWaitLimitNs) break;
-          }
-          __threadfence();
-        }
-        if (ok) {
-          last = atomicAdd(&tp.ws_count[static_cast<int64_t>(seq) * Hkv + kvh], 1) ==
-                 static_cast<int>(pieces - 1);
-        } else {
-          flag_error(p.debug_err, PA_DEVERR_TIMEOUT);
-        }
-        last |= ok ? 2 : 0;
-      }
-      last = __shfl_sync(kFull, last, 0);
-      all_arrived = (last & 2) != 0;
-      if (last & 1) {
-        __threadfence();
-        merge_segment(seq, kvh, seg0, ct);
       }
     }
   };
@@ -881,49 +712,201 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     }
   }
   (void)pending;
-  };
-  body();
+}
 
-  // the last warp of the call rearms the per-call counters
-  if (tp.part_tiles == 0) {
-    __syncwarp();
-    if (lane == 0) {
-      __threadfence();
-      if (atomicAdd(&tp.state->done, 1) == static_cast<int>(gridDim.x) * kWarps - 1) {
-        tp.state->claim = 0;
-        tp.state->arrive = 0;
-        tp.state->done = 0;
-        __threadfence();
+// Combine the partial states of every (sequence, KV head) that several warps
+// shared: with M = max_c m_c, out = sum_c 2^(m_c-M) acc_c / sum_c 2^(m_c-M) l_c.
+// Sequences with no context get zero rows here. The contributors (the warps
+// whose tile ranges meet the segment) are taken in chunks of one per thread:
+// their slots and per-head weights go to shared memory, then every thread
+// accumulates its elements over the chunk with independent loads.
+constexpr int kMergeThreads = 128;
+
+template <typename QT, int D>
+__global__ void __launch_bounds__(kMergeThreads) tc_merge_kernel(const TcParams tp) {
+  griddep_wait();
+  // the decode grid is complete: rearm its chunk counter for the next call
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *tp.claim = 0;
+  const DecodeParams& p = tp.p;
+  const int kvh = blockIdx.x;
+  const int seq = blockIdx.y;
+  const int G = tp.group;
+  const int Hkv = p.num_kv_heads;
+  const int B = p.num_seqs;
+  QT* out = static_cast<QT*>(p.out) + (static_cast<int64_t>(seq) * p.num_heads + kvh * G) * D;
+  const int tiles = tp.ws_prefix[seq + 1] - tp.ws_prefix[seq];
+  if (tiles == 0) {
+    for (int i = threadIdx.x; i < G * D; i += kMergeThreads) out[i] = from_float(0.f, static_cast<QT*>(nullptr));
+    return;
+  }
+  const int64_t U = static_cast<int64_t>(tp.ws_prefix[B]) * Hkv;
+  const int64_t W = tp.num_warps;
+  const int64_t seg0 = static_cast<int64_t>(tp.ws_prefix[seq]) * Hkv + static_cast<int64_t>(kvh) * tiles;
+  const int64_t seg1 = seg0 + tiles;
+  const Sched sc = make_sched(U, W);
+  const int64_t S = sc.S, C = sc.C;
+  // static shares meeting [seg0, min(seg1, S)): warp w holds [w*S/W, (w+1)*S/W),
+  // so the owner of tile x < S is ceil((x+1)W/S) - 1
+  int64_t ws0 = 0, nstat = 0;
+  if (seg0 < S) {
+    const int64_t e = seg1 < S ? seg1 : S;
+    ws0 = ((seg0 + 1) * W - 1) / S;
+    nstat = (e * W - 1) / S - ws0 + 1;
+  }
+  // chunks meeting [max(seg0, S), seg1)
+  int64_t k0 = 0, ndyn = 0;
+  if (seg1 > S) {
+    const int64_t a = seg0 > S ? seg0 : S;
+    k0 = (a - S) / C;
+    ndyn = (seg1 - 1 - S) / C - k0 + 1;
+  }
+  const int nc = static_cast<int>(nstat + ndyn);
+  if (nc == 1) return;  // one range held the whole segment and wrote the rows
+
+  __shared__ float s_w[kMergeThreads][kMaxG];
+  __shared__ int s_slot[kMergeThreads];
+  __shared__ float s_red[kMergeThreads / 32][kMaxG];
+  __shared__ float s_max[kMaxG], s_inv[kMaxG];
+  const float* slots = tp.ws_slots;
+  const int stride = G * (D + 2);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // slot of contributor c: static shares first, then chunks; a range that
+  // starts before the segment left it in its second slot; -1 for a warp
+  // whose static share is empty (it wrote nothing)
+  auto slot_of = [&](int c) -> int {
+    if (c < nstat) {
+      const int64_t w = ws0 + c;
+      const int64_t st = w * S / W, en = (w + 1) * S / W;
+      return st == en ? -1 : static_cast<int>((c == 0 && st < seg0) ? 2 * w + 1 : 2 * w);
+    }
+    const int64_t k = k0 + (c - nstat);
+    const int64_t st = S + k * C;
+    return static_cast<int>(2 * W + 2 * k + ((c == nstat && st < seg0) ? 1 : 0));
+  };
+
+  // pass 1: the largest max of each head over all contributors
+  float mx[kMaxG];
+#pragma unroll
+  for (int h = 0; h < kMaxG; ++h) mx[h] = -INFINITY;
+  for (int c = threadIdx.x; c < nc; c += kMergeThreads) {
+    const int slot = slot_of(c);
+    if (slot < 0) continue;
+#pragma unroll
+    for (int h = 0; h < kMaxG; ++h)
+      if (h < G) mx[h] = fmaxf(mx[h], slots[int64_t(slot) * stride + G * D + h]);
+  }
+#pragma unroll
+  for (int h = 0; h < kMaxG; ++h) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], off));
+    if (lane == 0) s_red[warp][h] = mx[h];
+  }
+  __syncthreads();
+  if (threadIdx.x < kMaxG) {
+    float m = s_red[0][threadIdx.x];
+    for (int w = 1; w < kMergeThreads / 32; ++w) m = fmaxf(m, s_red[w][threadIdx.x]);
+    s_max[threadIdx.x] = m;
+  }
+  __syncthreads();
+
+  // pass 2, one chunk of kMergeThreads contributors at a time: weights
+  // 2^(m_c - M), the denominator, and the weighted rows; a thread owns the
+  // elements threadIdx.x + k * kMergeThreads of the G x D block
+  constexpr int kPer = (kMaxG * D + kMergeThreads - 1) / kMergeThreads;
+  const int n = G * D;
+  float acc[kPer];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) acc[k] = 0.f;
+  float den[kMaxG];
+#pragma unroll
+  for (int h = 0; h < kMaxG; ++h) den[h] = 0.f;
+  for (int cb = 0; cb < nc; cb += kMergeThreads) {
+    const int c = cb + threadIdx.x;
+    const int slot = c < nc ? slot_of(c) : -1;
+    s_slot[threadIdx.x] = slot;
+#pragma unroll
+    for (int h = 0; h < kMaxG; ++h) {
+      float f = 0.f;
+      if (slot >= 0 && h < G && s_max[h] != -INFINITY) {
+        const float* sl = slots + int64_t(slot) * stride + G * D;
+        f = exp2f(sl[h] - s_max[h]);
+        den[h] += f * sl[G + h];
+      }
+      s_w[threadIdx.x][h] = f;
+    }
+    __syncthreads();
+    const int nchunk = min(kMergeThreads, nc - cb);
+    // eight contributors per step, all their loads issued before any use
+    for (int j0 = 0; j0 < nchunk; j0 += 8) {
+      float v[8][kPer];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int j = j0 + u;
+        const int sj = j < nchunk ? s_slot[j] : -1;
+        const float* sl = slots + int64_t(sj < 0 ? 0 : sj) * stride;
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+          const int i = threadIdx.x + k * kMergeThreads;
+          v[u][k] = (sj >= 0 && i < n) ? sl[i] : 0.f;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int j = j0 + u < nchunk ? j0 + u : 0;
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+          const int i = threadIdx.x + k * kMergeThreads;
+          if (i < n) acc[k] += s_w[j][i / D] * v[u][k];
+        }
       }
     }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int h = 0; h < kMaxG; ++h) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) den[h] += __shfl_xor_sync(0xffffffffu, den[h], off);
+    if (lane == 0) s_red[warp][h] = den[h];
+  }
+  __syncthreads();
+  if (threadIdx.x < kMaxG) {
+    float d = 0.f;
+    for (int w = 0; w < kMergeThreads / 32; ++w) d += s_red[w][threadIdx.x];
+    s_inv[threadIdx.x] = d > 0.f ? 1.f / d : 0.f;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int i = threadIdx.x + k * kMergeThreads;
+    if (i < n) out[i] = from_float(acc[k] * s_inv[i / D], static_cast<QT*>(nullptr));
   }
 }
 
 // ---- host side ----------------------------------------------------------
 
-// Per-call counters of the auto schedule, one block per call in flight
-// (calls take them round robin). Module memory is zero when the library loads
-// on a device and the last warp of every call sets its block back to zero, so
-// the schedule needs no prepared caller memory.
-constexpr int kStateSlots = 256;
-constexpr int kStateDevices = 64;
-__device__ CallState g_call_state[kStateSlots];
-std::mutex g_state_mutex;
-CallState* g_state_base[kStateDevices] = {};
-std::atomic<unsigned> g_state_next{0};
+// Chunk counters of the auto schedule, one per call in flight (calls take
+// them round robin). Module memory is zero when the library loads on a
+// device and every call's merge kernel sets its counter back to zero, so the
+// schedule needs nothing from the caller's memory.
+constexpr int kClaimSlots = 256;
+constexpr int kClaimDevices = 64;
+__device__ int32_t g_claim_counters[kClaimSlots];
+std::mutex g_claim_mutex;
+int32_t* g_claim_base[kClaimDevices] = {};
+std::atomic<unsigned> g_claim_next{0};
 
-CallState* next_call_state() {
+int32_t* next_claim_counter() {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kStateDevices) return nullptr;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kClaimDevices) return nullptr;
   {
-    std::lock_guard<std::mutex> lock(g_state_mutex);
-    if (g_state_base[dev] == nullptr) {
+    std::lock_guard<std::mutex> lock(g_claim_mutex);
+    if (g_claim_base[dev] == nullptr) {
       void* ptr = nullptr;
-      if (cudaGetSymbolAddress(&ptr, g_call_state) != cudaSuccess) return nullptr;
-      g_state_base[dev] = static_cast<CallState*>(ptr);
+      if (cudaGetSymbolAddress(&ptr, g_claim_counters) != cudaSuccess) return nullptr;
+      g_claim_base[dev] = static_cast<int32_t*>(ptr);
     }
   }
-  return g_state_base[dev] + (g_state_next.fetch_add(1, std::memory_order_relaxed) % kStateSlots);
+  return g_claim_base[dev] + (g_claim_next.fetch_add(1, std::memory_order_relaxed) % kClaimSlots);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -1003,7 +986,17 @@ cudaError_t launch_typed(const TcParams& tp, const void* k_cache, const void* v_
   if (tp.part_tiles != 0)
     return launch_reduce_partitions(p, D, std::is_same<QT, bf16>::value ? PA_BF16 : PA_F16,
                                     /*pdl=*/true, stream);
-  return cudaSuccess;
+  cudaLaunchConfig_t mcfg = cfg;
+  mcfg.gridDim = dim3(p.num_kv_heads, p.num_seqs);
+  mcfg.blockDim = dim3(kMergeThreads);
+  mcfg.dynamicSmemBytes = 0;
+  err = cudaLaunchKernelEx(&mcfg, tc_merge_kernel<QT, D>, tp);
+  if (err == cudaSuccess) {
+    note_launches(1);
+  } else {
+    cudaMemsetAsync(tp.claim, 0, sizeof(int32_t), stream);  // rearm the counter ourselves
+  }
+  return err;
 }
 
 }  // namespace
@@ -1021,14 +1014,12 @@ int tc_num_warps(int num_sms, int64_t max_units) {
   return static_cast<int>(w < 1 ? 1 : w);
 }
 
-size_t tc_auto_workspace_bytes(int num_seqs, int num_kv_heads, int head_dim, int group,
-                               int num_sms) {
-  const size_t counts =
-      (static_cast<size_t>(num_seqs) * num_kv_heads * sizeof(int32_t) + 255) / 256 * 256;
+size_t tc_auto_workspace_bytes(int num_seqs, int head_dim, int group, int num_sms) {
+  const size_t prefix = ((static_cast<size_t>(num_seqs) + 1) * sizeof(int32_t) + 255) / 256 * 256;
   // two partial states per static share and per chunk (at most 2W chunks)
   const size_t W = static_cast<size_t>(num_sms) * kWarps;
   const size_t slots = 6 * W * static_cast<size_t>(group) * (head_dim + 2) * sizeof(float);
-  return counts + slots;
+  return prefix + slots;
 }
 
 cudaError_t launch_decode_tc(const DecodeParams& p, int head_dim, pa_dtype q_dtype,
@@ -1040,13 +1031,13 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int head_dim, pa_dtype q_dty
   tp.part_tiles = part_tiles;
   const int64_t tiles_max = (static_cast<int64_t>(p.max_context_len) + kTile - 1) / kTile;
   if (part_tiles == 0) {
-    tp.state = next_call_state();
-    if (tp.state == nullptr) return cudaErrorInvalidDevice;
+    tp.claim = next_claim_counter();
+    if (tp.claim == nullptr) return cudaErrorInvalidDevice;
     tp.num_warps = tc_num_warps(num_sms, static_cast<int64_t>(p.num_seqs) * p.num_kv_heads * tiles_max);
-    tp.ws_count = static_cast<int32_t*>(workspace);
+    tp.ws_prefix = static_cast<int32_t*>(workspace);
     tp.ws_slots = reinterpret_cast<float*>(
         static_cast<char*>(workspace) +
-        (static_cast<size_t>(p.num_seqs) * p.num_kv_heads * sizeof(int32_t) + 255) / 256 * 256);
+        ((static_cast<size_t>(p.num_seqs) + 1) * sizeof(int32_t) + 255) / 256 * 256);
   } else {
     const int64_t parts_max = (tiles_max + part_tiles - 1) / part_tiles;
     tp.num_warps = tc_num_warps(num_sms, static_cast<int64_t>(p.num_seqs) * p.num_kv_heads * parts_max);

@@ -136,7 +136,7 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t num
   size_t need = 0;
   const int sms = current_sm_count();
   if (sms > 0 && num_kv_heads > 0 && num_heads % num_kv_heads == 0)
-    need = pa::tc_auto_workspace_bytes(num_seqs, num_kv_heads, head_dim, num_heads / num_kv_heads, sms);
+    need = pa::tc_auto_workspace_bytes(num_seqs, head_dim, num_heads / num_kv_heads, sms);
   const int part = auto_partition(max_context_len);
   if (part > 0) {
     const size_t simt = split_workspace_bytes(num_seqs, num_heads, head_dim,
@@ -238,7 +238,7 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
   }
 
   if (tc && workspace != nullptr &&
-      workspace_bytes >= pa::tc_auto_workspace_bytes(num_seqs, num_kv_heads, head_dim, group, sms)) {
+      workspace_bytes >= pa::tc_auto_workspace_bytes(num_seqs, head_dim, group, sms)) {
     p.partition_size = 0;
     p.num_partitions = 1;
     return from_cuda(pa::launch_decode_tc(p, head_dim, q_dtype, kv_dtype, 0, workspace, sms, stream),

@@ -714,13 +714,16 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
   (void)pending;
 }
 
-// Combine the partial states of every (sequence, KV head) that several warps
-// shared: with M = max_c m_c, out = sum_c 2^(m_c-M) acc_c / sum_c 2^(m_c-M) l_c.
-// Sequences with no context get zero rows here. The contributors (the warps
-// whose tile ranges meet the segment) are taken in chunks of one per thread:
-// their slots and per-head weights go to shared memory, then every thread
-// accumulates its elements over the chunk with independent loads.
-constexpr int kMergeThreads = 128;
+// Combine the partial states of every (sequence, KV head) that several
+// ranges shared: with M = max_c m_c, out = sum_c 2^(m_c-M) acc_c / sum_c
+// 2^(m_c-M) l_c. Sequences with no context get zero rows here. Contributors
+// are taken 128 at a time (one per thread for their slots, maxima and sums);
+// the rows are float4 elements of the G x D block, and when the block has
+// fewer than 256 float4s the threads split the contributors into groups, so
+// a step issues the loads of many contributors at once. A running maximum
+// carries the online softmax across chunks of contributors.
+constexpr int kMergeThreads = 256;
+constexpr int kMergeChunk = 128;
 
 template <typename QT, int D>
 __global__ void __launch_bounds__(kMergeThreads) tc_merge_kernel(const TcParams tp) {
@@ -763,13 +766,6 @@ __global__ void __launch_bounds__(kMergeThreads) tc_merge_kernel(const TcParams 
   const int nc = static_cast<int>(nstat + ndyn);
   if (nc == 1) return;  // one range held the whole segment and wrote the rows
 
-  __shared__ float s_w[kMergeThreads][kMaxG];
-  __shared__ int s_slot[kMergeThreads];
-  __shared__ float s_red[kMergeThreads / 32][kMaxG];
-  __shared__ float s_max[kMaxG], s_inv[kMaxG];
-  const float* slots = tp.ws_slots;
-  const int stride = G * (D + 2);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // slot of contributor c: static shares first, then chunks; a range that
   // starts before the segment left it in its second slot; -1 for a warp
   // whose static share is empty (it wrote nothing)
@@ -784,101 +780,97 @@ __global__ void __launch_bounds__(kMergeThreads) tc_merge_kernel(const TcParams 
     return static_cast<int>(2 * W + 2 * k + ((c == nstat && st < seg0) ? 1 : 0));
   };
 
-  // pass 1: the largest max of each head over all contributors
-  float mx[kMaxG];
-#pragma unroll
-  for (int h = 0; h < kMaxG; ++h) mx[h] = -INFINITY;
-  for (int c = threadIdx.x; c < nc; c += kMergeThreads) {
-    const int slot = slot_of(c);
-    if (slot < 0) continue;
-#pragma unroll
-    for (int h = 0; h < kMaxG; ++h)
-      if (h < G) mx[h] = fmaxf(mx[h], slots[int64_t(slot) * stride + G * D + h]);
-  }
-#pragma unroll
-  for (int h = 0; h < kMaxG; ++h) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], off));
-    if (lane == 0) s_red[warp][h] = mx[h];
-  }
-  __syncthreads();
+  __shared__ float s_w[kMergeChunk][kMaxG];  // max of each contributor, then its weight
+  __shared__ float s_l[kMergeChunk][kMaxG];
+  __shared__ int s_slot[kMergeChunk];
+  __shared__ float s_run[kMaxG], s_den[kMaxG], s_scale[kMaxG];
+  __shared__ float4 s_part[kMergeThreads];
+  const float* slots = tp.ws_slots;
+  const int stride = G * (D + 2);
+  const int ne4 = G * D / 4;                 // float4 elements in the block: 32..256
+  const int ngrp = kMergeThreads / ne4;      // contributor groups
+  const int e4 = threadIdx.x % ne4;
+  const int grp = threadIdx.x / ne4;
+  const int he = (4 * e4) / D;               // head of this thread's elements
   if (threadIdx.x < kMaxG) {
-    float m = s_red[0][threadIdx.x];
-    for (int w = 1; w < kMergeThreads / 32; ++w) m = fmaxf(m, s_red[w][threadIdx.x]);
-    s_max[threadIdx.x] = m;
+    s_run[threadIdx.x] = -INFINITY;
+    s_den[threadIdx.x] = 0.f;
   }
-  __syncthreads();
-
-  // pass 2, one chunk of kMergeThreads contributors at a time: weights
-  // 2^(m_c - M), the denominator, and the weighted rows; a thread owns the
-  // elements threadIdx.x + k * kMergeThreads of the G x D block
-  constexpr int kPer = (kMaxG * D + kMergeThreads - 1) / kMergeThreads;
-  const int n = G * D;
-  float acc[kPer];
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int cb = 0; cb < nc; cb += kMergeChunk) {
+    const int nin = min(kMergeChunk, nc - cb);
+    if (threadIdx.x < nin) {
+      const int sl = slot_of(cb + threadIdx.x);
+      s_slot[threadIdx.x] = sl;
 #pragma unroll
-  for (int k = 0; k < kPer; ++k) acc[k] = 0.f;
-  float den[kMaxG];
-#pragma unroll
-  for (int h = 0; h < kMaxG; ++h) den[h] = 0.f;
-  for (int cb = 0; cb < nc; cb += kMergeThreads) {
-    const int c = cb + threadIdx.x;
-    const int slot = c < nc ? slot_of(c) : -1;
-    s_slot[threadIdx.x] = slot;
-#pragma unroll
-    for (int h = 0; h < kMaxG; ++h) {
-      float f = 0.f;
-      if (slot >= 0 && h < G && s_max[h] != -INFINITY) {
-        const float* sl = slots + int64_t(slot) * stride + G * D;
-        f = exp2f(sl[h] - s_max[h]);
-        den[h] += f * sl[G + h];
-      }
-      s_w[threadIdx.x][h] = f;
-    }
-    __syncthreads();
-    const int nchunk = min(kMergeThreads, nc - cb);
-    // eight contributors per step, all their loads issued before any use
-    for (int j0 = 0; j0 < nchunk; j0 += 8) {
-      float v[8][kPer];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int j = j0 + u;
-        const int sj = j < nchunk ? s_slot[j] : -1;
-        const float* sl = slots + int64_t(sj < 0 ? 0 : sj) * stride;
-#pragma unroll
-        for (int k = 0; k < kPer; ++k) {
-          const int i = threadIdx.x + k * kMergeThreads;
-          v[u][k] = (sj >= 0 && i < n) ? sl[i] : 0.f;
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int j = j0 + u < nchunk ? j0 + u : 0;
-#pragma unroll
-        for (int k = 0; k < kPer; ++k) {
-          const int i = threadIdx.x + k * kMergeThreads;
-          if (i < n) acc[k] += s_w[j][i / D] * v[u][k];
-        }
+      for (int h = 0; h < kMaxG; ++h) {
+        const bool ok = sl >= 0 && h < G;
+        s_w[threadIdx.x][h] = ok ? __ldcg(slots + int64_t(sl) * stride + G * D + h) : -INFINITY;
+        s_l[threadIdx.x][h] = ok ? __ldcg(slots + int64_t(sl) * stride + G * D + G + h) : 0.f;
       }
     }
     __syncthreads();
+    if (threadIdx.x < G) {
+      const int h = threadIdx.x;
+      float cm = -INFINITY;
+      for (int j = 0; j < nin; ++j) cm = fmaxf(cm, s_w[j][h]);
+      const float old = s_run[h];
+      const float nm = fmaxf(old, cm);
+      s_scale[h] = old == -INFINITY ? 0.f : exp2f(old - nm);
+      s_run[h] = nm;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < nin * kMaxG; i += kMergeThreads) {
+      const int j = i / kMaxG, h = i % kMaxG;
+      const float m = s_w[j][h];
+      s_w[j][h] = m == -INFINITY ? 0.f : exp2f(m - s_run[h]);
+    }
+    __syncthreads();
+    if (threadIdx.x < G) {
+      const int h = threadIdx.x;
+      float d = s_den[h] * s_scale[h];
+      for (int j = 0; j < nin; ++j) d += s_w[j][h] * s_l[j][h];
+      s_den[h] = d;
+    }
+    const float sc_e = s_scale[he];
+    acc.x *= sc_e;
+    acc.y *= sc_e;
+    acc.z *= sc_e;
+    acc.w *= sc_e;
+#pragma unroll 8
+    for (int j = grp; j < nin; j += ngrp) {
+      const int sl = s_slot[j];
+      const float wt = sl >= 0 ? s_w[j][he] : 0.f;
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(slots + int64_t(sl < 0 ? 0 : sl) * stride) + e4);
+      acc.x += wt * v.x;
+      acc.y += wt * v.y;
+      acc.z += wt * v.z;
+      acc.w += wt * v.w;
+    }
+    __syncthreads();
   }
-#pragma unroll
-  for (int h = 0; h < kMaxG; ++h) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) den[h] += __shfl_xor_sync(0xffffffffu, den[h], off);
-    if (lane == 0) s_red[warp][h] = den[h];
-  }
+  s_part[threadIdx.x] = acc;
   __syncthreads();
-  if (threadIdx.x < kMaxG) {
-    float d = 0.f;
-    for (int w = 0; w < kMergeThreads / 32; ++w) d += s_red[w][threadIdx.x];
-    s_inv[threadIdx.x] = d > 0.f ? 1.f / d : 0.f;
-  }
-  __syncthreads();
-#pragma unroll
-  for (int k = 0; k < kPer; ++k) {
-    const int i = threadIdx.x + k * kMergeThreads;
-    if (i < n) out[i] = from_float(acc[k] * s_inv[i / D], static_cast<QT*>(nullptr));
+  if (grp == 0) {
+    float4 t = acc;
+    for (int gi = 1; gi < ngrp; ++gi) {
+      const float4 u = s_part[gi * ne4 + e4];
+      t.x += u.x;
+      t.y += u.y;
+      t.z += u.z;
+      t.w += u.w;
+    }
+    const float d = s_den[he];
+    const float inv = d > 0.f ? 1.f / d : 0.f;
+    uint2 pk;
+    if constexpr (std::is_same<QT, bf16>::value) {
+      pk.x = pack_bf16(t.x * inv, t.y * inv);
+      pk.y = pack_bf16(t.z * inv, t.w * inv);
+    } else {
+      pk.x = pack_f16(t.x * inv, t.y * inv);
+      pk.y = pack_f16(t.z * inv, t.w * inv);
+    }
+    *reinterpret_cast<uint2*>(out + 4 * e4) = pk;
   }
 }
 

@@ -70,7 +70,6 @@ struct SlotMeta {
 
 struct TcParams {
   DecodeParams p;
-  int32_t* ws_prefix;  // [num_seqs + 1] tile prefix, written by CTA 0 (auto schedule)
   float* ws_slots;     // [6 * num_warps][group * (D + 2)] partial states (auto schedule)
   int32_t* claim;      // chunk counter of the auto schedule: 0 on entry, reset by the merge
   int32_t num_warps;   // warps that share the work
@@ -238,8 +237,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     s_prefP[B] = run_p;
   }
   __syncthreads();
-  if (blockIdx.x == 0 && tp.ws_prefix != nullptr)
-    for (int i = threadIdx.x; i <= B; i += kThreads) tp.ws_prefix[i] = s_prefT[i];
   griddep_launch_dependents();
 
   // ---- this warp's share of the tile list --------------------------------
@@ -715,7 +712,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
 }
 
 // Combine the partial states of every (sequence, KV head) that several
-// ranges shared: with M = max_c m_c, out = sum_c 2^(m_c-M) acc_c / sum_c
+// ranges shared (launched as a programmatic dependent of the decode grid): with M = max_c m_c, out = sum_c 2^(m_c-M) acc_c / sum_c
 // 2^(m_c-M) l_c. Sequences with no context get zero rows here. Contributors
 // are taken 128 at a time (one per thread for their slots, maxima and sums);
 // the rows are float4 elements of the G x D block, and when the block has
@@ -726,25 +723,54 @@ constexpr int kMergeThreads = 256;
 constexpr int kMergeChunk = 128;
 
 template <typename QT, int D>
-__global__ void __launch_bounds__(kMergeThreads) tc_merge_kernel(const TcParams tp) {
-  griddep_wait();
-  // the decode grid is complete: rearm its chunk counter for the next call
-  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *tp.claim = 0;
+__global__ void __launch_bounds__(kMergeThreads, 4) tc_merge_kernel(const TcParams tp) {
   const DecodeParams& p = tp.p;
+  if (blockIdx.x == 0 && blockIdx.y == 0) {
+    // the decode grid is complete: rearm its chunk counter for the next call
+    griddep_wait();
+    if (threadIdx.x == 0) *tp.claim = 0;
+  }
   const int kvh = blockIdx.x;
   const int seq = blockIdx.y;
   const int G = tp.group;
   const int Hkv = p.num_kv_heads;
   const int B = p.num_seqs;
   QT* out = static_cast<QT*>(p.out) + (static_cast<int64_t>(seq) * p.num_heads + kvh * G) * D;
-  const int tiles = tp.ws_prefix[seq + 1] - tp.ws_prefix[seq];
+
+  // Until the wait below, only inputs are read (the decode grid writes none
+  // of them): this sequence's tile offset in the list and the total, from
+  // the clamped context lengths exactly as the decode grid computes them.
+  __shared__ int s_sum[kMergeThreads / 32][2];
+  int before = 0, total = 0;
+  for (int i = threadIdx.x; i < B; i += kMergeThreads) {
+    const int tl = (clamp_context(p, i) + kTile - 1) / kTile;
+    total += tl;
+    if (i < seq) before += tl;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    before += __shfl_xor_sync(0xffffffffu, before, off);
+    total += __shfl_xor_sync(0xffffffffu, total, off);
+  }
+  if ((threadIdx.x & 31) == 0) {
+    s_sum[threadIdx.x >> 5][0] = before;
+    s_sum[threadIdx.x >> 5][1] = total;
+  }
+  __syncthreads();
+  before = total = 0;
+#pragma unroll
+  for (int w = 0; w < kMergeThreads / 32; ++w) {
+    before += s_sum[w][0];
+    total += s_sum[w][1];
+  }
+  const int tiles = (clamp_context(p, seq) + kTile - 1) / kTile;
   if (tiles == 0) {
     for (int i = threadIdx.x; i < G * D; i += kMergeThreads) out[i] = from_float(0.f, static_cast<QT*>(nullptr));
     return;
   }
-  const int64_t U = static_cast<int64_t>(tp.ws_prefix[B]) * Hkv;
+  const int64_t U = static_cast<int64_t>(total) * Hkv;
   const int64_t W = tp.num_warps;
-  const int64_t seg0 = static_cast<int64_t>(tp.ws_prefix[seq]) * Hkv + static_cast<int64_t>(kvh) * tiles;
+  const int64_t seg0 = static_cast<int64_t>(before) * Hkv + static_cast<int64_t>(kvh) * tiles;
   const int64_t seg1 = seg0 + tiles;
   const Sched sc = make_sched(U, W);
   const int64_t S = sc.S, C = sc.C;
@@ -797,10 +823,12 @@ __global__ void __launch_bounds__(kMergeThreads) tc_merge_kernel(const TcParams 
     s_den[threadIdx.x] = 0.f;
   }
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (threadIdx.x < min(kMergeChunk, nc)) s_slot[threadIdx.x] = slot_of(threadIdx.x);
+  griddep_wait();  // the decode grid's partial states are complete from here on
   for (int cb = 0; cb < nc; cb += kMergeChunk) {
     const int nin = min(kMergeChunk, nc - cb);
     if (threadIdx.x < nin) {
-      const int sl = slot_of(cb + threadIdx.x);
+      const int sl = cb == 0 ? s_slot[threadIdx.x] : slot_of(cb + threadIdx.x);
       s_slot[threadIdx.x] = sl;
 #pragma unroll
       for (int h = 0; h < kMaxG; ++h) {
@@ -1007,11 +1035,11 @@ int tc_num_warps(int num_sms, int64_t max_units) {
 }
 
 size_t tc_auto_workspace_bytes(int num_seqs, int head_dim, int group, int num_sms) {
-  const size_t prefix = ((static_cast<size_t>(num_seqs) + 1) * sizeof(int32_t) + 255) / 256 * 256;
+  (void)num_seqs;
   // two partial states per static share and per chunk (at most 2W chunks)
   const size_t W = static_cast<size_t>(num_sms) * kWarps;
   const size_t slots = 6 * W * static_cast<size_t>(group) * (head_dim + 2) * sizeof(float);
-  return prefix + slots;
+  return slots;
 }
 
 cudaError_t launch_decode_tc(const DecodeParams& p, int head_dim, pa_dtype q_dtype,
@@ -1026,10 +1054,7 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int head_dim, pa_dtype q_dty
     tp.claim = next_claim_counter();
     if (tp.claim == nullptr) return cudaErrorInvalidDevice;
     tp.num_warps = tc_num_warps(num_sms, static_cast<int64_t>(p.num_seqs) * p.num_kv_heads * tiles_max);
-    tp.ws_prefix = static_cast<int32_t*>(workspace);
-    tp.ws_slots = reinterpret_cast<float*>(
-        static_cast<char*>(workspace) +
-        ((static_cast<size_t>(p.num_seqs) + 1) * sizeof(int32_t) + 255) / 256 * 256);
+    tp.ws_slots = static_cast<float*>(workspace);
   } else {
     const int64_t parts_max = (tiles_max + part_tiles - 1) / part_tiles;
     tp.num_warps = tc_num_warps(num_sms, static_cast<int64_t>(p.num_seqs) * p.num_kv_heads * parts_max);

@@ -818,18 +818,26 @@ __global__ void __launch_bounds__(kMergeThreads, 4) tc_merge_kernel(const TcPara
   const int e4 = threadIdx.x % ne4;
   const int grp = threadIdx.x / ne4;
   const int he = (4 * e4) / D;               // head of this thread's elements
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x < kMaxG) {
     s_run[threadIdx.x] = -INFINITY;
     s_den[threadIdx.x] = 0.f;
   }
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (threadIdx.x < min(kMergeChunk, nc)) s_slot[threadIdx.x] = slot_of(threadIdx.x);
+  __syncthreads();
   griddep_wait();  // the decode grid's partial states are complete from here on
+  constexpr int kBatch = 4;  // row loads a thread keeps in flight
   for (int cb = 0; cb < nc; cb += kMergeChunk) {
     const int nin = min(kMergeChunk, nc - cb);
+    if (cb > 0) {
+      if (threadIdx.x < nin) s_slot[threadIdx.x] = slot_of(cb + threadIdx.x);
+      __syncthreads();
+    }
+    // one round of loads: each contributor's (max, sum) per head, and this
+    // thread's first kBatch rows
     if (threadIdx.x < nin) {
-      const int sl = cb == 0 ? s_slot[threadIdx.x] : slot_of(cb + threadIdx.x);
-      s_slot[threadIdx.x] = sl;
+      const int sl = s_slot[threadIdx.x];
 #pragma unroll
       for (int h = 0; h < kMaxG; ++h) {
         const bool ok = sl >= 0 && h < G;
@@ -837,43 +845,74 @@ __global__ void __launch_bounds__(kMergeThreads, 4) tc_merge_kernel(const TcPara
         s_l[threadIdx.x][h] = ok ? __ldcg(slots + int64_t(sl) * stride + G * D + G + h) : 0.f;
       }
     }
+    float4 v[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int j = grp + u * ngrp;
+      const int sl = j < nin ? s_slot[j] : -1;
+      v[u] = sl >= 0 ? __ldcg(reinterpret_cast<const float4*>(slots + int64_t(sl) * stride) + e4)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     __syncthreads();
-    if (threadIdx.x < G) {
-      const int h = threadIdx.x;
+    // per head (warp h): new running max, rescale factor, weights, sum
+    if (warp < G) {
+      const int h = warp;
       float cm = -INFINITY;
-      for (int j = 0; j < nin; ++j) cm = fmaxf(cm, s_w[j][h]);
+      for (int j = lane; j < nin; j += 32) cm = fmaxf(cm, s_w[j][h]);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, off));
       const float old = s_run[h];
       const float nm = fmaxf(old, cm);
-      s_scale[h] = old == -INFINITY ? 0.f : exp2f(old - nm);
-      s_run[h] = nm;
+      float d = 0.f;
+      for (int j = lane; j < nin; j += 32) {
+        const float m = s_w[j][h];
+        const float w = m == -INFINITY ? 0.f : exp2f(m - nm);
+        s_w[j][h] = w;
+        d += w * s_l[j][h];
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+      __syncwarp();
+      if (lane == 0) {
+        const float scale = old == -INFINITY ? 0.f : exp2f(old - nm);
+        s_scale[h] = scale;
+        s_den[h] = s_den[h] * scale + d;
+        s_run[h] = nm;
+      }
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < nin * kMaxG; i += kMergeThreads) {
-      const int j = i / kMaxG, h = i % kMaxG;
-      const float m = s_w[j][h];
-      s_w[j][h] = m == -INFINITY ? 0.f : exp2f(m - s_run[h]);
-    }
-    __syncthreads();
-    if (threadIdx.x < G) {
-      const int h = threadIdx.x;
-      float d = s_den[h] * s_scale[h];
-      for (int j = 0; j < nin; ++j) d += s_w[j][h] * s_l[j][h];
-      s_den[h] = d;
-    }
     const float sc_e = s_scale[he];
     acc.x *= sc_e;
     acc.y *= sc_e;
     acc.z *= sc_e;
     acc.w *= sc_e;
-#pragma unroll 8
-    for (int j = grp; j < nin; j += ngrp) {
-      const int sl = s_slot[j];
-      const float wt = sl >= 0 ? s_w[j][he] : 0.f;
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(slots + int64_t(sl < 0 ? 0 : sl) * stride) + e4);
-      acc.x += wt * v.x;
-      acc.y += wt * v.y;
-      acc.z += wt * v.z;
-      acc.w += wt * v.w;
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int j = grp + u * ngrp;
+      const float wt = j < nin ? s_w[j][he] : 0.f;
+      acc.x += wt * v[u].x;
+      acc.y += wt * v[u].y;
+      acc.z += wt * v[u].z;
+      acc.w += wt * v[u].w;
+    }
+    // contributors beyond the first batch of this thread
+    for (int j0 = grp + kBatch * ngrp; j0 < nin; j0 += kBatch * ngrp) {
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int j = j0 + u * ngrp;
+        const int sl = j < nin ? s_slot[j] : -1;
+        v[u] = sl >= 0 ? __ldcg(reinterpret_cast<const float4*>(slots + int64_t(sl) * stride) + e4)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int j = j0 + u * ngrp;
+        const float wt = j < nin ? s_w[j][he] : 0.f;
+        acc.x += wt * v[u].x;
+        acc.y += wt * v[u].y;
+        acc.z += wt * v[u].z;
+        acc.w += wt * v[u].w;
+      }
     }
     __syncthreads();
   }

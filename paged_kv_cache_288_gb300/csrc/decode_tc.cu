@@ -293,13 +293,27 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
   const uint32_t bar_base = smem_u32(bars + warp * NS);
 
   // block-table window: lane l holds entry win_base + l of sequence win_seq
-  int win_seq = -1, win_base = 0, win_val = -1;
-  auto table_entry = [&](int seq, int j) -> int {
+  // and, for E4M3 caches, that block's K and V scales for KV head win_kvh
+  int win_seq = -1, win_base = 0, win_val = -1, win_kvh = -1;
+  float win_ks = 1.f, win_vs = 1.f;
+  auto table_entry = [&](int seq, int kvh, int j, float& ksc, float& vsc) -> int {
     if (seq != win_seq || j < win_base || j >= win_base + 32) {
       win_seq = seq;
       win_base = j;
+      win_kvh = -1;
       const int jj = j + lane;
       win_val = jj < width ? p.block_tables[static_cast<int64_t>(seq) * width + jj] : -1;
+    }
+    if constexpr (kFp8) {
+      if (kvh != win_kvh) {
+        win_kvh = kvh;
+        const bool ok = win_val >= 0 && win_val < p.num_blocks;
+        const int64_t si = static_cast<int64_t>(ok ? win_val : 0) * Hkv + kvh;
+        win_ks = ok ? p.k_scale[si] : 1.f;
+        win_vs = ok ? p.v_scale[si] : 1.f;
+      }
+      ksc = __shfl_sync(kFull, win_ks, j - win_base);
+      vsc = __shfl_sync(kFull, win_vs, j - win_base);
     }
     return __shfl_sync(kFull, win_val, j - win_base);
   };
@@ -316,19 +330,19 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     int phys[2] = {-1, -1};
     int rows[2] = {0, 0};
     int off[2] = {0, 0};
+    float ks[2] = {1.f, 1.f}, vs[2] = {1.f, 1.f};
     if (bs >= kTile) {
-      phys[0] = table_entry(c.seq, tok0 / bs);
+      phys[0] = table_entry(c.seq, c.kvh, tok0 / bs, ks[0], vs[0]);
       rows[0] = kTile;
       off[0] = tok0 % bs;
     } else {  // block size 8: two blocks per tile
-      phys[0] = table_entry(c.seq, tok0 / bs);
+      phys[0] = table_entry(c.seq, c.kvh, tok0 / bs, ks[0], vs[0]);
       rows[0] = bs;
       if (valid > bs) {
-        phys[1] = table_entry(c.seq, tok0 / bs + 1);
+        phys[1] = table_entry(c.seq, c.kvh, tok0 / bs + 1, ks[1], vs[1]);
         rows[1] = bs;
       }
     }
-    float ks[2] = {1.f, 1.f}, vs[2] = {1.f, 1.f};
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       if (rows[h] == 0) continue;
@@ -341,11 +355,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
       }
       mask |= ((1u << nvalid) - 1u) << first;
       tx += 2u * rows[h] * Gm::kRowBytes;
-      if constexpr (kFp8) {
-        const int64_t si = static_cast<int64_t>(phys[h]) * Hkv + c.kvh;
-        ks[h] = p.k_scale[si];
-        vs[h] = p.v_scale[si];
-      }
     }
     if (lane == 0) {
       SlotMeta& m = my_meta[s];

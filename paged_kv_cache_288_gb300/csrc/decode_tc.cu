@@ -113,11 +113,6 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
 }
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
-  __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes & 0xffffu),
-                                             __NV_E4M3);
-  return static_cast<uint32_t>(r.x) | (static_cast<uint32_t>(r.y) << 16);
-}
 
 // Keep the 16-bit halves of a (token t, token t+1) register whose token holds data.
 __device__ __forceinline__ uint32_t keep_tokens(uint32_t v, uint32_t mask, int t) {
@@ -286,6 +281,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
   if (cr0 >= cr1 && !claim(cr0, cr1, cslot)) return;
 
   const int bs = p.block_size;
+  const int lbs = 31 - __clz(bs);  // block sizes are powers of two
   const int width = p.max_blocks_per_seq;
   const int Hq = p.num_heads;
   const uint32_t slot_base0 = smem_u32(slots) + warp * NS * Gm::kSlotBytes;
@@ -332,14 +328,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     int off[2] = {0, 0};
     float ks[2] = {1.f, 1.f}, vs[2] = {1.f, 1.f};
     if (bs >= kTile) {
-      phys[0] = table_entry(c.seq, c.kvh, tok0 / bs, ks[0], vs[0]);
+      phys[0] = table_entry(c.seq, c.kvh, tok0 >> lbs, ks[0], vs[0]);
       rows[0] = kTile;
-      off[0] = tok0 % bs;
+      off[0] = tok0 & (bs - 1);
     } else {  // block size 8: two blocks per tile
-      phys[0] = table_entry(c.seq, c.kvh, tok0 / bs, ks[0], vs[0]);
+      phys[0] = table_entry(c.seq, c.kvh, tok0 >> lbs, ks[0], vs[0]);
       rows[0] = bs;
       if (valid > bs) {
-        phys[1] = table_entry(c.seq, c.kvh, tok0 / bs + 1, ks[1], vs[1]);
+        phys[1] = table_entry(c.seq, c.kvh, (tok0 >> lbs) + 1, ks[1], vs[1]);
         rows[1] = bs;
       }
     }
@@ -586,10 +582,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
       for (int k = 0; k < Gm::kSteps; k += 2) {
         uint32_t r[4];
         ldsm_x4(tile_addr(kbase, lane & 15, k + (lane >> 4)), r[0], r[1], r[2], r[3]);
-        const uint32_t a0[4] = {e4m3x2_to_f16x2(r[0]), e4m3x2_to_f16x2(r[1]),
-                                e4m3x2_to_f16x2(r[0] >> 16), e4m3x2_to_f16x2(r[1] >> 16)};
-        const uint32_t a1[4] = {e4m3x2_to_f16x2(r[2]), e4m3x2_to_f16x2(r[3]),
-                                e4m3x2_to_f16x2(r[2] >> 16), e4m3x2_to_f16x2(r[3] >> 16)};
+        // a lane's four bytes of a row are d = 16c + 4tig .. +3: the low pair
+        // feeds contraction slots 2tig, 2tig+1, the high pair 2tig+8, 2tig+9
+        uint32_t a0[4], a1[4];
+        e4m3x4_to_f16x2x2(r[0], a0[0], a0[2]);
+        e4m3x4_to_f16x2x2(r[1], a0[1], a0[3]);
+        e4m3x4_to_f16x2x2(r[2], a1[0], a1[2]);
+        e4m3x4_to_f16x2x2(r[3], a1[1], a1[3]);
         mma_f16(sa, a0, qb[k][0], qb[k][1]);
         mma_f16(sb, a1, qb[k + 1][0], qb[k + 1][1]);
       }
@@ -666,11 +665,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
         ldsm_x4_trans(tile_addr(vbase, lane & 15, k + (lane >> 4)), r[0], r[1], r[2], r[3]);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const uint32_t lo = r[2 * h], hi = r[2 * h + 1];  // tokens 0-7 / 8-15 of chunk k+h
-          uint32_t a[4] = {e4m3x2_to_f16x2(__byte_perm(lo, 0, 0x0020)),
-                           e4m3x2_to_f16x2(__byte_perm(lo, 0, 0x0031)),
-                           e4m3x2_to_f16x2(__byte_perm(hi, 0, 0x0020)),
-                           e4m3x2_to_f16x2(__byte_perm(hi, 0, 0x0031))};
+          // tokens 0-7 / 8-15 of chunk k+h; bytes (t, d0), (t, d1), (t+1, d0),
+          // (t+1, d1) regrouped as (d0: t, t+1) and (d1: t, t+1)
+          uint32_t a[4];
+          e4m3x4_to_f16x2x2(__byte_perm(r[2 * h], 0, 0x3120), a[0], a[1]);
+          e4m3x4_to_f16x2x2(__byte_perm(r[2 * h + 1], 0, 0x3120), a[2], a[3]);
           if (partial) {
             a[0] = keep_tokens(a[0], mask, 2 * tig);
             a[1] = keep_tokens(a[1], mask, 2 * tig);

@@ -45,17 +45,22 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
-constexpr int kTile = 16;      // tokens per tile = MMA M
+constexpr int kRowTile = 16;   // MMA M: tokens per row tile
 constexpr int kMaxG = 8;       // MMA N
 constexpr uint32_t kFull = 0xffffffffu;
 
-template <typename KT, int D>
+// A tile is TT tokens (16 or 32, one or two MMA row tiles) of one
+// (sequence, KV head): TT rows of K and TT rows of V in one ring slot.
+template <typename KT, int D, int TT>
 struct Geom {
   static constexpr int kElem = int(sizeof(KT));
   static constexpr int kRowBytes = D * kElem;
   static constexpr int kBoxW = 128 / kElem;        // elements in one 128-byte box row
   static constexpr int kBoxes = kRowBytes / 128;   // boxes across a row
-  static constexpr int kTileBytes = kTile * kRowBytes;
+  static constexpr int kBoxBytes = TT * 128;       // one 128-byte column of the tile
+  static constexpr int kRowTiles = TT / kRowTile;
+  static constexpr uint32_t kFullMask = TT == 32 ? 0xffffffffu : 0xffffu;
+  static constexpr int kTileBytes = TT * kRowBytes;
   static constexpr int kSlotBytes = 2 * kTileBytes;
   static constexpr int kSlots = kSlotBytes >= 8192 ? 3 : 6;
   static constexpr int kSteps = D / 16;            // 16-column steps of QK^T and PV
@@ -63,8 +68,8 @@ struct Geom {
 
 struct SlotMeta {
   uint32_t mask;  // bit t: token t of the tile holds data
-  float ks0, ks1; // E4M3 K scale of tokens 0-7 and 8-15
-  float vs0, vs1; // E4M3 V scale
+  float ks[4];    // E4M3 K scale of tokens 8i .. 8i+7
+  float vs[4];    // E4M3 V scale
   uint32_t pad[3];
 };
 
@@ -98,11 +103,18 @@ __device__ __forceinline__ Sched make_sched(int64_t U, int64_t W) {
   return sc;
 }
 
-// Byte address of 16-byte chunk `chunk` of row `row` in a tile: 128-byte boxes
-// of 16 rows (8-row boxes stack to the same layout), chunks XOR-swizzled by
-// row % 8 as the TMA 128B swizzle stores them.
+// Byte address of 16-byte chunk `chunk` of row `row` in a tile whose
+// 128-byte columns are box_bytes apart (boxes of 8, 16 or 32 rows of one
+// block stack in row order), chunks XOR-swizzled by row % 8 as the TMA 128B
+// swizzle stores them.
+template <int box_bytes>
 __device__ __forceinline__ uint32_t tile_addr(uint32_t base, int row, int chunk) {
-  return base + (chunk >> 3) * 2048 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4);
+  return base + (chunk >> 3) * box_bytes + row * 128 + (((chunk & 7) ^ (row & 7)) << 4);
+}
+
+// Bits [first, first + n) set, n <= 32.
+__device__ __forceinline__ uint32_t bit_range(int first, int n) {
+  return (n >= 32 ? 0xffffffffu : ((1u << n) - 1u)) << first;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -157,11 +169,12 @@ __device__ __forceinline__ void cursor_next(Cursor& c, const int* prefT, int B, 
   if (c.seq < B) c.tiles = prefT[c.seq + 1] - prefT[c.seq];
 }
 
-template <typename QT, typename KT, int D>
+template <typename QT, typename KT, int D, int TT>
 __global__ void __launch_bounds__(kThreads, 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                  const __grid_constant__ CUtensorMap tmap_v, const TcParams tp) {
-  using Gm = Geom<KT, D>;
+  using Gm = Geom<KT, D, TT>;
+  constexpr int RT = Gm::kRowTiles;
   constexpr bool kFp8 = is_fp8<KT>::value;
   constexpr int NS = Gm::kSlots;
   const DecodeParams& p = tp.p;
@@ -196,7 +209,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
   for (int i = i0; i < i1; ++i) {
     const int ctx = clamp_context(p, i);
     s_ctx[i] = ctx;
-    const int tl = (ctx + kTile - 1) / kTile;
+    const int tl = (ctx + TT - 1) / TT;
     sum_t += tl;
     if (tp.part_tiles) sum_p += (tl + tp.part_tiles - 1) / tp.part_tiles;
   }
@@ -223,7 +236,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
   for (int i = i0; i < i1; ++i) {
     s_prefT[i] = run_t;
     s_prefP[i] = run_p;
-    const int tl = (s_ctx[i] + kTile - 1) / kTile;
+    const int tl = (s_ctx[i] + TT - 1) / TT;
     run_t += tl;
     if (tp.part_tiles) run_p += (tl + tp.part_tiles - 1) / tp.part_tiles;
   }
@@ -314,61 +327,65 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     return __shfl_sync(kFull, win_val, j - win_base);
   };
 
-  // Issue the TMA loads of the tile under `c` into slot `s` (whole warp).
+  // Issue the TMA loads of the tile under `c` into slot `s` (whole warp):
+  // one box per 128-byte column per block the tile touches (a tile lies in
+  // one block when the block holds at least TT tokens, else it spans
+  // TT / block_size blocks).
+  constexpr int kMaxSub = TT / 8;
   auto issue = [&](const Cursor& c, int s) {
     const int ctx = s_ctx[c.seq];
-    const int tok0 = c.t * kTile;
-    const int valid = min(kTile, ctx - tok0);
+    const int tok0 = c.t * TT;
+    const int valid = min(TT, ctx - tok0);
     const uint32_t kdst = slot_base0 + s * Gm::kSlotBytes;
     const uint32_t vdst = kdst + Gm::kTileBytes;
     const uint32_t bar = bar_base + s * 8;
+    const int bh = bs < TT ? bs : TT;  // rows per box
+    const int nsub = TT / bh;
     uint32_t mask = 0, tx = 0;
-    int phys[2] = {-1, -1};
-    int rows[2] = {0, 0};
-    int off[2] = {0, 0};
-    float ks[2] = {1.f, 1.f}, vs[2] = {1.f, 1.f};
-    if (bs >= kTile) {
-      phys[0] = table_entry(c.seq, c.kvh, tok0 >> lbs, ks[0], vs[0]);
-      rows[0] = kTile;
-      off[0] = tok0 & (bs - 1);
-    } else {  // block size 8: two blocks per tile
-      phys[0] = table_entry(c.seq, c.kvh, tok0 >> lbs, ks[0], vs[0]);
-      rows[0] = bs;
-      if (valid > bs) {
-        phys[1] = table_entry(c.seq, c.kvh, (tok0 >> lbs) + 1, ks[1], vs[1]);
-        rows[1] = bs;
-      }
-    }
+    int phys[kMaxSub];
+    float ks[kMaxSub], vs[kMaxSub];
+    const int off = tok0 & (bs - 1);  // 0 when the tile spans blocks
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      if (rows[h] == 0) continue;
-      const int first = h * bs;  // first token of this half in the tile
-      const int nvalid = min(rows[h], valid - first);
+    for (int h = 0; h < kMaxSub; ++h) {
+      phys[h] = -1;
+      ks[h] = vs[h] = 1.f;
+      const int first = h * bh;
+      if (h >= nsub || first >= valid) continue;
+      phys[h] = table_entry(c.seq, c.kvh, (tok0 >> lbs) + h, ks[h], vs[h]);
       if (phys[h] < 0 || phys[h] >= p.num_blocks) {
         if (lane == 0) flag_error(p.debug_err, PA_DEVERR_BLOCK_RANGE);
         phys[h] = -1;
         continue;
       }
-      mask |= ((1u << nvalid) - 1u) << first;
-      tx += 2u * rows[h] * Gm::kRowBytes;
+      mask |= bit_range(first, min(bh, valid - first));
+      tx += 2u * bh * Gm::kRowBytes;
     }
     if (lane == 0) {
       SlotMeta& m = my_meta[s];
       m.mask = mask;
-      m.ks0 = ks[0];
-      m.vs0 = vs[0];
-      m.ks1 = (bs >= kTile) ? ks[0] : ks[1];
-      m.vs1 = (bs >= kTile) ? vs[0] : vs[1];
+#pragma unroll
+      for (int i = 0; i < TT / 8; ++i) {
+        const int h = (8 * i) / bh;  // the block holding tokens 8i .. 8i+7
+        float k = ks[0], v = vs[0];
+#pragma unroll
+        for (int q = 1; q < kMaxSub; ++q)
+          if (h == q) {
+            k = ks[q];
+            v = vs[q];
+          }
+        m.ks[i] = k;
+        m.vs[i] = v;
+      }
       mbar_arrive_expect_tx(bar, tx);
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < kMaxSub; ++h) {
         if (phys[h] < 0) continue;
         const int z = phys[h] * Hkv + c.kvh;
-        const uint32_t half = h * bs * 128;  // 8-row boxes of the second block sit after the first
+        const uint32_t rows_before = h * bh * 128;  // boxes of later blocks sit after earlier ones
 #pragma unroll
         for (int b = 0; b < Gm::kBoxes; ++b) {
-          tma_load_3d(kdst + b * 2048 + half, &tmap_k, b * Gm::kBoxW, off[h], z, bar);
-          tma_load_3d(vdst + b * 2048 + half, &tmap_v, b * Gm::kBoxW, off[h], z, bar);
+          tma_load_3d(kdst + b * Gm::kBoxBytes + rows_before, &tmap_k, b * Gm::kBoxW, off, z, bar);
+          tma_load_3d(vdst + b * Gm::kBoxBytes + rows_before, &tmap_v, b * Gm::kBoxW, off, z, bar);
         }
       }
     }
@@ -567,41 +584,53 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const uint32_t kbase = slot_base0 + s * Gm::kSlotBytes;
     const uint32_t vbase = kbase + Gm::kTileBytes;
 
-    // S^T = K Q^T: rows = the tile's 16 tokens, columns = query heads
-    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-    if constexpr (!kFp8) {
+    // S^T = K Q^T per 16-token row tile: rows = tokens, columns = query heads
+    float sv[RT][4];
 #pragma unroll
-      for (int k = 0; k < Gm::kSteps; ++k) {
-        uint32_t a[4];
-        ldsm_x4(tile_addr(kbase, lane & 15, 2 * k + (lane >> 4)), a[0], a[1], a[2], a[3]);
-        if constexpr (std::is_same<KT, bf16>::value) mma_bf16((k & 1) ? sb : sa, a, qb[k][0], qb[k][1]);
-        else mma_f16((k & 1) ? sb : sa, a, qb[k][0], qb[k][1]);
-      }
-    } else {
+    for (int rt = 0; rt < RT; ++rt) {
+      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+      const int row = rt * kRowTile + (lane & 15);
+      if constexpr (!kFp8) {
 #pragma unroll
-      for (int k = 0; k < Gm::kSteps; k += 2) {
-        uint32_t r[4];
-        ldsm_x4(tile_addr(kbase, lane & 15, k + (lane >> 4)), r[0], r[1], r[2], r[3]);
-        // a lane's four bytes of a row are d = 16c + 4tig .. +3: the low pair
-        // feeds contraction slots 2tig, 2tig+1, the high pair 2tig+8, 2tig+9
-        uint32_t a0[4], a1[4];
-        e4m3x4_to_f16x2x2(r[0], a0[0], a0[2]);
-        e4m3x4_to_f16x2x2(r[1], a0[1], a0[3]);
-        e4m3x4_to_f16x2x2(r[2], a1[0], a1[2]);
-        e4m3x4_to_f16x2x2(r[3], a1[1], a1[3]);
-        mma_f16(sa, a0, qb[k][0], qb[k][1]);
-        mma_f16(sb, a1, qb[k + 1][0], qb[k + 1][1]);
+        for (int k = 0; k < Gm::kSteps; ++k) {
+          uint32_t a[4];
+          ldsm_x4(tile_addr<Gm::kBoxBytes>(kbase, row, 2 * k + (lane >> 4)), a[0], a[1], a[2], a[3]);
+          if constexpr (std::is_same<KT, bf16>::value) mma_bf16((k & 1) ? sb : sa, a, qb[k][0], qb[k][1]);
+          else mma_f16((k & 1) ? sb : sa, a, qb[k][0], qb[k][1]);
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < Gm::kSteps; k += 2) {
+          uint32_t r[4];
+          ldsm_x4(tile_addr<Gm::kBoxBytes>(kbase, row, k + (lane >> 4)), r[0], r[1], r[2], r[3]);
+          // a lane's four bytes of a row are d = 16c + 4tig .. +3: the low pair
+          // feeds contraction slots 2tig, 2tig+1, the high pair 2tig+8, 2tig+9
+          uint32_t a0[4], a1[4];
+          e4m3x4_to_f16x2x2(r[0], a0[0], a0[2]);
+          e4m3x4_to_f16x2x2(r[1], a0[1], a0[3]);
+          e4m3x4_to_f16x2x2(r[2], a1[0], a1[2]);
+          e4m3x4_to_f16x2x2(r[3], a1[1], a1[3]);
+          mma_f16(sa, a0, qb[k][0], qb[k][1]);
+          mma_f16(sb, a1, qb[k + 1][0], qb[k + 1][1]);
+        }
       }
+      const float sc0 = p.scale_log2 * mt.ks[2 * rt], sc1 = p.scale_log2 * mt.ks[2 * rt + 1];
+      sv[rt][0] = (sa[0] + sb[0]) * sc0;
+      sv[rt][1] = (sa[1] + sb[1]) * sc0;
+      sv[rt][2] = (sa[2] + sb[2]) * sc1;
+      sv[rt][3] = (sa[3] + sb[3]) * sc1;
     }
-    const float sc0 = p.scale_log2 * mt.ks0, sc1 = p.scale_log2 * mt.ks1;
-    float s0 = (sa[0] + sb[0]) * sc0, s1 = (sa[1] + sb[1]) * sc0;
-    float s2 = (sa[2] + sb[2]) * sc1, s3 = (sa[3] + sb[3]) * sc1;
     const uint32_t mask = mt.mask;
-    if (!((mask >> g) & 1u)) s0 = s1 = -INFINITY;
-    if (!((mask >> (g + 8)) & 1u)) s2 = s3 = -INFINITY;
+    float x0 = -INFINITY, x1 = -INFINITY;
+#pragma unroll
+    for (int rt = 0; rt < RT; ++rt) {
+      if (!((mask >> (rt * kRowTile + g)) & 1u)) sv[rt][0] = sv[rt][1] = -INFINITY;
+      if (!((mask >> (rt * kRowTile + g + 8)) & 1u)) sv[rt][2] = sv[rt][3] = -INFINITY;
+      x0 = fmaxf(x0, fmaxf(sv[rt][0], sv[rt][2]));
+      x1 = fmaxf(x1, fmaxf(sv[rt][1], sv[rt][3]));
+    }
 
     // online softmax (log2 units), per head column
-    float x0 = fmaxf(s0, s2), x1 = fmaxf(s1, s3);
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
       x0 = fmaxf(x0, __shfl_xor_sync(kFull, x0, off));
@@ -623,60 +652,70 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
       }
     }
     const float b0 = m0 == -INFINITY ? 0.f : m0, b1 = m1 == -INFINITY ? 0.f : m1;
-    const float p0 = exp2f(s0 - b0), p1 = exp2f(s1 - b1);
-    const float p2 = exp2f(s2 - b0), p3 = exp2f(s3 - b1);
-    l0 += p0 + p2;
-    l1 += p1 + p3;
-
-    // P^T as the B operand: transpose the accumulator-layout rows
-    uint32_t pb0, pb1;
-    if constexpr (std::is_same<KT, bf16>::value) {
-      pb0 = movmatrix_trans(pack_bf16(p0, p1));
-      pb1 = movmatrix_trans(pack_bf16(p2, p3));
-    } else if constexpr (!kFp8) {
-      pb0 = movmatrix_trans(pack_f16(p0, p1));
-      pb1 = movmatrix_trans(pack_f16(p2, p3));
-    } else {
-      pb0 = movmatrix_trans(pack_f16(p0 * mt.vs0, p1 * mt.vs0));
-      pb1 = movmatrix_trans(pack_f16(p2 * mt.vs1, p3 * mt.vs1));
+    // P^T of each row tile as B operands: transpose the accumulator-layout rows
+    uint32_t pb[RT][2];
+#pragma unroll
+    for (int rt = 0; rt < RT; ++rt) {
+      const float p0 = exp2f(sv[rt][0] - b0), p1 = exp2f(sv[rt][1] - b1);
+      const float p2 = exp2f(sv[rt][2] - b0), p3 = exp2f(sv[rt][3] - b1);
+      l0 += p0 + p2;
+      l1 += p1 + p3;
+      if constexpr (std::is_same<KT, bf16>::value) {
+        pb[rt][0] = movmatrix_trans(pack_bf16(p0, p1));
+        pb[rt][1] = movmatrix_trans(pack_bf16(p2, p3));
+      } else if constexpr (!kFp8) {
+        pb[rt][0] = movmatrix_trans(pack_f16(p0, p1));
+        pb[rt][1] = movmatrix_trans(pack_f16(p2, p3));
+      } else {
+        const float v0 = mt.vs[2 * rt], v1 = mt.vs[2 * rt + 1];
+        pb[rt][0] = movmatrix_trans(pack_f16(p0 * v0, p1 * v0));
+        pb[rt][1] = movmatrix_trans(pack_f16(p2 * v1, p3 * v1));
+      }
     }
 
-    // O^T += V^T P^T, one 16-row step of d at a time
-    const bool partial = mask != 0xffffu;
-    if constexpr (!kFp8) {
+    // O^T += V^T P^T: each row tile is one 16-token contraction step,
+    // one 16-row step of d at a time
+    const bool partial = mask != Gm::kFullMask;
 #pragma unroll
-      for (int k = 0; k < Gm::kSteps; ++k) {
-        uint32_t a[4];
-        ldsm_x4_trans(tile_addr(vbase, (lane & 7) + ((lane >> 4) << 3), 2 * k + ((lane >> 3) & 1)),
-                      a[0], a[1], a[2], a[3]);
-        if (partial) {
-          a[0] = keep_tokens(a[0], mask, 2 * tig);
-          a[1] = keep_tokens(a[1], mask, 2 * tig);
-          a[2] = keep_tokens(a[2], mask, 2 * tig + 8);
-          a[3] = keep_tokens(a[3], mask, 2 * tig + 8);
-        }
-        if constexpr (std::is_same<KT, bf16>::value) mma_bf16(o[k], a, pb0, pb1);
-        else mma_f16(o[k], a, pb0, pb1);
-      }
-    } else {
+    for (int rt = 0; rt < RT; ++rt) {
+      const int t0 = rt * kRowTile;
+      if constexpr (!kFp8) {
 #pragma unroll
-      for (int k = 0; k < Gm::kSteps; k += 2) {
-        uint32_t r[4];
-        ldsm_x4_trans(tile_addr(vbase, lane & 15, k + (lane >> 4)), r[0], r[1], r[2], r[3]);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          // tokens 0-7 / 8-15 of chunk k+h; bytes (t, d0), (t, d1), (t+1, d0),
-          // (t+1, d1) regrouped as (d0: t, t+1) and (d1: t, t+1)
+        for (int k = 0; k < Gm::kSteps; ++k) {
           uint32_t a[4];
-          e4m3x4_to_f16x2x2(__byte_perm(r[2 * h], 0, 0x3120), a[0], a[1]);
-          e4m3x4_to_f16x2x2(__byte_perm(r[2 * h + 1], 0, 0x3120), a[2], a[3]);
+          ldsm_x4_trans(tile_addr<Gm::kBoxBytes>(vbase, t0 + (lane & 7) + ((lane >> 4) << 3),
+                                                 2 * k + ((lane >> 3) & 1)),
+                        a[0], a[1], a[2], a[3]);
           if (partial) {
-            a[0] = keep_tokens(a[0], mask, 2 * tig);
-            a[1] = keep_tokens(a[1], mask, 2 * tig);
-            a[2] = keep_tokens(a[2], mask, 2 * tig + 8);
-            a[3] = keep_tokens(a[3], mask, 2 * tig + 8);
+            a[0] = keep_tokens(a[0], mask, t0 + 2 * tig);
+            a[1] = keep_tokens(a[1], mask, t0 + 2 * tig);
+            a[2] = keep_tokens(a[2], mask, t0 + 2 * tig + 8);
+            a[3] = keep_tokens(a[3], mask, t0 + 2 * tig + 8);
           }
-          mma_f16(o[k + h], a, pb0, pb1);
+          if constexpr (std::is_same<KT, bf16>::value) mma_bf16(o[k], a, pb[rt][0], pb[rt][1]);
+          else mma_f16(o[k], a, pb[rt][0], pb[rt][1]);
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < Gm::kSteps; k += 2) {
+          uint32_t r[4];
+          ldsm_x4_trans(tile_addr<Gm::kBoxBytes>(vbase, t0 + (lane & 15), k + (lane >> 4)),
+                        r[0], r[1], r[2], r[3]);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            // tokens 0-7 / 8-15 of chunk k+h; bytes (t, d0), (t, d1), (t+1, d0),
+            // (t+1, d1) regrouped as (d0: t, t+1) and (d1: t, t+1)
+            uint32_t a[4];
+            e4m3x4_to_f16x2x2(__byte_perm(r[2 * h], 0, 0x3120), a[0], a[1]);
+            e4m3x4_to_f16x2x2(__byte_perm(r[2 * h + 1], 0, 0x3120), a[2], a[3]);
+            if (partial) {
+              a[0] = keep_tokens(a[0], mask, t0 + 2 * tig);
+              a[1] = keep_tokens(a[1], mask, t0 + 2 * tig);
+              a[2] = keep_tokens(a[2], mask, t0 + 2 * tig + 8);
+              a[3] = keep_tokens(a[3], mask, t0 + 2 * tig + 8);
+            }
+            mma_f16(o[k + h], a, pb[rt][0], pb[rt][1]);
+          }
         }
       }
     }
@@ -730,7 +769,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
 constexpr int kMergeThreads = 256;
 constexpr int kMergeChunk = 128;
 
-template <typename QT, int D>
+template <typename QT, int D, int TT>
 __global__ void __launch_bounds__(kMergeThreads, 4) tc_merge_kernel(const TcParams tp) {
   const DecodeParams& p = tp.p;
   if (blockIdx.x == 0 && blockIdx.y == 0) {
@@ -751,7 +790,7 @@ __global__ void __launch_bounds__(kMergeThreads, 4) tc_merge_kernel(const TcPara
   __shared__ int s_sum[kMergeThreads / 32][2];
   int before = 0, total = 0;
   for (int i = threadIdx.x; i < B; i += kMergeThreads) {
-    const int tl = (clamp_context(p, i) + kTile - 1) / kTile;
+    const int tl = (clamp_context(p, i) + TT - 1) / TT;
     total += tl;
     if (i < seq) before += tl;
   }
@@ -771,7 +810,7 @@ __global__ void __launch_bounds__(kMergeThreads, 4) tc_merge_kernel(const TcPara
     before += s_sum[w][0];
     total += s_sum[w][1];
   }
-  const int tiles = (clamp_context(p, seq) + kTile - 1) / kTile;
+  const int tiles = (clamp_context(p, seq) + TT - 1) / TT;
   if (tiles == 0) {
     for (int i = threadIdx.x; i < G * D; i += kMergeThreads) out[i] = from_float(0.f, static_cast<QT*>(nullptr));
     return;
@@ -994,7 +1033,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // 3-D view of a cache: (d, token in block, block x KV head), boxes of 128
 // bytes x min(block_size, 16) rows x 1, 128-byte swizzle.
 bool make_cache_map(CUtensorMap* map, const void* base, int head_dim, int elem, int block_size,
-                    int64_t blocks_x_heads) {
+                    int tile_tokens, int64_t blocks_x_heads) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(block_size),
@@ -1002,7 +1041,7 @@ bool make_cache_map(CUtensorMap* map, const void* base, int head_dim, int elem, 
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * elem,
                            static_cast<cuuint64_t>(head_dim) * elem * block_size};
   cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elem),
-                       static_cast<cuuint32_t>(block_size < kTile ? block_size : kTile), 1};
+                       static_cast<cuuint32_t>(block_size < tile_tokens ? block_size : tile_tokens), 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, elem == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 3,
                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -1011,27 +1050,27 @@ bool make_cache_map(CUtensorMap* map, const void* base, int head_dim, int elem, 
   return r == CUDA_SUCCESS;
 }
 
-template <typename QT, typename KT, int D>
+template <typename QT, typename KT, int D, int TT>
 size_t smem_bytes(int num_seqs) {
-  using Gm = Geom<KT, D>;
+  using Gm = Geom<KT, D, TT>;
   return 1024 + static_cast<size_t>(kWarps) * Gm::kSlots * (Gm::kSlotBytes + sizeof(SlotMeta) + 8) +
          (3 * static_cast<size_t>(num_seqs) + 2) * sizeof(int);
 }
 
-template <typename QT, typename KT, int D>
+template <typename QT, typename KT, int D, int TT>
 cudaError_t launch_typed(const TcParams& tp, const void* k_cache, const void* v_cache, int num_sms,
                          cudaStream_t stream) {
   const DecodeParams& p = tp.p;
   CUtensorMap mk, mv;
   const int64_t bxh = static_cast<int64_t>(p.num_blocks) * p.num_kv_heads;
-  if (!make_cache_map(&mk, k_cache, D, int(sizeof(KT)), p.block_size, bxh) ||
-      !make_cache_map(&mv, v_cache, D, int(sizeof(KT)), p.block_size, bxh))
+  if (!make_cache_map(&mk, k_cache, D, int(sizeof(KT)), p.block_size, TT, bxh) ||
+      !make_cache_map(&mv, v_cache, D, int(sizeof(KT)), p.block_size, TT, bxh))
     return cudaErrorInvalidValue;
-  auto kernel = decode_tc_kernel<QT, KT, D>;
+  auto kernel = decode_tc_kernel<QT, KT, D, TT>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem_bytes<QT, KT, D>(kTcMaxSeqs)));
+                                         static_cast<int>(smem_bytes<QT, KT, D, TT>(kTcMaxSeqs)));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -1043,7 +1082,7 @@ cudaError_t launch_typed(const TcParams& tp, const void* k_cache, const void* v_
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem_bytes<QT, KT, D>(p.num_seqs);
+  cfg.dynamicSmemBytes = smem_bytes<QT, KT, D, TT>(p.num_seqs);
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
@@ -1057,7 +1096,7 @@ cudaError_t launch_typed(const TcParams& tp, const void* k_cache, const void* v_
   mcfg.gridDim = dim3(p.num_kv_heads, p.num_seqs);
   mcfg.blockDim = dim3(kMergeThreads);
   mcfg.dynamicSmemBytes = 0;
-  err = cudaLaunchKernelEx(&mcfg, tc_merge_kernel<QT, D>, tp);
+  err = cudaLaunchKernelEx(&mcfg, tc_merge_kernel<QT, D, TT>, tp);
   if (err == cudaSuccess) {
     note_launches(1);
   } else {
@@ -1068,9 +1107,14 @@ cudaError_t launch_typed(const TcParams& tp, const void* k_cache, const void* v_
 
 }  // namespace
 
-bool tc_supported(int group, int head_dim, pa_dtype kv_dtype, int num_seqs) {
+// E4M3 tiles carry half the bytes of 16-bit ones, so they take 32 tokens per
+// pipeline step to keep the same work per step.
+int tc_tile_tokens(pa_dtype kv_dtype) { return kv_dtype == PA_FP8_E4M3 ? 32 : 16; }
+
+bool tc_supported(int group, int head_dim, pa_dtype kv_dtype, int num_seqs, int partition_size) {
   if (group != 2 && group != 4 && group != 8) return false;
   if (num_seqs > kTcMaxSeqs) return false;
+  if (partition_size % tc_tile_tokens(kv_dtype) != 0) return false;
   if (kv_dtype == PA_FP8_E4M3) return head_dim == 128;
   return head_dim == 64 || head_dim == 128;
 }
@@ -1090,13 +1134,15 @@ size_t tc_auto_workspace_bytes(int num_seqs, int head_dim, int group, int num_sm
 }
 
 cudaError_t launch_decode_tc(const DecodeParams& p, int head_dim, pa_dtype q_dtype,
-                             pa_dtype kv_dtype, int part_tiles, void* workspace, int num_sms,
+                             pa_dtype kv_dtype, int partition_size, void* workspace, int num_sms,
                              cudaStream_t stream) {
+  const int tt = tc_tile_tokens(kv_dtype);
+  const int part_tiles = partition_size / tt;
   TcParams tp{};
   tp.p = p;
   tp.group = p.num_heads / p.num_kv_heads;
   tp.part_tiles = part_tiles;
-  const int64_t tiles_max = (static_cast<int64_t>(p.max_context_len) + kTile - 1) / kTile;
+  const int64_t tiles_max = (static_cast<int64_t>(p.max_context_len) + tt - 1) / tt;
   if (part_tiles == 0) {
     tp.claim = next_claim_counter();
     if (tp.claim == nullptr) return cudaErrorInvalidDevice;
@@ -1109,15 +1155,15 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int head_dim, pa_dtype q_dty
   const void* kc = p.k_cache;
   const void* vc = p.v_cache;
   if (kv_dtype == PA_BF16) {
-    if (head_dim == 128) return launch_typed<bf16, bf16, 128>(tp, kc, vc, num_sms, stream);
-    return launch_typed<bf16, bf16, 64>(tp, kc, vc, num_sms, stream);
+    if (head_dim == 128) return launch_typed<bf16, bf16, 128, 16>(tp, kc, vc, num_sms, stream);
+    return launch_typed<bf16, bf16, 64, 16>(tp, kc, vc, num_sms, stream);
   }
   if (kv_dtype == PA_F16) {
-    if (head_dim == 128) return launch_typed<f16, f16, 128>(tp, kc, vc, num_sms, stream);
-    return launch_typed<f16, f16, 64>(tp, kc, vc, num_sms, stream);
+    if (head_dim == 128) return launch_typed<f16, f16, 128, 16>(tp, kc, vc, num_sms, stream);
+    return launch_typed<f16, f16, 64, 16>(tp, kc, vc, num_sms, stream);
   }
-  if (q_dtype == PA_BF16) return launch_typed<bf16, fp8, 128>(tp, kc, vc, num_sms, stream);
-  return launch_typed<f16, fp8, 128>(tp, kc, vc, num_sms, stream);
+  if (q_dtype == PA_BF16) return launch_typed<bf16, fp8, 128, 32>(tp, kc, vc, num_sms, stream);
+  return launch_typed<f16, fp8, 128, 32>(tp, kc, vc, num_sms, stream);
 }
 
 }  // namespace pa

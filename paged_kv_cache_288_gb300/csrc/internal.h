@@ -37,15 +37,15 @@ cudaError_t launch_decode_simt(const DecodeParams& p, int head_dim, pa_dtype q_d
 cudaError_t launch_reduce_partitions(const DecodeParams& p, int head_dim, pa_dtype q_dtype,
                                      bool pdl, cudaStream_t stream);
 
-// Tensor-core decode (GQA groups of 2/4/8). part_tiles = 0: balanced schedule
+// Tensor-core decode (GQA groups of 2/4/8). partition_size = 0: balanced schedule
 // over all warps of the GPU with partial states merged by a second kernel
-// (workspace of tc_auto_workspace_bytes); part_tiles > 0: split path with
-// partitions of part_tiles * 16 tokens into p.ws_acc / p.ws_ml.
+// (workspace of tc_auto_workspace_bytes); partition_size > 0: split path
+// with partitions of that many tokens into p.ws_acc / p.ws_ml.
 constexpr int kTcMaxSeqs = 2048;
-bool tc_supported(int group, int head_dim, pa_dtype kv_dtype, int num_seqs);
+bool tc_supported(int group, int head_dim, pa_dtype kv_dtype, int num_seqs, int partition_size);
 size_t tc_auto_workspace_bytes(int num_seqs, int head_dim, int group, int num_sms);
 cudaError_t launch_decode_tc(const DecodeParams& p, int head_dim, pa_dtype q_dtype,
-                             pa_dtype kv_dtype, int part_tiles, void* workspace, int num_sms,
+                             pa_dtype kv_dtype, int partition_size, void* workspace, int num_sms,
                              cudaStream_t stream);
 
 }  // namespace pa

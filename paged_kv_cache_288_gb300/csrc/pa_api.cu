@@ -209,7 +209,7 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
   p.scale_log2 = scale * pa::kLog2e;
 
   const int group = num_heads / num_kv_heads;
-  const bool tc = pa::tc_supported(group, head_dim, kv_dtype, num_seqs);
+  const bool tc = pa::tc_supported(group, head_dim, kv_dtype, num_seqs, partition_size > 0 ? partition_size : 0);
   if (partition_size > 0) {
     const int nparts = num_partitions_for(max_context_len, partition_size);
     const size_t need = split_workspace_bytes(num_seqs, num_heads, head_dim, nparts);
@@ -230,7 +230,7 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
     p.ws_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                        ((slots * head_dim * sizeof(float)) + 255) / 256 * 256);
     if (tc)
-      return from_cuda(pa::launch_decode_tc(p, head_dim, q_dtype, kv_dtype, partition_size / 16,
+      return from_cuda(pa::launch_decode_tc(p, head_dim, q_dtype, kv_dtype, partition_size,
                                             nullptr, sms, stream),
                        "decode launch");
     return from_cuda(pa::launch_decode_simt(p, head_dim, q_dtype, kv_dtype, stream),

@@ -46,18 +46,27 @@ L2_FLUSH_BYTES = 256 << 20
 # workloads and their algorithmic bytes
 
 
+def rank_seed(base, rank):
+    """Each rank runs its own replica batch of the same shape."""
+    return base + 10007 * rank
+
+
 def make_case(name, rank):
-    seed_shift = 10007 * rank  # each rank gets its own replica batch of the same shape
     if name == "llama8b":
-        return workloads.llama8b(seed=1002 + seed_shift)
+        return workloads.llama8b(seed=rank_seed(1002, rank))
     if name == "shared_prefix":
-        return workloads.shared_prefix(seed=1003 + seed_shift)
+        return workloads.shared_prefix(seed=rank_seed(1003, rank))
     if name.startswith("long_context"):
         bs = int(name.split("bs")[-1]) if "bs" in name else 16
-        return workloads.long_context(bs, seed=1004 + seed_shift)
+        return workloads.long_context(bs, seed=rank_seed(1004, rank))
     if name == "fp8_layer":
-        return workloads.fp8_step_layer(0, seed=1005 + seed_shift)
+        return workloads.fp8_step_layer(0, seed=rank_seed(1005, rank))
     raise ValueError(name)
+
+
+def job_throughput_gbs(bytes_per_step, steps, world, max_total_ms):
+    """Whole-job GB/s: every rank's bytes over the slowest rank's time."""
+    return world * bytes_per_step * steps / (max_total_ms / 1e3) / 1e9
 
 
 def elem(dtype):
@@ -360,8 +369,8 @@ def run_ours(args, world, rank, local):
                             device)
 
     bytes_step = decode_bytes(case) + write_bytes(case)
-    value = world * bytes_step * K / (total_ms / 1e3) / 1e9
-    e2e_value = world * bytes_step * Ke / (e2e_ms / 1e3) / 1e9
+    value = job_throughput_gbs(bytes_step, K, world, total_ms)
+    e2e_value = job_throughput_gbs(bytes_step, Ke, world, e2e_ms)
     dbytes = decode_bytes(case)
     achieved = dbytes / (dec_mean_ms / 1e3) / 1e9
     peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")

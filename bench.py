@@ -21,6 +21,7 @@ during a timed step).
 """
 
 import argparse
+import hashlib
 import json
 import math
 import os
@@ -40,6 +41,35 @@ import workloads  # noqa: E402
 
 METRIC = "pa_decode KV GB/s and decode tokens/s per layer; % of GB300 HBM roofline"
 L2_FLUSH_BYTES = 256 << 20
+# DRAM bytes of one pa_decode call measured by ncu, valid while these
+# sources are unchanged (their hash is stored beside the numbers)
+TRAFFIC_PATH = os.path.join(ROOT, "profiles", "traffic.json")
+TRAFFIC_SOURCES = ("paged_kv_cache_288_gb300/csrc/decode_tc.cu",
+                   "paged_kv_cache_288_gb300/csrc/ptx.cuh",
+                   "paged_kv_cache_288_gb300/csrc/common.cuh",
+                   "paged_kv_cache_288_gb300/csrc/pa_api.cu")
+
+
+def kernel_sources_hash():
+    h = hashlib.sha256()
+    for rel in TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload, partition_size):
+    """ncu DRAM bytes (read + write) per pa_decode call, or None when no capture
+    of the current kernel sources exists for this workload."""
+    try:
+        with open(TRAFFIC_PATH) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("sources_sha256") != kernel_sources_hash():
+        return None
+    w = rec.get("workloads", {}).get(f"{workload}/p{partition_size}")
+    return None if w is None else int(w["bytes_per_call"])
 
 
 # ----------------------------------------------------------------------------
@@ -412,7 +442,8 @@ def run_ours(args, world, rank, local):
         "step_bytes": bytes_step,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": None, "kernel": "pa_decode"},
+                     "traffic": recorded_traffic(args.workload, part),
+                     "kernel": "pa_decode (every kernel of the call)"},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": Ke},
         "clocks": sampler.summary(t0, t1),

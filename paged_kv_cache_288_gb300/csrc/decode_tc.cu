@@ -766,11 +766,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
 // fewer than 256 float4s the threads split the contributors into groups, so
 // a step issues the loads of many contributors at once. A running maximum
 // carries the online softmax across chunks of contributors.
+// Threads of a merge CTA: 256, or 1024 when there are few pairs (their
+// contributor lists are then long, and more threads keep more rows in flight).
 constexpr int kMergeThreads = 256;
-constexpr int kMergeChunk = 128;
+constexpr int kMergeThreadsFew = 1024;
 
-template <typename QT, int D, int TT>
-__global__ void __launch_bounds__(kMergeThreads, 4) tc_merge_kernel(const TcParams tp) {
+template <typename QT, int D, int TT, int NT>
+__global__ void __launch_bounds__(NT, 1024 / NT) tc_merge_kernel(const TcParams tp) {
+  constexpr int kMergeThreads = NT;
+  constexpr int kMergeChunk = NT >= 512 ? 256 : 128;  // contributors taken at a time
   const DecodeParams& p = tp.p;
   if (blockIdx.x == 0 && blockIdx.y == 0) {
     // the decode grid is complete: rearm its chunk counter for the next call
@@ -1075,7 +1079,6 @@ cudaError_t launch_typed(const TcParams& tp, const void* k_cache, const void* v_
     attr_set = true;
   }
   const int grid = (tp.num_warps + kWarps - 1) / kWarps;
-  (void)num_sms;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -1094,9 +1097,14 @@ cudaError_t launch_typed(const TcParams& tp, const void* k_cache, const void* v_
                                     /*pdl=*/true, stream);
   cudaLaunchConfig_t mcfg = cfg;
   mcfg.gridDim = dim3(p.num_kv_heads, p.num_seqs);
-  mcfg.blockDim = dim3(kMergeThreads);
   mcfg.dynamicSmemBytes = 0;
-  err = cudaLaunchKernelEx(&mcfg, tc_merge_kernel<QT, D, TT>, tp);
+  if (static_cast<int64_t>(p.num_seqs) * p.num_kv_heads <= num_sms) {
+    mcfg.blockDim = dim3(kMergeThreadsFew);
+    err = cudaLaunchKernelEx(&mcfg, tc_merge_kernel<QT, D, TT, kMergeThreadsFew>, tp);
+  } else {
+    mcfg.blockDim = dim3(kMergeThreads);
+    err = cudaLaunchKernelEx(&mcfg, tc_merge_kernel<QT, D, TT, kMergeThreads>, tp);
+  }
   if (err == cudaSuccess) {
     note_launches(1);
   } else {

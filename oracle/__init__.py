@@ -38,6 +38,7 @@ from .paged_attention import (
     bits_to_f64,
     reshape_and_cache,
     copy_blocks,
+    swap_blocks,
     gather_sequence,
     paged_decode,
     paged_decode_partitioned,
@@ -58,6 +59,7 @@ __all__ = [
     "bits_to_f64",
     "reshape_and_cache",
     "copy_blocks",
+    "swap_blocks",
     "gather_sequence",
     "paged_decode",
     "paged_decode_partitioned",

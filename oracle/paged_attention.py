@@ -94,6 +94,29 @@ def copy_blocks(k_caches, v_caches, block_mapping):
             vc[int(dst)] = vc[int(src)]
 
 
+def swap_blocks(dst_k, dst_v, src_k, src_v, block_mapping):
+    """Move whole blocks, K and V, in every layer, from the src pools to the
+    dst pools (lists of per-layer arrays [num_blocks, ...]).
+
+    serving-paged-attention, section "그래도 넘칠 때 — 선점": when the pool has
+    no free block left, a request is preempted; the swap way moves its blocks
+    to CPU memory and later back, so nothing is recomputed. Each (src, dst)
+    pair of ``block_mapping`` copies block src of every src pool to block dst
+    of the matching dst pool. Returns the pairs skipped because an index lies
+    outside its pool (the library flags those and leaves them untouched).
+    """
+    skipped = []
+    for src, dst in block_mapping:
+        src, dst = int(src), int(dst)
+        if not (0 <= src < src_k[0].shape[0] and 0 <= dst < dst_k[0].shape[0]):
+            skipped.append((src, dst))
+            continue
+        for layer in range(len(src_k)):
+            dst_k[layer][dst] = src_k[layer][src]
+            dst_v[layer][dst] = src_v[layer][src]
+    return skipped
+
+
 def gather_sequence(cache, table_row, context_len, block_size, kv_head,
                     kv_dtype, scale=None):
     """One sequence's K (or V) rows for one KV head, in logical order, float64.

@@ -224,6 +224,58 @@ def test_copy_blocks_copies_every_layer_and_nothing_else():
             assert np.array_equal(vs[L][b], v0[L][b])
 
 
+def _block_bytes(pool, b):
+    """Block b of a pool read through a flat byte view at its byte offset (an
+    indexing route independent of the oracle's per-block assignment)."""
+    flat = pool.reshape(-1).view(np.uint8)
+    n = flat.size // pool.shape[0]
+    return flat[b * n:(b + 1) * n]
+
+
+def test_swap_out_then_in_restores_the_request():
+    """Swap-out copies the preempted request's blocks to the host pool byte for
+    byte, swap-in brings them back into other device blocks: the round trip is
+    the identity on those bytes, and no other block of either pool changes."""
+    rng = np.random.default_rng(3)
+    L, Nd, Nh = 3, 9, 5
+    dk = [rng.integers(0, 65535, (Nd, 2, 4, 8), dtype=np.uint16) for _ in range(L)]
+    dv = [rng.integers(0, 65535, (Nd, 2, 4, 8), dtype=np.uint16) for _ in range(L)]
+    hk = [rng.integers(0, 65535, (Nh, 2, 4, 8), dtype=np.uint16) for _ in range(L)]
+    hv = [rng.integers(0, 65535, (Nh, 2, 4, 8), dtype=np.uint16) for _ in range(L)]
+    dk0, dv0 = [x.copy() for x in dk], [x.copy() for x in dv]
+    hk0, hv0 = [x.copy() for x in hk], [x.copy() for x in hv]
+    out_pairs = [(7, 0), (2, 3), (5, 4)]
+    assert oracle.swap_blocks(hk, hv, dk, dv, out_pairs) == []
+    for layer in range(L):
+        for s, d in out_pairs:
+            assert np.array_equal(_block_bytes(hk[layer], d), _block_bytes(dk0[layer], s))
+            assert np.array_equal(_block_bytes(hv[layer], d), _block_bytes(dv0[layer], s))
+        for b in (1, 2):
+            assert np.array_equal(_block_bytes(hk[layer], b), _block_bytes(hk0[layer], b))
+        for b in range(Nd):
+            assert np.array_equal(_block_bytes(dk[layer], b), _block_bytes(dk0[layer], b))
+    in_pairs = [(0, 1), (3, 8), (4, 6)]
+    oracle.swap_blocks(dk, dv, hk, hv, in_pairs)
+    for layer in range(L):
+        for (s, _), (_, d) in zip(out_pairs, in_pairs):
+            assert np.array_equal(_block_bytes(dk[layer], d), _block_bytes(dk0[layer], s))
+            assert np.array_equal(_block_bytes(dv[layer], d), _block_bytes(dv0[layer], s))
+        for b in (0, 2, 3, 4, 5, 7):
+            assert np.array_equal(_block_bytes(dk[layer], b), _block_bytes(dk0[layer], b))
+
+
+def test_swap_skips_pairs_outside_their_pool():
+    rng = np.random.default_rng(4)
+    dk = [rng.integers(0, 255, (4, 16), dtype=np.uint8)]
+    hk = [rng.integers(0, 255, (2, 16), dtype=np.uint8)]
+    dv, hv = [dk[0].copy()], [hk[0].copy()]
+    h0 = hk[0].copy()
+    skipped = oracle.swap_blocks(hk, hv, dk, dv, [(4, 0), (1, 2), (-1, 1), (3, 1)])
+    assert skipped == [(4, 0), (1, 2), (-1, 1)]
+    assert np.array_equal(hk[0][0], h0[0])
+    assert np.array_equal(hk[0][1], dk[0][3])
+
+
 # ----------------------------------------------------------------------------
 # decode
 

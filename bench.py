@@ -456,6 +456,185 @@ def run_ours(args, world, rank, local):
     return line
 
 
+# ----------------------------------------------------------------------------
+# swap: preemption of one request by moving its blocks to pinned host memory
+# and back (pa_swap_blocks)
+
+SWAP_METRIC = "pa_swap_blocks host-link GB/s (swap-out + swap-in of one preempted request)"
+
+
+def swap_shape():
+    """The Llama-8B-shaped pool (32 layers, 8 KV heads, d 128, bf16, 16-token
+    blocks) with the longest request of the decode batch (4096 tokens, 256
+    blocks per layer) preempted."""
+    return dict(layers=32, kv_heads=8, block_size=16, head_dim=128, elem=2, request_blocks=256,
+                device_blocks=512)
+
+
+def run_swap(args, world, rank, local):
+    import paged_kv_cache_288_gb300 as pa
+    from paged_kv_cache_288_gb300 import build
+
+    build.build_library()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    sh = swap_shape()
+    L, nb, nd = sh["layers"], sh["request_blocks"], sh["device_blocks"]
+    blk_elems = sh["kv_heads"] * sh["block_size"] * sh["head_dim"]
+    block_bytes = blk_elems * sh["elem"]
+    g = torch.Generator(device="cpu").manual_seed(rank_seed(1006, rank))
+    dk = [torch.empty(nd, blk_elems, dtype=torch.bfloat16, device=device).normal_() for _ in range(L)]
+    dv = [torch.empty(nd, blk_elems, dtype=torch.bfloat16, device=device).normal_() for _ in range(L)]
+    hk = [torch.empty(nb, blk_elems, dtype=torch.bfloat16).pin_memory() for _ in range(L)]
+    hv = [torch.empty(nb, blk_elems, dtype=torch.bfloat16).pin_memory() for _ in range(L)]
+    # the request's blocks are scattered over the device pool; it comes back
+    # into other free blocks
+    perm = torch.randperm(nd, generator=g)
+    out_map = torch.stack([perm[:nb], torch.arange(nb)], 1).to(torch.int64)
+    in_map = torch.stack([torch.arange(nb), perm[nb:2 * nb]], 1).to(torch.int64)
+    out_d, in_d = out_map.to(device), in_map.to(device)
+    err = torch.zeros(1, dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream(device)
+    moved = 2 * L * nb * block_bytes  # K and V, all layers, one direction
+
+    def swap_out():
+        pa.swap_blocks(hk, hv, dk, dv, out_d, debug_err=err)
+
+    def swap_in():
+        pa.swap_blocks(dk, dv, hk, hv, in_d, debug_err=err)
+
+    # the host link's copy-engine rate for the same number of bytes, one
+    # contiguous cudaMemcpyAsync per direction: the roofline denominator
+    dbuf = torch.empty(moved, dtype=torch.uint8, device=device)
+    hbuf = torch.empty(moved, dtype=torch.uint8).pin_memory()
+    for _ in range(args.warmup):
+        swap_out()
+        swap_in()
+        hbuf.copy_(dbuf, non_blocking=True)
+        dbuf.copy_(hbuf, non_blocking=True)
+    torch.cuda.synchronize()
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    cev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    n0 = pa.lib().pa_kernel_launch_count()
+    t0 = time.time()
+    for k in range(K):
+        ev[k][0].record(stream)
+        swap_out()
+        ev[k][1].record(stream)
+        swap_in()
+        ev[k][2].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier(world)
+    n1 = pa.lib().pa_kernel_launch_count()
+    sampler.stop()
+    for k in range(K):
+        cev[k][0].record(stream)
+        hbuf.copy_(dbuf, non_blocking=True)
+        cev[k][1].record(stream)
+        dbuf.copy_(hbuf, non_blocking=True)
+        cev[k][2].record(stream)
+    torch.cuda.synchronize()
+    out_ms = statistics.mean(ev[k][0].elapsed_time(ev[k][1]) for k in range(K))
+    in_ms = statistics.mean(ev[k][1].elapsed_time(ev[k][2]) for k in range(K))
+    total_ms = max_over_ranks(sum(ev[k][0].elapsed_time(ev[k][2]) for k in range(K)), world, device)
+    d2h_ms = statistics.mean(cev[k][0].elapsed_time(cev[k][1]) for k in range(K))
+    h2d_ms = statistics.mean(cev[k][1].elapsed_time(cev[k][2]) for k in range(K))
+    value = job_throughput_gbs(2 * moved, K, world, total_ms)
+    peak = 2 * moved / ((d2h_ms + h2d_ms) / 1e3) / 1e9
+    achieved = 2 * moved / ((out_ms + in_ms) / 1e3) / 1e9
+
+    # end to end through the public API: the mapping comes from pinned host
+    # memory each step and the error flag is read back
+    h_out, h_in = out_map.pin_memory(), in_map.pin_memory()
+    h_err = torch.zeros(1, dtype=torch.int32).pin_memory()
+    Ke = min(K, 50)
+    eev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Ke)]
+    torch.cuda.synchronize()
+    for k in range(Ke):
+        eev[k][0].record(stream)
+        out_d.copy_(h_out, non_blocking=True)
+        swap_out()
+        in_d.copy_(h_in, non_blocking=True)
+        swap_in()
+        h_err.copy_(err, non_blocking=True)
+        eev[k][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(sum(eev[k][0].elapsed_time(eev[k][1]) for k in range(Ke)), world, device)
+    assert int(h_err.item()) == 0, "swap flagged an out-of-range block"
+    if rank != 0:
+        return None
+    line = {
+        "metric": SWAP_METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_ms / K, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16 (bytes moved as is)",
+        "data": "synthetic (seeded N(0,1) pools, shuffled request blocks)",
+        "config": {"workload": args.workload, "layers": L, "num_kv_heads": sh["kv_heads"],
+                   "block_size": sh["block_size"], "head_dim": sh["head_dim"],
+                   "request_blocks": nb, "device_blocks": nd, "block_bytes": block_bytes,
+                   "bytes_per_direction": moved,
+                   "l2": "not flushed: each direction moves 512 MiB, four times the L2",
+                   "parallelism": f"{world} independent replica(s), one per GPU"},
+        "swap_out_us": round(out_ms * 1e3, 1),
+        "swap_in_us": round(in_ms * 1e3, 1),
+        "swap_out_gbs": round(moved / (out_ms / 1e3) / 1e9, 1),
+        "swap_in_gbs": round(moved / (in_ms / 1e3) / 1e9, 1),
+        "roofline": {"bound": "host_link", "achieved": round(achieved, 1), "peak": round(peak, 1),
+                     "peak_source": "measured in this run: one contiguous cudaMemcpyAsync of the "
+                                    "same bytes per direction over the same link",
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
+                     "kernel": "swap_blocks_kernel",
+                     "copy_engine_d2h_gbs": round(moved / (d2h_ms / 1e3) / 1e9, 1),
+                     "copy_engine_h2d_gbs": round(moved / (h2d_ms / 1e3) / 1e9, 1)},
+        "e2e": {"value": round(job_throughput_gbs(2 * moved, Ke, world, e2e_ms), 2), "unit": "GB/s",
+                "h2d_bytes_per_step": int(out_map.numel() * 8 + in_map.numel() * 8),
+                "d2h_bytes_per_step": 4, "steps": Ke},
+        "clocks": sampler.summary(t0, t1),
+        "gpu_launches": n1 - n0,
+        "launches_per_step": (n1 - n0) / K,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = swap_cpu_baseline()
+    return line
+
+
+def swap_oracle_gbs(layers, blocks, reps):
+    """The oracle's swap (numpy byte copies) on host arrays of the swap shape."""
+    import oracle
+    sh = swap_shape()
+    n = sh["kv_heads"] * sh["block_size"] * sh["head_dim"]
+    rng = np.random.default_rng(7)
+    src = [rng.integers(0, 65535, (2 * blocks, n), dtype=np.uint16) for _ in range(2 * layers)]
+    dst = [np.zeros((blocks, n), dtype=np.uint16) for _ in range(2 * layers)]
+    pairs = [(2 * i + 1, i) for i in range(blocks)]
+    t = time.perf_counter()
+    for _ in range(reps):
+        oracle.swap_blocks(dst[:layers], dst[layers:], src[:layers], src[layers:], pairs)
+    dt = time.perf_counter() - t
+    return 2 * layers * blocks * n * 2 * reps / dt / 1e9, dt
+
+
+def swap_cpu_baseline():
+    value, dt = swap_oracle_gbs(32, 256, 3)
+    return {"value": round(value, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"numpy oracle swap of the full request (32 layers x 256 blocks, K and V) "
+                      f"between host arrays, 3 repetitions, {dt:.1f} s, 1 thread"}
+
+
 def run_reference(args, world, rank):
     if rank != 0:
         return None
@@ -489,6 +668,33 @@ def run_reference(args, world, rank):
     }
 
 
+def run_swap_reference(args, world, rank):
+    if rank != 0:
+        return None
+    secs = []
+    value = 0.0
+    for _ in range(args.warmup + args.steps):
+        v, dt = swap_oracle_gbs(32, 32, 1)
+        secs.append(dt)
+        value = v
+    timed = secs[args.warmup:]
+    sh = swap_shape()
+    moved = 2 * 32 * 32 * sh["kv_heads"] * sh["block_size"] * sh["head_dim"] * sh["elem"]  # K and V
+    value = moved * len(timed) / sum(timed) / 1e9
+    return {
+        "impl": "reference", "metric": SWAP_METRIC, "value": round(value, 3), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * sum(timed) / len(timed), 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bytes (oracle)",
+        "data": "synthetic host arrays", "config": {"workload": args.workload,
+                                                    "sample_blocks_per_layer": 32},
+        "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": "numpy oracle swap of 32 of the request's 256 blocks per layer, "
+                                   "32 layers, K and V, 1 thread"},
+        "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -503,10 +709,11 @@ def main():
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
     world, rank, local = setup_dist()
+    swap = args.workload.startswith("swap")
     if args.impl == "reference":
-        line = run_reference(args, world, rank)
+        line = run_swap_reference(args, world, rank) if swap else run_reference(args, world, rank)
     else:
-        line = run_ours(args, world, rank, local)
+        line = run_swap(args, world, rank, local) if swap else run_ours(args, world, rank, local)
     if line is not None:
         print(json.dumps(line), flush=True)
     if world > 1:

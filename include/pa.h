@@ -176,6 +176,43 @@ pa_status pa_copy_blocks(void* const* k_caches, void* const* v_caches,
                          size_t block_bytes, int32_t* debug_err,
                          cudaStream_t stream);
 
+/* Layers one pa_swap_blocks call moves at most. */
+#define PA_SWAP_MAX_LAYERS 64
+
+/*
+ * pa_swap_blocks - move whole blocks, K and V, in every layer, between two
+ * pools, typically the device pool and a pool in pinned host memory.
+ *
+ * This is the swap way of preempting a request when the pool runs out of
+ * free blocks: its blocks are moved to CPU memory and brought back later,
+ * which keeps the computed cache at the price of the transfer over the host
+ * link (serving-paged-attention, "그래도 넘칠 때 — 선점", item "스왑").
+ * For each pair p, src = block_mapping[2p], dst = block_mapping[2p+1], and
+ * each layer l: block dst of dst_k[l] (dst_v[l]) becomes a byte copy of
+ * block src of src_k[l] (src_v[l]). Swap-out passes the device caches as
+ * src and the host pools as dst; swap-in the reverse. The caller updates
+ * the block tables and frees or allocates the blocks.
+ *
+ * dst_k, dst_v, src_k, src_v are HOST arrays of num_layers pointers (1 <=
+ * num_layers <= PA_SWAP_MAX_LAYERS). Each pointer, and block_mapping (int64
+ * [num_pairs, 2]), must be device memory or pinned host memory mapped into
+ * the device's address space (cudaHostAlloc / cudaHostRegister, torch
+ * pin_memory); other pointers are refused with PA_ERR_INVALID before any
+ * launch. Pointers are 16-byte aligned; block_bytes (one block of one cache
+ * of one layer) is a positive multiple of 16; the src pools hold
+ * src_num_blocks blocks, the dst pools dst_num_blocks. Pairs outside those
+ * ranges set PA_DEVERR_BLOCK_RANGE in *debug_err (if not NULL) and are
+ * skipped. dst blocks must be distinct and must not overlap the src blocks
+ * of the same call. The call is asynchronous on `stream`; the caller keeps
+ * every buffer alive and unmodified until the stream has passed it.
+ */
+pa_status pa_swap_blocks(void* const* dst_k, void* const* dst_v,
+                         const void* const* src_k, const void* const* src_v,
+                         int32_t num_layers, const int64_t* block_mapping,
+                         int32_t num_pairs, int32_t src_num_blocks,
+                         int32_t dst_num_blocks, size_t block_bytes,
+                         int32_t* debug_err, cudaStream_t stream);
+
 /*
  * pa_decode_split_noalloc - pa_decode's split-context path without a
  * caller-provided workspace. (The source pages have no counterpart; this is

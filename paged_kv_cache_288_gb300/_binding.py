@@ -66,6 +66,9 @@ def lib():
             _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int32, _c_ptr, _c_int32, _c_int32,
             _c_int32, _c_int32, _c_int32, _c_int32, ctypes.c_float, ctypes.c_int, ctypes.c_int,
             _c_ptr, _c_ptr, _c_int32, _c_int32, _c_ptr, _c_ptr]
+        L.pa_swap_blocks.restype = ctypes.c_int
+        L.pa_swap_blocks.argtypes = [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int32, _c_ptr, _c_int32,
+                                     _c_int32, _c_int32, _c_size, _c_ptr, _c_ptr]
         L.pa_copy_blocks.restype = ctypes.c_int
         L.pa_copy_blocks.argtypes = [_c_ptr, _c_ptr, _c_int32, _c_ptr, _c_int32, _c_int32,
                                      _c_size, _c_ptr, _c_ptr]
@@ -182,3 +185,44 @@ def copy_blocks(k_ptrs, v_ptrs, block_mapping, num_blocks, block_bytes, debug_er
     _check(lib().pa_copy_blocks(
         _ptr(k_ptrs), _ptr(v_ptrs), k_ptrs.numel(), _ptr(block_mapping), block_mapping.shape[0],
         int(num_blocks), int(block_bytes), _ptr(debug_err), _stream(stream)), "pa_copy_blocks")
+
+
+SWAP_MAX_LAYERS = 64
+
+
+def _host_ptr_array(tensors):
+    arr = (ctypes.c_void_p * max(1, len(tensors)))()
+    for i, t in enumerate(tensors):
+        arr[i] = t.data_ptr()
+    return arr
+
+
+def swap_blocks(dst_k, dst_v, src_k, src_v, block_mapping, debug_err=None, stream=None):
+    """Move blocks (src, dst) = block_mapping[p] from the src pools to the dst pools, K and V,
+    in every layer.
+
+    dst_k, dst_v, src_k, src_v are lists (one tensor per layer) of pools shaped
+    [num_blocks, ...]; each is a device tensor or a pinned host tensor
+    (pin_memory=True). block_mapping is int64 [num_pairs, 2] on the device or
+    in pinned host memory.
+    """
+    n = len(src_k)
+    if not (len(src_v) == len(dst_k) == len(dst_v) == n):
+        raise ValueError("one K and one V pool per layer on each side")
+    if block_mapping.dtype != torch.int64 or block_mapping.dim() != 2 or block_mapping.shape[1] != 2:
+        raise ValueError("block_mapping must be int64 [num_pairs, 2]")
+    if n == 0:
+        return
+    blk = src_k[0][0].numel() * src_k[0].element_size()
+    for t in list(src_k) + list(src_v) + list(dst_k) + list(dst_v):
+        if not t.is_contiguous() or t[0].numel() * t.element_size() != blk:
+            raise ValueError("every pool must be contiguous with the same block size")
+    src_nb, dst_nb = src_k[0].shape[0], dst_k[0].shape[0]
+    if any(t.shape[0] != src_nb for t in src_v) or any(t.shape[0] != dst_nb for t in list(dst_k) + list(dst_v)):
+        raise ValueError("the pools of one side must hold the same number of blocks")
+    if any(t.shape[0] != src_nb for t in src_k):
+        raise ValueError("the pools of one side must hold the same number of blocks")
+    _check(lib().pa_swap_blocks(
+        _host_ptr_array(dst_k), _host_ptr_array(dst_v), _host_ptr_array(src_k), _host_ptr_array(src_v),
+        n, _ptr(block_mapping), block_mapping.shape[0], int(src_nb), int(dst_nb), int(blk),
+        _ptr(debug_err), _stream(stream)), "pa_swap_blocks")

@@ -76,6 +76,39 @@ __global__ void copy_blocks_kernel(void* const* __restrict__ k_caches, void* con
   for (int64_t i = threadIdx.x; i < block_vecs; i += blockDim.x) d[i] = s[i];
 }
 
+// grid = (num_pairs, num_layers, 2: K then V). Each CTA moves one block of
+// one cache of one layer between two pools (device memory or mapped pinned
+// host memory), kSwapUnroll 16-byte vectors per thread in flight.
+constexpr int kSwapThreads = 256;
+constexpr int kSwapUnroll = 4;
+
+__global__ void __launch_bounds__(kSwapThreads) swap_blocks_kernel(const __grid_constant__ SwapPools pools,
+                                                                   const int64_t* __restrict__ block_mapping,
+                                                                   int src_num_blocks, int dst_num_blocks,
+                                                                   int64_t block_vecs, int32_t* debug_err) {
+  const int pair = blockIdx.x;
+  const int layer = blockIdx.y;
+  const int kv = blockIdx.z;
+  const int64_t src = block_mapping[2 * pair];
+  const int64_t dst = block_mapping[2 * pair + 1];
+  if (src < 0 || src >= src_num_blocks || dst < 0 || dst >= dst_num_blocks) {
+    if (threadIdx.x == 0 && layer == 0 && kv == 0) flag_error(debug_err, PA_DEVERR_BLOCK_RANGE);
+    return;
+  }
+  const uint4* s = static_cast<const uint4*>(pools.src[kv][layer]) + src * block_vecs;
+  uint4* d = static_cast<uint4*>(pools.dst[kv][layer]) + dst * block_vecs;
+  constexpr int kStep = kSwapThreads * kSwapUnroll;
+  int64_t i = threadIdx.x;
+  for (; i + (kSwapUnroll - 1) * kSwapThreads < block_vecs; i += kStep) {
+    uint4 v[kSwapUnroll];
+#pragma unroll
+    for (int u = 0; u < kSwapUnroll; ++u) v[u] = __ldcs(s + i + u * kSwapThreads);
+#pragma unroll
+    for (int u = 0; u < kSwapUnroll; ++u) __stcs(d + i + u * kSwapThreads, v[u]);
+  }
+  for (; i < block_vecs; i += kSwapThreads) __stcs(d + i, __ldcs(s + i));
+}
+
 }  // namespace
 
 cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* k_cache,
@@ -114,6 +147,19 @@ cudaError_t launch_copy_blocks(void* const* k_caches, void* const* v_caches, int
   dim3 grid(num_pairs, num_layers, 2);
   copy_blocks_kernel<<<grid, 256, 0, stream>>>(k_caches, v_caches, block_mapping, num_blocks,
                                                static_cast<int64_t>(block_bytes / 16), debug_err);
+  cudaError_t err = cudaGetLastError();
+  if (err == cudaSuccess) note_launches(1);
+  return err;
+}
+
+cudaError_t launch_swap_blocks(const SwapPools& pools, int num_layers, const int64_t* block_mapping,
+                               int num_pairs, int src_num_blocks, int dst_num_blocks,
+                               size_t block_bytes, int32_t* debug_err, cudaStream_t stream) {
+  if (num_pairs == 0 || num_layers == 0) return cudaSuccess;
+  dim3 grid(num_pairs, num_layers, 2);
+  swap_blocks_kernel<<<grid, kSwapThreads, 0, stream>>>(pools, block_mapping, src_num_blocks,
+                                                        dst_num_blocks,
+                                                        static_cast<int64_t>(block_bytes / 16), debug_err);
   cudaError_t err = cudaGetLastError();
   if (err == cudaSuccess) note_launches(1);
   return err;

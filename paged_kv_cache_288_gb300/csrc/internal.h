@@ -27,6 +27,15 @@ cudaError_t launch_copy_blocks(void* const* k_caches, void* const* v_caches, int
                                const int64_t* block_mapping, int num_pairs, int num_blocks,
                                size_t block_bytes, int32_t* debug_err, cudaStream_t stream);
 
+// Per-layer pool pointers of one swap, all device-accessible.
+struct SwapPools {
+  const void* src[2][PA_SWAP_MAX_LAYERS];  // [K, V][layer]
+  void* dst[2][PA_SWAP_MAX_LAYERS];
+};
+cudaError_t launch_swap_blocks(const SwapPools& pools, int num_layers, const int64_t* block_mapping,
+                               int num_pairs, int src_num_blocks, int dst_num_blocks,
+                               size_t block_bytes, int32_t* debug_err, cudaStream_t stream);
+
 // CUDA-core decode: grid (num_partitions, num_kv_heads, num_seqs), plus the
 // partition reduce when num_partitions > 1.
 cudaError_t launch_decode_simt(const DecodeParams& p, int head_dim, pa_dtype q_dtype,

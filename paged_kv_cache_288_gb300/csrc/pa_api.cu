@@ -282,4 +282,65 @@ pa_status pa_copy_blocks(void* const* k_caches, void* const* v_caches, int32_t n
                    "copy_blocks launch");
 }
 
+// The device-side address of `p` when the device can read and write it (device
+// or managed memory, or pinned host memory mapped into the device's address
+// space), else nullptr.
+static const void* device_accessible(const void* p) {
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();  // clear the sticky-free error of an unknown pointer
+    return nullptr;
+  }
+  switch (at.type) {
+    case cudaMemoryTypeDevice:
+    case cudaMemoryTypeManaged:
+      return p;
+    case cudaMemoryTypeHost:
+      return at.devicePointer;
+    default:
+      return nullptr;
+  }
+}
+
+pa_status pa_swap_blocks(void* const* dst_k, void* const* dst_v, const void* const* src_k,
+                         const void* const* src_v, int32_t num_layers,
+                         const int64_t* block_mapping, int32_t num_pairs, int32_t src_num_blocks,
+                         int32_t dst_num_blocks, size_t block_bytes, int32_t* debug_err,
+                         cudaStream_t stream) {
+  if (num_layers < 0 || num_pairs < 0) return fail(PA_ERR_INVALID, "negative count");
+  if (num_layers > PA_SWAP_MAX_LAYERS)
+    return fail(PA_ERR_UNSUPPORTED, "more than %d layers in one swap", PA_SWAP_MAX_LAYERS);
+  if (src_num_blocks <= 0 || dst_num_blocks <= 0)
+    return fail(PA_ERR_INVALID, "pool sizes must be positive");
+  if (block_bytes == 0 || block_bytes % 16 != 0)
+    return fail(PA_ERR_INVALID, "block_bytes must be a positive multiple of 16");
+  if (num_layers == 0 || num_pairs == 0) return PA_OK;
+  if (num_pairs > 2147483647 / 2) return fail(PA_ERR_UNSUPPORTED, "too many pairs");
+  if (!dst_k || !dst_v || !src_k || !src_v || !block_mapping) return fail(PA_ERR_INVALID, "null pointer");
+  pa::SwapPools pools{};
+  for (int l = 0; l < num_layers; ++l) {
+    const void* in[4] = {src_k[l], src_v[l], dst_k[l], dst_v[l]};
+    const void* dev[4];
+    for (int i = 0; i < 4; ++i) {
+      if (in[i] == nullptr) return fail(PA_ERR_INVALID, "null pool pointer for layer %d", l);
+      if (reinterpret_cast<uintptr_t>(in[i]) % 16 != 0)
+        return fail(PA_ERR_INVALID, "pool pointer of layer %d is not 16-byte aligned", l);
+      dev[i] = device_accessible(in[i]);
+      if (dev[i] == nullptr)
+        return fail(PA_ERR_INVALID,
+                    "pool pointer of layer %d is neither device memory nor mapped pinned host memory", l);
+    }
+    pools.src[0][l] = dev[0];
+    pools.src[1][l] = dev[1];
+    pools.dst[0][l] = const_cast<void*>(dev[2]);
+    pools.dst[1][l] = const_cast<void*>(dev[3]);
+  }
+  const void* map = device_accessible(block_mapping);
+  if (map == nullptr)
+    return fail(PA_ERR_INVALID, "block_mapping is neither device memory nor mapped pinned host memory");
+  return from_cuda(pa::launch_swap_blocks(pools, num_layers, static_cast<const int64_t*>(map), num_pairs,
+                                          src_num_blocks, dst_num_blocks, block_bytes, debug_err, stream),
+                   "swap_blocks launch");
+}
+
 }  // extern "C"

@@ -34,6 +34,7 @@ def _declared_functions():
 def test_header_declares_the_boundary():
     names = _declared_functions()
     for f in ("pa_reshape_and_cache", "pa_decode", "pa_decode_workspace_size", "pa_copy_blocks",
+              "pa_swap_blocks",
               "pa_status_string", "pa_last_error_message", "pa_version"):
         assert f in names
 
@@ -130,3 +131,17 @@ def test_product_package_does_not_import_the_oracle():
     for path in glob.glob(os.path.join(ROOT, "oracle", "*.py")):
         src = open(path).read()
         assert "paged_kv_cache_288_gb300" not in src and "workloads" not in src, path
+
+
+def test_swap_blocks_argument_checks(L):
+    arr = (ctypes.c_void_p * 65)(*([16] * 65))
+    def swap(layers=1, pairs=1, snb=4, dnb=4, bb=4096):
+        return L.pa_swap_blocks(arr, arr, arr, arr, layers, 16, pairs, snb, dnb, bb, NULL, NULL)
+    assert swap(layers=65) == 2           # PA_ERR_UNSUPPORTED: over PA_SWAP_MAX_LAYERS
+    assert swap(layers=-1) == 1           # PA_ERR_INVALID
+    assert swap(pairs=-1) == 1
+    assert swap(snb=0) == 1
+    assert swap(bb=4000) == 1             # not a multiple of 16
+    assert swap(pairs=0) == 0             # nothing to move: no CUDA call
+    assert swap(layers=0) == 0
+    assert L.pa_swap_blocks(None, arr, arr, arr, 1, 16, 1, 4, 4, 4096, NULL, NULL) == 1

@@ -142,3 +142,99 @@ def test_copy_blocks_flags_out_of_range_pairs():
     torch.cuda.synchronize()
     assert err.item() & pa.DEVERR_BLOCK_RANGE
     assert np.array_equal(host_bits(kd), want)
+
+
+# ----------------------------------------------------------------------------
+# swap to and from pinned host memory
+
+
+def _pinned(bits, dtype):
+    """Raw-bit numpy array -> pinned host tensor of the storage dtype."""
+    return dev(bits, dtype, device="cpu").pin_memory()
+
+
+@pytest.mark.parametrize("dtype,L", [(BF16, 1), (F16, 3), (FP8_E4M3, 2)])
+@pytest.mark.parametrize("map_on_host", [False, True])
+def test_swap_out_then_in_bit_exact(dtype, L, map_on_host):
+    """A preempted request's blocks go to a pinned host pool and come back into
+    other device blocks; every byte of both pools matches the oracle."""
+    Nd, Nh, Hkv, bs, d = 24, 10, 8, 16, 128
+    dk = [_random_pool(40 + i, Nd, Hkv, bs, d, dtype) for i in range(L)]
+    dv = [_random_pool(50 + i, Nd, Hkv, bs, d, dtype) for i in range(L)]
+    hk = [_random_pool(60 + i, Nh, Hkv, bs, d, dtype) for i in range(L)]
+    hv = [_random_pool(70 + i, Nh, Hkv, bs, d, dtype) for i in range(L)]
+    dkt, dvt = [dev(x, dtype) for x in dk], [dev(x, dtype) for x in dv]
+    hkt, hvt = [_pinned(x, dtype) for x in hk], [_pinned(x, dtype) for x in hv]
+
+    def mapping(pairs):
+        t = torch.from_numpy(np.array(pairs, dtype=np.int64).reshape(-1, 2))
+        return t.pin_memory() if map_on_host else t.cuda()
+
+    out_pairs = [[17, 0], [3, 9], [4, 5], [23, 2]]
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    m_out = mapping(out_pairs)
+    pa.swap_blocks(hkt, hvt, dkt, dvt, m_out, debug_err=err)
+    oracle.swap_blocks(hk, hv, dk, dv, out_pairs)
+    torch.cuda.synchronize()
+    for i in range(L):
+        assert np.array_equal(host_bits(hkt[i]), hk[i])
+        assert np.array_equal(host_bits(hvt[i]), hv[i])
+
+    in_pairs = [[0, 1], [9, 20], [5, 17], [2, 3]]
+    m_in = mapping(in_pairs)
+    pa.swap_blocks(dkt, dvt, hkt, hvt, m_in, debug_err=err)
+    oracle.swap_blocks(dk, dv, hk, hv, in_pairs)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    for i in range(L):
+        assert np.array_equal(host_bits(dkt[i]), dk[i])
+        assert np.array_equal(host_bits(dvt[i]), dv[i])
+
+
+def test_swap_flags_out_of_range_pairs():
+    Nd, Nh, Hkv, bs, d = 6, 3, 2, 8, 64
+    dk = _random_pool(80, Nd, Hkv, bs, d, BF16)
+    hk = _random_pool(81, Nh, Hkv, bs, d, BF16)
+    dkt, hkt, hvt = dev(dk, BF16), _pinned(hk, BF16), _pinned(hk, BF16)
+    pairs = [[6, 0], [1, 3], [-1, 1], [2, 1]]
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.swap_blocks([hkt], [hvt], [dkt], [dkt], torch.tensor(pairs, dtype=torch.int64).cuda(), debug_err=err)
+    want = hk.copy()
+    skipped = oracle.swap_blocks([want], [hk.copy()], [dk], [dk], pairs)
+    torch.cuda.synchronize()
+    assert skipped == [(6, 0), (1, 3), (-1, 1)]
+    assert err.item() & pa.DEVERR_BLOCK_RANGE
+    assert np.array_equal(host_bits(hkt), want)
+
+
+def test_swap_refuses_pageable_host_memory():
+    """Host memory the device cannot address is refused before any launch."""
+    dk = _random_pool(82, 4, 2, 8, 64, BF16)
+    dkt = dev(dk, BF16)
+    pageable = dev(dk, BF16, device="cpu")
+    assert not pageable.is_pinned()
+    n0 = pa.lib().pa_kernel_launch_count()
+    with pytest.raises(pa.PaError) as e:
+        pa.swap_blocks([pageable], [pageable], [dkt], [dkt], torch.tensor([[0, 1]], dtype=torch.int64).cuda())
+    assert e.value.status == 1
+    with pytest.raises(pa.PaError):
+        pa.swap_blocks([dkt], [dkt], [dkt], [dkt], torch.tensor([[0, 1]], dtype=torch.int64))
+    assert pa.lib().pa_kernel_launch_count() == n0
+
+
+def test_swap_all_layers_at_the_limit():
+    L, Nd, Nh, Hkv, bs, d = pa.SWAP_MAX_LAYERS, 3, 2, 1, 8, 64
+    dk = [_random_pool(100 + i, Nd, Hkv, bs, d, F16) for i in range(L)]
+    hk = [_random_pool(200 + i, Nh, Hkv, bs, d, F16) for i in range(L)]
+    dkt = [dev(x, F16) for x in dk]
+    hkt = [_pinned(x, F16) for x in hk]
+    pairs = [[2, 1], [0, 0]]
+    pa.swap_blocks(hkt, hkt, dkt, dkt, torch.tensor(pairs, dtype=torch.int64).cuda())
+    oracle.swap_blocks(hk, hk, dk, dk, pairs)
+    torch.cuda.synchronize()
+    for i in range(L):
+        assert np.array_equal(host_bits(hkt[i]), hk[i])
+    with pytest.raises(pa.PaError) as e:
+        pa.swap_blocks(hkt + hkt[:1], hkt + hkt[:1], dkt + dkt[:1], dkt + dkt[:1],
+                       torch.tensor(pairs, dtype=torch.int64).cuda())
+    assert e.value.status == 2

@@ -46,8 +46,7 @@ L2_FLUSH_BYTES = 256 << 20
 TRAFFIC_PATH = os.path.join(ROOT, "profiles", "traffic.json")
 TRAFFIC_SOURCES = ("paged_kv_cache_288_gb300/csrc/decode_tc.cu",
                    "paged_kv_cache_288_gb300/csrc/ptx.cuh",
-                   "paged_kv_cache_288_gb300/csrc/common.cuh",
-                   "paged_kv_cache_288_gb300/csrc/pa_api.cu")
+                   "paged_kv_cache_288_gb300/csrc/common.cuh")
 
 
 def kernel_sources_hash():
@@ -629,10 +628,13 @@ def swap_oracle_gbs(layers, blocks, reps):
 
 
 def swap_cpu_baseline():
-    value, dt = swap_oracle_gbs(32, 256, 3)
+    """The oracle on host arrays, repeated for about 10 s."""
+    value, dt = swap_oracle_gbs(32, 256, 1)
+    reps = max(1, int(10.0 / max(dt, 1e-3)))
+    value, dt = swap_oracle_gbs(32, 256, reps)
     return {"value": round(value, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"numpy oracle swap of the full request (32 layers x 256 blocks, K and V) "
-                      f"between host arrays, 3 repetitions, {dt:.1f} s, 1 thread"}
+                      f"between host arrays, {reps} repetitions, {dt:.1f} s, 1 thread"}
 
 
 def run_reference(args, world, rank):

@@ -90,7 +90,68 @@ def make_case(name, rank):
         return workloads.long_context(bs, seed=rank_seed(1004, rank))
     if name == "fp8_layer":
         return workloads.fp8_step_layer(0, seed=rank_seed(1005, rank))
+    if name == "prefix_cache":
+        return prefix_cache_case(rank_seed(1007, rank))
     raise ValueError(name)
+
+
+def prefix_cache_case(seed, num_seqs=100, prefix_len=1016, suffix_lo=32, suffix_hi=512,
+                      num_heads=32, num_kv_heads=8, head_dim=128, block_size=16):
+    """The shared-prefix shape with the sharing found by the prefix cache.
+
+    num_seqs requests open with one prefix_len-token system prompt and go on
+    with a private suffix of suffix_lo..suffix_hi tokens (token ids are seeded
+    random). Each request is admitted through the prefix cache, which finds
+    the system prompt's full blocks from the token ids; its last token is the
+    one written and decoded in the timed step. Pool contents are random bf16,
+    block ids shuffled; host admission time is kept in ``meta``.
+    """
+    from paged_kv_cache_288_gb300.block_pool import BlockPool, PrefixCache
+
+    g = workloads._gen(seed)
+    bs = block_size
+    system = torch.randint(0, 32000, (prefix_len,), generator=g).numpy()
+    suffix = torch.randint(suffix_lo, suffix_hi + 1, (num_seqs,), generator=g).numpy()
+    prompts = [np.concatenate([system, torch.randint(0, 32000, (int(n),), generator=g).numpy()])
+               for n in suffix]
+    full = prefix_len // bs
+    need = full + sum(-(-len(t) // bs) - full for t in prompts)
+    num_blocks = int(math.ceil(1.25 * need)) + 1
+    pool = BlockPool(num_blocks - 1, bs)
+    cache = PrefixCache(pool)
+    t0 = time.perf_counter()
+    cached = [cache.add_sequence(i, t)[0] for i, t in enumerate(prompts)]
+    host_s = time.perf_counter() - t0
+    perm = torch.randperm(num_blocks, generator=g).numpy().astype(np.int32)
+    poison = int(perm[-1])
+    ctx = np.array([len(t) for t in prompts], dtype=np.int64)
+    width = int(max(-(-c // bs) for c in ctx))
+    tables = np.full((num_seqs, width), poison, dtype=np.int32)
+    for i in range(num_seqs):
+        tables[i, :len(pool.tables[i])] = perm[np.asarray(pool.tables[i])]
+    dtype = workloads.BF16
+    shape = (num_blocks, num_kv_heads, bs, head_dim)
+    kc = workloads.normal_bits(g, shape, dtype)
+    vc = workloads.normal_bits(g, shape, dtype)
+    kc[poison] = workloads.NAN_BITS[dtype]
+    vc[poison] = workloads.NAN_BITS[dtype]
+    workloads._poison_tails(kc, tables, ctx, bs, dtype)
+    workloads._poison_tails(vc, tables, ctx, bs, dtype)
+    slots = np.array([int(tables[i, (c - 1) // bs]) * bs + (c - 1) % bs for i, c in enumerate(ctx)],
+                     dtype=np.int64)
+    return workloads.DecodeCase(
+        name="prefix_cache", num_seqs=num_seqs, num_heads=num_heads, num_kv_heads=num_kv_heads,
+        head_dim=head_dim, block_size=bs, num_blocks=num_blocks, q_dtype=dtype, kv_dtype=dtype,
+        scale=1.0 / math.sqrt(head_dim), q=workloads.normal_bits(g, (num_seqs, num_heads, head_dim), dtype),
+        k_cache=kc, v_cache=vc, block_tables=tables, context_lens=ctx.astype(np.int32),
+        poison_block=poison, new_key=workloads.normal_bits(g, (num_seqs, num_kv_heads, head_dim), dtype),
+        new_value=workloads.normal_bits(g, (num_seqs, num_kv_heads, head_dim), dtype),
+        slot_mapping=slots, src_dtype=dtype,
+        meta={"prefix_cache": {"requests": num_seqs, "cached_tokens": int(sum(cached)),
+                               "hit_blocks": cache.hits, "miss_blocks": cache.misses,
+                               "host_admission_us_per_request": round(1e6 * host_s / num_seqs, 1),
+                               "blocks_in_use": pool.used_blocks(),
+                               "blocks_without_sharing": int(sum(-(-c // bs) for c in ctx))}})
 
 
 def job_throughput_gbs(bytes_per_step, steps, world, max_total_ms):
@@ -449,10 +510,234 @@ def run_ours(args, world, rank, local):
         "gpu_launches": launches,
         "launches_per_step": launches / K,
     }
+    if case.meta and "prefix_cache" in case.meta:
+        line["prefix_cache"] = case.meta["prefix_cache"]
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(args.workload, case)
     del launches_before
     return line
+
+
+# ----------------------------------------------------------------------------
+# beam search: fork + copy-on-write + decode
+
+
+def beam_plan(steps, seed, requests=16, beams=4, prompt_lo=1536, prompt_hi=2560, block_size=16):
+    """Host bookkeeping of a beam-search decode, planned ahead of the GPU run.
+
+    ``requests`` prompts (lengths uniform in [prompt_lo, prompt_hi]) each fork
+    into ``beams`` beams that share the prompt's blocks. Every step each beam
+    appends one token (copying a shared, partly filled last block first), all
+    beams decode, and in every request the lowest-ranked beam is dropped and
+    a random surviving beam forked in its place (ranks are seeded random:
+    there is no model). Returns the pool size and per step the copy pairs,
+    new-token slots, tables and context lengths.
+    """
+    from paged_kv_cache_288_gb300.block_pool import BlockPool
+
+    rng = np.random.default_rng(seed)
+    bs = block_size
+    prompts = rng.integers(prompt_lo, prompt_hi + 1, requests)
+    max_len = int(prompts.max()) + steps + 1
+    num_blocks = requests * (-(-int(prompts.max()) // bs)) + requests * beams * (-(-(steps + 1) // bs) + 2) + 1
+    pool = BlockPool(num_blocks, bs)
+    names = [[(r, b) for b in range(beams)] for r in range(requests)]
+    for r in range(requests):
+        pool.add_sequence(("p", r), int(prompts[r]))
+        for n in names[r]:
+            pool.fork(("p", r), n)
+        pool.free_sequence(("p", r))
+    order = [n for group in names for n in group]
+    width = -(-max_len // bs)
+    plan = []
+    for _ in range(steps):
+        pairs, slots = [], []
+        for n in order:
+            sl, cow = pool.append(n, 1)
+            pairs += cow
+            slots += sl
+        plan.append({"pairs": np.array(pairs, dtype=np.int64).reshape(-1, 2),
+                     "slots": np.array(slots, dtype=np.int64),
+                     "tables": pool.block_table_array(order, width=width, pad=0),
+                     "lens": pool.context_lens(order)})
+        for r in range(requests):
+            worst, best = rng.choice(beams, 2, replace=False)
+            pool.free_sequence(names[r][worst])
+            pool.fork(names[r][best], names[r][worst])
+    return num_blocks, width, plan
+
+
+def run_beam_reference(args, world, rank):
+    """The oracle on the beam-search plan: copies, cache writes and the decode
+    of a sample of beams per step, on host pools."""
+    if rank != 0:
+        return None
+    import oracle
+    H, Hkv, d, bs, sample = 32, 8, 128, 16, 4
+    num_blocks, width, plan = beam_plan(args.warmup + args.steps, rank_seed(1008, 0))
+    g = workloads._gen(1010)
+    kc = workloads.normal_bits(g, (num_blocks, Hkv, bs, d), workloads.BF16)
+    vc = workloads.normal_bits(g, (num_blocks, Hkv, bs, d), workloads.BF16)
+    B = plan[0]["lens"].shape[0]
+    q = workloads.normal_bits(g, (B, H, d), workloads.BF16)
+    nk = workloads.normal_bits(g, (B, Hkv, d), workloads.BF16)
+    secs, nbytes = [], []
+    for st in plan:
+        t = time.perf_counter()
+        oracle.copy_blocks([kc], [vc], st["pairs"])
+        oracle.reshape_and_cache(nk, nk, kc, vc, st["slots"], bs, workloads.BF16, workloads.BF16)
+        oracle.paged_decode(q[:sample], kc, vc, st["tables"][:sample], st["lens"][:sample],
+                            1.0 / math.sqrt(d), bs, workloads.BF16, workloads.BF16)
+        secs.append(time.perf_counter() - t)
+        nbytes.append(int(st["lens"][:sample].astype(np.int64).sum()) * Hkv * 2 * d * 2)
+    W = args.warmup
+    value = sum(nbytes[W:]) / sum(secs[W:]) / 1e9
+    return {"impl": "reference", "metric": METRIC + " (beam search step: copy-on-write + cache write + "
+            "decode, logical KV bytes)", "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": W, "ms_per_step": round(1e3 * sum(secs[W:]) / args.steps, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+            "data": "synthetic", "config": {"workload": args.workload, "sample_beams_per_step": sample},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"fp64 numpy oracle: every step's copies and cache writes, the "
+                                       f"decode of {sample} of {B} beams, 1 thread"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def run_beam(args, world, rank, local):
+    import paged_kv_cache_288_gb300 as pa
+    from paged_kv_cache_288_gb300 import build
+
+    build.build_library()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    H, Hkv, d, bs = 32, 8, 128, 16
+    W, K = args.warmup, args.steps
+    num_blocks, width, plan = beam_plan(W + K, rank_seed(1008, rank))
+    B = plan[0]["lens"].shape[0]
+    shape = (num_blocks, Hkv, bs, d)
+    kc = torch.empty(shape, dtype=torch.bfloat16, device=device).normal_()
+    vc = torch.empty(shape, dtype=torch.bfloat16, device=device).normal_()
+    kptr, vptr = pa.pointer_array([kc], device), pa.pointer_array([vc], device)
+    block_bytes = Hkv * bs * d * 2
+    g = torch.Generator(device="cpu").manual_seed(rank_seed(1009, rank))
+    dev_plan = []
+    for st in plan:
+        dev_plan.append({
+            "pairs": torch.from_numpy(st["pairs"]).to(device),
+            "slots": torch.from_numpy(st["slots"]).to(device),
+            "tables": torch.from_numpy(st["tables"]).to(device),
+            "lens": torch.from_numpy(st["lens"]).to(device),
+            "max": int(st["lens"].max())})
+    q = torch.randn(B, H, d, generator=g).to(torch.bfloat16).to(device)
+    nk = torch.randn(B, Hkv, d, generator=g).to(torch.bfloat16).to(device)
+    nv = torch.randn(B, Hkv, d, generator=g).to(torch.bfloat16).to(device)
+    out = torch.empty_like(q)
+    ws = torch.empty(pa.decode_workspace_size(B, H, Hkv, d, max(st["max"] for st in dev_plan), 0),
+                     dtype=torch.uint8, device=device)
+    err = torch.zeros(1, dtype=torch.int32, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step(st):
+        if st["pairs"].shape[0]:
+            pa.copy_blocks(kptr, vptr, st["pairs"], num_blocks, block_bytes, debug_err=err)
+        pa.reshape_and_cache(nk, nv, kc, vc, st["slots"], debug_err=err)
+        pa.decode(out, q, kc, vc, st["tables"], st["lens"], 1.0 / math.sqrt(d), st["max"],
+                  workspace=ws, debug_err=err)
+
+    for k in range(W):
+        flush.zero_()
+        flush.sum()
+        step(dev_plan[k])
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    n0 = pa.lib().pa_kernel_launch_count()
+    t0 = time.time()
+    for k in range(K):
+        flush.zero_()
+        flush.sum()
+        ev[k][0].record(stream)
+        step(dev_plan[W + k])
+        ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier(world)
+    n1 = pa.lib().pa_kernel_launch_count()
+    sampler.stop()
+    assert err.item() == 0, "a kernel flagged an out-of-range index"
+    # end to end through the public API: each step's plan (pairs, slots,
+    # tables, lengths) and new tokens come from pinned host memory, the
+    # output goes back to pinned host memory
+    Ke = min(K, 100)
+    host_plan = [{k: torch.from_numpy(v).pin_memory() for k, v in st.items()} for st in plan[W:W + Ke]]
+    h_nk, h_nv, h_out = nk.cpu().pin_memory(), nv.cpu().pin_memory(), torch.empty_like(out, device="cpu").pin_memory()
+    eev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Ke)]
+    h2d = d2h = 0
+    for k in range(Ke):
+        st, hp = dev_plan[W + k], host_plan[k]
+        flush.zero_()
+        flush.sum()
+        eev[k][0].record(stream)
+        for key in ("pairs", "slots", "tables", "lens"):
+            st[key].copy_(hp[key], non_blocking=True)
+        nk.copy_(h_nk, non_blocking=True)
+        nv.copy_(h_nv, non_blocking=True)
+        step(st)
+        h_out.copy_(out, non_blocking=True)
+        eev[k][1].record(stream)
+        h2d += sum(hp[key].numel() * hp[key].element_size() for key in ("pairs", "slots", "tables", "lens"))
+        h2d += 2 * h_nk.numel() * 2
+        d2h += h_out.numel() * 2
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(sum(eev[k][0].elapsed_time(eev[k][1]) for k in range(Ke)), world, device)
+    ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
+    total_ms = max_over_ranks(sum(ms), world, device)
+    timed = plan[W:]
+    kv_bytes = [int(st["lens"].astype(np.int64).sum()) * Hkv * 2 * d * 2 for st in timed]
+    copies = [st["pairs"].shape[0] for st in timed]
+    step_bytes = [kvb + 2 * B * H * d * 2 + 2 * c * 2 * block_bytes + 2 * B * Hkv * d * 2 * 2
+                  for kvb, c in zip(kv_bytes, copies)]
+    value = world * sum(step_bytes) / (total_ms / 1e3) / 1e9
+    if rank != 0:
+        return None
+    peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    peak = json.load(open(peaks_path))["hbm_gbs"] if os.path.exists(peaks_path) else 6800.0
+    return {
+        "metric": METRIC + " (beam search step: copy-on-write + cache write + decode, logical KV bytes)",
+        "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": round(total_ms / K, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (random pools, seeded beam ranks)",
+        "config": {"workload": args.workload, "requests": 16, "beams": 4, "num_seqs": B,
+                   "num_heads": H, "num_kv_heads": Hkv, "head_dim": d, "block_size": bs,
+                   "prompt_tokens": "uniform 1536..2560", "num_blocks": num_blocks,
+                   "l2": "flushed between steps: 256 MiB written then read back, outside the timed events",
+                   "parallelism": f"{world} independent replica(s), one per GPU"},
+        "tokens_per_s_per_layer": round(world * B * K / (total_ms / 1e3), 1),
+        "copies_per_step": round(statistics.mean(copies), 2),
+        "roofline": {"bound": "hbm", "achieved": round(value, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(value / peak, 4), "traffic": None,
+                     "kernel": "copy_blocks + reshape_and_cache + pa_decode (logical bytes: "
+                               "beams re-read their shared prompt blocks, mostly from L2)"},
+        "e2e": {"value": round(world * sum(step_bytes[:Ke]) / (e2e_ms / 1e3) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d // Ke, "d2h_bytes_per_step": d2h // Ke, "steps": Ke},
+        "clocks": sampler.summary(t0, t1), "gpu_launches": n1 - n0,
+        "launches_per_step": (n1 - n0) / K,
+        **({} if args.no_cpu_baseline or world != 1 else {"cpu_baseline": beam_cpu_baseline()}),
+    }
+
+
+def beam_cpu_baseline():
+    """The oracle arm on about 10 s of steps."""
+    ns = argparse.Namespace(warmup=0, steps=200)
+    ref = run_beam_reference(ns, 1, 0)
+    return ref["cpu_baseline"]
 
 
 # ----------------------------------------------------------------------------
@@ -712,8 +997,14 @@ def main():
         ap.error("at least 3 warm-up steps")
     world, rank, local = setup_dist()
     swap = args.workload.startswith("swap")
+    beam = args.workload.startswith("beam")
     if args.impl == "reference":
-        line = run_swap_reference(args, world, rank) if swap else run_reference(args, world, rank)
+        if beam:
+            line = run_beam_reference(args, world, rank)
+        else:
+            line = run_swap_reference(args, world, rank) if swap else run_reference(args, world, rank)
+    elif beam:
+        line = run_beam(args, world, rank, local)
     else:
         line = run_swap(args, world, rank, local) if swap else run_ours(args, world, rank, local)
     if line is not None:

@@ -18,7 +18,18 @@ This is the bookkeeping that sits above the kernels (it is not timed):
 
 ``append`` returns the (src, dst) pairs that must be copied with
 ``pa_copy_blocks`` before the new tokens are written.
+
+``PrefixCache`` adds automatic sharing of common prompt prefixes (prefix
+caching, which caches the blocks of shared prompt beginnings so that they
+are neither recomputed nor stored twice: LLM 추론 확장, 품질·비용 절충 필수,
+the paragraph on prefix caching; serving-paged-attention, "공유는 표를
+베끼는 일이 된다", the 100 requests with one system prompt). A full block
+is found by a key that chains its token ids to the key of the block before
+it, so equal keys mean equal prefixes up to and including that block.
 """
+
+import hashlib
+from collections import OrderedDict
 
 import numpy as np
 
@@ -141,3 +152,108 @@ class BlockPool:
 
     def used_blocks(self):
         return self.num_blocks - self.num_free
+
+
+def block_key(parent_key, token_ids):
+    """Key of a full block: BLAKE2b-128 of the parent block's key and the
+    block's token ids (int64, little endian). The first block's parent key is
+    the empty byte string."""
+    h = hashlib.blake2b(digest_size=16)
+    h.update(parent_key)
+    h.update(np.asarray(token_ids, dtype="<i8").tobytes())
+    return h.digest()
+
+
+class PrefixCache:
+    """Full blocks of earlier prompts, found by their chained keys.
+
+    The cache holds one reference of its own on every block it maps, so a
+    cached block outlives the requests that filled it; such a block with no
+    other holder is evictable, least recently used first, when the pool runs
+    out of free blocks. Only full blocks are cached (a partly filled last
+    block still changes).
+    """
+
+    def __init__(self, pool):
+        self.pool = pool
+        self.block_of = {}      # key -> physical block
+        self.key_of = {}        # physical block -> key
+        self._lru = OrderedDict()  # cached blocks nobody else holds, oldest first
+        self.hits = 0
+        self.misses = 0
+
+    def _touch(self, b):
+        if self.pool.refcount[b] == 1:
+            self._lru[b] = True
+            self._lru.move_to_end(b)
+        else:
+            self._lru.pop(b, None)
+
+    def evict(self, n):
+        """Return up to n evictable cached blocks to the free list."""
+        done = 0
+        while done < n and self._lru:
+            b, _ = self._lru.popitem(last=False)
+            del self.block_of[self.key_of.pop(b)]
+            self.pool._release(b)
+            done += 1
+        return done
+
+    def add_sequence(self, seq_id, token_ids):
+        """New sequence for a prompt: its longest cached run of full blocks is
+        shared; the rest is allocated. Returns (number of prompt tokens whose
+        K/V are already cached, slots of the remaining prompt tokens, which
+        the caller computes and writes with pa_reshape_and_cache)."""
+        pool, bs = self.pool, self.pool.block_size
+        tokens = np.asarray(token_ids, dtype=np.int64)
+        n_full = len(tokens) // bs
+        keys, key = [], b""
+        for j in range(n_full):
+            key = block_key(key, tokens[j * bs:(j + 1) * bs])
+            keys.append(key)
+        shared = []
+        for k in keys:
+            b = self.block_of.get(k)
+            if b is None:
+                break
+            shared.append(b)
+        self.hits += len(shared)
+        self.misses += n_full - len(shared)
+        need = -(-len(tokens) // bs) - len(shared)
+        if need > pool.num_free:
+            # evictable blocks other than the ones this request is about to share
+            for b in shared:
+                self._lru.pop(b, None)
+            self.evict(need - pool.num_free)
+        if need > pool.num_free:
+            for b in shared:
+                self._touch(b)
+            raise OutOfBlocks(f"prompt of {len(tokens)} tokens needs {need} blocks, {pool.num_free} free")
+        if seq_id in pool.tables:
+            raise KeyError(f"sequence {seq_id} exists")
+        for b in shared:
+            pool.refcount[b] += 1
+            self._lru.pop(b, None)
+        pool.tables[seq_id] = list(shared)
+        pool.lengths[seq_id] = len(shared) * bs
+        slots, cow = pool.append(seq_id, len(tokens) - len(shared) * bs)
+        assert not cow
+        # the newly filled full blocks become cached (the caller writes them
+        # in the same step, before any later request can read them)
+        table = pool.tables[seq_id]
+        for j in range(len(shared), n_full):
+            b = table[j]
+            if keys[j] not in self.block_of:
+                self.block_of[keys[j]] = b
+                self.key_of[b] = keys[j]
+                pool.refcount[b] += 1
+        return len(shared) * bs, slots
+
+    def free_sequence(self, seq_id):
+        """Release a sequence; its cached blocks stay cached (evictable once no
+        other sequence holds them)."""
+        blocks = list(self.pool.tables[seq_id])
+        self.pool.free_sequence(seq_id)
+        for b in blocks:
+            if b in self.key_of:
+                self._touch(b)

@@ -4,7 +4,7 @@ import numpy as np
 import pytest
 
 import oracle
-from paged_kv_cache_288_gb300 import BlockPool, OutOfBlocks
+from paged_kv_cache_288_gb300 import BlockPool, OutOfBlocks, PrefixCache, block_key
 
 
 def test_grows_one_block_at_a_time():
@@ -109,3 +109,84 @@ def test_block_table_array_padding():
     assert t.dtype == np.int32 and t.shape == (2, 4)
     assert list(t[1, 1:]) == [7, 7, 7]
     assert list(pool.context_lens([0, 1])) == [9, 2]
+
+
+# ----------------------------------------------------------------------------
+# prefix cache
+
+
+def _prompt(seed, n):
+    return np.random.default_rng(seed).integers(0, 32000, n)
+
+
+def test_prefix_cache_shares_the_full_blocks_of_a_common_prefix():
+    pool = BlockPool(64, 16)
+    cache = PrefixCache(pool)
+    common = _prompt(1, 40)
+    a = np.concatenate([common, _prompt(2, 10)])
+    b = np.concatenate([common, _prompt(3, 30)])
+    cached, slots = cache.add_sequence("a", a)
+    assert cached == 0 and len(slots) == 50
+    cached, slots = cache.add_sequence("b", b)
+    # 40 common tokens = 2 full blocks (32 tokens) + 8 in a block that differs
+    assert cached == 32 and len(slots) == 70 - 32
+    assert pool.tables["b"][:2] == pool.tables["a"][:2]
+    assert pool.tables["b"][2] != pool.tables["a"][2]
+    assert slots[0] == pool.tables["b"][2] * 16
+    # refcounts: a, b and the cache hold the two shared blocks
+    assert all(pool.refcount[x] == 3 for x in pool.tables["a"][:2])
+    assert cache.hits == 2 and cache.misses == 3 + 2
+
+
+def test_prefix_cache_keys_chain_the_whole_prefix():
+    t = _prompt(4, 32)
+    k1 = block_key(b"", t[:16])
+    assert block_key(b"", t[:16]) == k1
+    assert block_key(k1, t[16:]) != block_key(b"", t[16:])  # same tokens, other position
+    u = t.copy()
+    u[3] += 1  # an earlier change makes every later block different
+    assert block_key(block_key(b"", u[:16]), u[16:]) != block_key(k1, t[16:])
+    pool = BlockPool(16, 16)
+    cache = PrefixCache(pool)
+    cache.add_sequence("t", t)
+    cached, _ = cache.add_sequence("u", u)
+    assert cached == 0
+
+
+def test_prefix_cache_keeps_blocks_after_the_request_and_evicts_oldest():
+    pool = BlockPool(6, 4)
+    cache = PrefixCache(pool)
+    p, q = _prompt(5, 8), _prompt(6, 8)
+    cache.add_sequence("p", p)
+    cache.free_sequence("p")
+    assert pool.num_free == 4  # the two full blocks stay cached
+    cached, _ = cache.add_sequence("p2", p)
+    assert cached == 8 and pool.num_free == 4
+    cache.free_sequence("p2")
+    cache.add_sequence("q", q)  # caches two more blocks: pool has 2 free
+    cache.free_sequence("q")
+    assert pool.num_free == 2
+    # a 16-token prompt needs 4 blocks: the two oldest cached blocks (p's) go
+    cached, _ = cache.add_sequence("r", _prompt(7, 16))
+    assert cached == 0
+    assert cache.add_sequence("q2", q)[0] == 8     # q is still cached
+    with pytest.raises(OutOfBlocks):
+        cache.add_sequence("p3", np.concatenate([p, p]))
+
+
+def test_prefix_cache_one_hundred_requests_over_one_system_prompt():
+    """The pages' example: 100 requests starting with the same system prompt
+    keep one copy of its full blocks (1016 tokens: 63 full blocks + 8 tokens)."""
+    pool = BlockPool(4000, 16)
+    cache = PrefixCache(pool)
+    system = _prompt(8, 1016)
+    for i in range(100):
+        suffix = _prompt(100 + i, 40)
+        cached, slots = cache.add_sequence(i, np.concatenate([system, suffix]))
+        assert cached == (0 if i == 0 else 63 * 16)
+        assert len(slots) == 1056 - cached
+    shared = pool.tables[0][:63]
+    assert all(pool.tables[i][:63] == shared for i in range(100))
+    assert all(pool.refcount[b] == 101 for b in shared)
+    # blocks in use: 63 shared + per request ceil((1056 - 1008) / 16) = 3 own
+    assert pool.used_blocks() == 63 + 100 * 3

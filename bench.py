@@ -735,7 +735,7 @@ def run_beam(args, world, rank, local):
 
 def beam_cpu_baseline():
     """The oracle arm on about 10 s of steps."""
-    ns = argparse.Namespace(warmup=0, steps=200)
+    ns = argparse.Namespace(warmup=0, steps=200, workload="beam_llama8b")
     ref = run_beam_reference(ns, 1, 0)
     return ref["cpu_baseline"]
 

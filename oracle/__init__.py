@@ -42,6 +42,7 @@ from .paged_attention import (
     gather_sequence,
     paged_decode,
     paged_decode_partitioned,
+    paged_prefill,
 )
 
 __all__ = [
@@ -63,4 +64,5 @@ __all__ = [
     "gather_sequence",
     "paged_decode",
     "paged_decode_partitioned",
+    "paged_prefill",
 ]

@@ -212,3 +212,45 @@ def paged_decode_partitioned(q, k_cache, v_cache, block_tables, context_lens,
                 w = np.array([np.exp(mp - m) * lp for mp, lp in zip(ms, ls)])
                 out[i, h] = (w[:, None] * np.array(os_)).sum(axis=0) / w.sum()
     return out
+
+
+def paged_prefill(q, k_cache, v_cache, block_tables, context_lens, query_start, scale,
+                  block_size, q_dtype, kv_dtype):
+    """Causal attention of each sequence's chunk of new query tokens over its
+    paged KV, float64.
+
+    The step before decode: a prompt (or a chunk of it, after earlier chunks
+    are already cached) is attended with many queries at once (LLM 추론 확장,
+    품질·비용 절충 필수, the prefill / decode split; serving-paged-attention,
+    "블록으로 쪼개고 표로 잇는다": the same block tables serve both). Sequence i
+    holds context_lens[i] tokens, the last n_i = query_start[i+1] -
+    query_start[i] of which are its queries (their K/V already written).
+    Query j of sequence i sits at position p = context_lens[i] - n_i + j and
+    attends to the keys at positions 0..p:
+
+        out[query_start[i] + j, h] = softmax(scale * K[0..p] q) V[0..p]
+
+    with K, V the sequence's rows gathered through its table for KV head
+    h // G. ``q`` and the result are [num_tokens, num_heads, head_dim].
+    """
+    qf = bits_to_f64(q, q_dtype)
+    num_tokens, num_heads, head_dim = qf.shape
+    num_kv_heads = k_cache.shape[1]
+    group = num_heads // num_kv_heads
+    out = np.zeros((num_tokens, num_heads, head_dim))
+    for i in range(len(context_lens)):
+        ctx = int(context_lens[i])
+        q0, q1 = int(query_start[i]), int(query_start[i + 1])
+        n = q1 - q0
+        if n <= 0:
+            continue
+        for g in range(num_kv_heads):
+            K = gather_sequence(k_cache, block_tables[i], ctx, block_size, g, kv_dtype)
+            V = gather_sequence(v_cache, block_tables[i], ctx, block_size, g, kv_dtype)
+            for j in range(n):
+                p = ctx - n + j
+                for h in range(g * group, (g + 1) * group):
+                    s = scale * (K[:p + 1] @ qf[q0 + j, h])
+                    w = np.exp(s - s.max())
+                    out[q0 + j, h] = (w @ V[:p + 1]) / w.sum()
+    return out

@@ -535,3 +535,62 @@ def test_planted_mistakes_are_caught(monkeypatch):
             err = float("inf")
         assert not err < 1e-6, name
         monkeypatch.setattr(oracle.paged_attention, "gather_sequence", real_gather)
+
+
+# ----------------------------------------------------------------------------
+# prefill
+
+
+def test_prefill_without_prefix_is_causal_sdpa():
+    """With no cached prefix the chunk is the whole sequence: torch's causal
+    scaled_dot_product_attention (float64) over the gathered K/V."""
+    case = workloads.prefill_case(51, [0, 0, 0], [1, 17, 40], 8, 2, 16, 16, BF16)
+    out = oracle.paged_prefill(case.q, case.k_cache, case.v_cache, case.block_tables, case.context_lens,
+                               case.query_start, case.scale, 16, BF16, BF16)
+    qf = _f(case.q, BF16)
+    for i, n in enumerate(case.context_lens):
+        n = int(n)
+        nb = -(-n // 16)
+        ids = case.block_tables[i, :nb]
+        K = torch.from_numpy(_f(case.k_cache[ids], BF16)).permute(1, 0, 2, 3).reshape(2, -1, 16)[:, :n]
+        V = torch.from_numpy(_f(case.v_cache[ids], BF16)).permute(1, 0, 2, 3).reshape(2, -1, 16)[:, :n]
+        K, V = K.repeat_interleave(4, dim=0), V.repeat_interleave(4, dim=0)
+        q0 = int(case.query_start[i])
+        Q = torch.from_numpy(qf[q0:q0 + n]).permute(1, 0, 2)  # [Hq, n, d]
+        ref = torch.nn.functional.scaled_dot_product_attention(Q, K, V, is_causal=True, scale=case.scale)
+        np.testing.assert_allclose(out[q0:q0 + n], ref.permute(1, 0, 2).numpy(), rtol=1e-11, atol=1e-12)
+
+
+def test_prefill_query_equals_decode_over_its_prefix():
+    """Query j of a chunk after a cached prefix sees exactly the first
+    ctx - n + j + 1 tokens: it equals a single-query decode over a context cut
+    to that length."""
+    case = workloads.prefill_case(52, [0, 5, 16, 33], [3, 12, 1, 20], 4, 2, 8, 8, F16)
+    out = oracle.paged_prefill(case.q, case.k_cache, case.v_cache, case.block_tables, case.context_lens,
+                               case.query_start, case.scale, 8, F16, F16)
+    for i in range(case.num_seqs):
+        q0, q1 = int(case.query_start[i]), int(case.query_start[i + 1])
+        n, ctx = q1 - q0, int(case.context_lens[i])
+        for j in range(n):
+            dec = oracle.paged_decode(case.q[q0 + j:q0 + j + 1], case.k_cache, case.v_cache,
+                                      case.block_tables[i:i + 1], np.array([ctx - n + j + 1], np.int32),
+                                      case.scale, 8, F16, F16)
+            np.testing.assert_allclose(out[q0 + j], dec[0], rtol=1e-12, atol=1e-13)
+
+
+def test_prefill_brute_force_loops():
+    case = workloads.prefill_case(53, [2, 9], [4, 3], 2, 1, 4, 4, F16)
+    out = oracle.paged_prefill(case.q, case.k_cache, case.v_cache, case.block_tables, case.context_lens,
+                               case.query_start, case.scale, 4, F16, F16)
+    for i in range(2):
+        ctx = int(case.context_lens[i])
+        rows = [(int(case.block_tables[i, p // 4]), p % 4) for p in range(ctx)]
+        q0, q1 = int(case.query_start[i]), int(case.query_start[i + 1])
+        for j in range(q1 - q0):
+            last = ctx - (q1 - q0) + j
+            for h in range(2):
+                qv = list(_f(case.q[q0 + j, h], F16))
+                K = [list(_f(case.k_cache[b, 0, o], F16)) for b, o in rows[:last + 1]]
+                V = [list(_f(case.v_cache[b, 0, o], F16)) for b, o in rows[:last + 1]]
+                ref = _brute_force_decode(qv, K, V, case.scale)
+                np.testing.assert_allclose(out[q0 + j, h], ref, rtol=1e-12, atol=1e-14)

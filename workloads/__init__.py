@@ -19,6 +19,9 @@ Inputs follow the shapes of the five workloads:
 * ``fp8_step``: batch 256, 32/8/128, block size 16, lognormal lengths (mean
   500, clipped to [16, 2048]), E4M3 KV with one float32 scale per (block, KV
   head), bf16 queries.
+* ``prefill``: chunked prefill, 16 sequences with cached prefixes uniform in
+  [0, 2048] tokens and a 512-token chunk of new queries each, 32/8/128, bf16,
+  block size 16.
 
 Random values are i.i.d. N(0, 1) drawn with ``torch.Generator('cpu')`` and
 rounded to the storage type. Physical block ids are a seeded permutation of
@@ -385,3 +388,80 @@ def random_small_case(seed, *, num_seqs, group, num_kv_heads, head_dim, block_si
     ctx = torch.randint(min_ctx, max_ctx + 1, (num_seqs,), generator=g).numpy().astype(np.int64)
     return paged_case(seed + 7, ctx, group * num_kv_heads, num_kv_heads, head_dim,
                       block_size, dtype, name=f"rand{seed}", append=append, q_dtype=q_dtype)
+
+
+@dataclass
+class PrefillCase:
+    """A chunked-prefill problem: every sequence's last chunk of tokens are
+    queries; the K/V of all its tokens (chunk included) are in the pool."""
+
+    num_seqs: int
+    num_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    num_blocks: int
+    dtype: str
+    scale: float
+    q: np.ndarray                 # [T, Hq, d] raw bits, chunks packed in sequence order
+    k_cache: np.ndarray           # [Nb, Hkv, bs, d] raw bits
+    v_cache: np.ndarray
+    block_tables: np.ndarray      # int32 [B, width]
+    context_lens: np.ndarray      # int32 [B], chunk included
+    query_start: np.ndarray       # int32 [B + 1]
+    new_key: np.ndarray           # [T, Hkv, d]: the chunks' K/V, as stored in the pool
+    new_value: np.ndarray
+    slot_mapping: np.ndarray      # int64 [T]: the chunks' slots
+    poison_block: int = -1
+
+    @property
+    def max_query_len(self):
+        return int(np.diff(self.query_start).max()) if self.num_seqs else 0
+
+
+def prefill_case(seed, prefix_lens, chunk_lens, num_heads, num_kv_heads, head_dim, block_size,
+                 dtype, *, pool_factor=1.25, table_width=None):
+    """Random K/V for every token of prefix + chunk, queries for the chunks."""
+    g = _gen(seed)
+    pre = np.asarray(prefix_lens, dtype=np.int64)
+    chunk = np.asarray(chunk_lens, dtype=np.int64)
+    ctx = pre + chunk
+    bs = block_size
+    nbs = [int(-(-c // bs)) for c in ctx]
+    need = sum(nbs)
+    num_blocks = max(int(math.ceil(pool_factor * need)), need) + 1
+    poison = int(torch.randint(num_blocks, (1,), generator=g).item())
+    width = table_width or max(max(nbs + [1]), 1)
+    tables, _ = _assign_tables(g, nbs, num_blocks, width, poison)
+    shape = (num_blocks, num_kv_heads, bs, head_dim)
+    k_cache = normal_bits(g, shape, dtype)
+    v_cache = normal_bits(g, shape, dtype)
+    k_cache[poison] = NAN_BITS[dtype]
+    v_cache[poison] = NAN_BITS[dtype]
+    _poison_tails(k_cache, tables, ctx, bs, dtype)
+    _poison_tails(v_cache, tables, ctx, bs, dtype)
+    qs = np.zeros(len(ctx) + 1, dtype=np.int32)
+    qs[1:] = np.cumsum(chunk)
+    T = int(qs[-1])
+    slots = np.empty(T, dtype=np.int64)
+    t = 0
+    for i in range(len(ctx)):
+        for pos in range(int(pre[i]), int(ctx[i])):
+            slots[t] = int(tables[i, pos // bs]) * bs + pos % bs
+            t += 1
+    blk, off = slots // bs, slots % bs
+    new_key = k_cache[blk, :, off, :].copy() if T else np.zeros((0, num_kv_heads, head_dim), np.uint16)
+    new_value = v_cache[blk, :, off, :].copy() if T else np.zeros((0, num_kv_heads, head_dim), np.uint16)
+    q = normal_bits(g, (T, num_heads, head_dim), dtype)
+    return PrefillCase(
+        num_seqs=len(ctx), num_heads=num_heads, num_kv_heads=num_kv_heads, head_dim=head_dim,
+        block_size=bs, num_blocks=num_blocks, dtype=dtype, scale=1.0 / math.sqrt(head_dim),
+        q=q, k_cache=k_cache, v_cache=v_cache, block_tables=tables,
+        context_lens=ctx.astype(np.int32), query_start=qs, new_key=new_key, new_value=new_value,
+        slot_mapping=slots, poison_block=poison)
+
+
+def prefill_llama8b(seed=1011, num_seqs=16, chunk=512, prefix_hi=2048):
+    g = _gen(seed)
+    pre = torch.randint(0, prefix_hi + 1, (num_seqs,), generator=g).numpy()
+    return prefill_case(seed + 1, pre, [chunk] * num_seqs, 32, 8, 128, 16, BF16)

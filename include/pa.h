@@ -176,6 +176,43 @@ pa_status pa_copy_blocks(void* const* k_caches, void* const* v_caches,
                          size_t block_bytes, int32_t* debug_err,
                          cudaStream_t stream);
 
+/*
+ * pa_prefill - causal attention of each sequence's chunk of new query tokens
+ * over its paged KV cache (the prompt, or a chunk of it after earlier chunks
+ * were cached: chunked prefill).
+ *
+ * Prefill is the many-query step before decode (LLM 추론 확장, 품질·비용 절충
+ * 필수, the prefill / decode split) and reads the same block tables
+ * (serving-paged-attention, "블록으로 쪼개고 표로 잇는다"). Sequence i holds
+ * context_lens[i] tokens whose K/V are in the caches (write the chunk's own
+ * K/V with pa_reshape_and_cache first); its queries are the last
+ * n_i = query_start[i+1] - query_start[i] of them, rows query_start[i] ..
+ * query_start[i+1]-1 of q. Query j sits at position context_lens[i] - n_i + j
+ * and attends to positions 0..that:
+ *   out[query_start[i] + j, h] = softmax(scale * q . K[0..p]) V[0..p],
+ * K, V of KV head h / (num_heads / num_kv_heads).
+ *
+ * q, out: DEVICE [num_tokens, num_heads, head_dim] of `dtype`, 16-byte
+ * aligned; caches as for pa_decode, same dtype; block_tables, context_lens,
+ * query_start (int32 [num_seqs + 1], non-decreasing, query_start[0] = 0,
+ * query_start[num_seqs] = num_tokens): DEVICE. max_query_len bounds n_i (it
+ * sizes the grid; chunks beyond it are not computed). Sequences whose
+ * context is shorter than their chunk, or longer than the table holds, set
+ * PA_DEVERR_CONTEXT_RANGE; table entries outside [0, num_blocks) set
+ * PA_DEVERR_BLOCK_RANGE and their keys are skipped.
+ *
+ * Supported: dtype PA_F16 or PA_BF16, head_dim 128, num_heads / num_kv_heads
+ * in {1, 2, 4, 8}, block_size in {8, 16, 32, 64}; others return
+ * PA_ERR_UNSUPPORTED.
+ */
+pa_status pa_prefill(void* out, const void* q, const void* k_cache, const void* v_cache,
+                     const int32_t* block_tables, int32_t max_blocks_per_seq,
+                     const int32_t* context_lens, const int32_t* query_start,
+                     int32_t num_seqs, int32_t num_tokens, int32_t max_query_len,
+                     int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                     int32_t block_size, int32_t num_blocks, float scale, pa_dtype dtype,
+                     int32_t* debug_err, cudaStream_t stream);
+
 /* Layers one pa_swap_blocks call moves at most. */
 #define PA_SWAP_MAX_LAYERS 64
 

@@ -66,6 +66,10 @@ def lib():
             _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int32, _c_ptr, _c_int32, _c_int32,
             _c_int32, _c_int32, _c_int32, _c_int32, ctypes.c_float, ctypes.c_int, ctypes.c_int,
             _c_ptr, _c_ptr, _c_int32, _c_int32, _c_ptr, _c_ptr]
+        L.pa_prefill.restype = ctypes.c_int
+        L.pa_prefill.argtypes = [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int32, _c_ptr, _c_ptr,
+                                 _c_int32, _c_int32, _c_int32, _c_int32, _c_int32, _c_int32,
+                                 _c_int32, _c_int32, ctypes.c_float, ctypes.c_int, _c_ptr, _c_ptr]
         L.pa_swap_blocks.restype = ctypes.c_int
         L.pa_swap_blocks.argtypes = [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int32, _c_ptr, _c_int32,
                                      _c_int32, _c_int32, _c_size, _c_ptr, _c_ptr]
@@ -148,6 +152,27 @@ def decode(out, q, k_cache, v_cache, block_tables, context_lens, scale, max_cont
         _dtype_code(q.dtype), _dtype_code(k_cache.dtype), _ptr(k_scale), _ptr(v_scale),
         int(max_context_len), int(partition_size), _ptr(workspace), ws_bytes, _ptr(debug_err),
         _stream(stream)), "pa_decode")
+
+
+def prefill(out, q, k_cache, v_cache, block_tables, context_lens, query_start, scale,
+            max_query_len, debug_err=None, stream=None):
+    """out[T, Hq, d] = causal attention of each sequence's chunk of queries (rows
+    query_start[i] .. query_start[i+1]-1 of q[T, Hq, d]) over its paged KV."""
+    T, Hq, d = q.shape
+    Nb, Hkv, bs, d2 = k_cache.shape
+    if d2 != d or out.shape != q.shape or v_cache.shape != k_cache.shape or q.dtype != k_cache.dtype:
+        raise ValueError("shape or dtype mismatch")
+    for t, name in ((block_tables, "block_tables"), (context_lens, "context_lens"),
+                    (query_start, "query_start")):
+        if t.dtype != torch.int32:
+            raise ValueError(f"{name} must be int32")
+    B = context_lens.numel()
+    if query_start.numel() != B + 1 or block_tables.dim() != 2 or block_tables.shape[0] != B:
+        raise ValueError("query_start must be [num_seqs + 1]; block_tables [num_seqs, width]")
+    _check(lib().pa_prefill(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
+        _ptr(context_lens), _ptr(query_start), B, T, int(max_query_len), Hq, Hkv, d, bs, Nb,
+        float(scale), _dtype_code(q.dtype), _ptr(debug_err), _stream(stream)), "pa_prefill")
 
 
 def decode_split_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, scale,

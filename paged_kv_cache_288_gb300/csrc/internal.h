@@ -27,6 +27,15 @@ cudaError_t launch_copy_blocks(void* const* k_caches, void* const* v_caches, int
                                const int64_t* block_mapping, int num_pairs, int num_blocks,
                                size_t block_bytes, int32_t* debug_err, cudaStream_t stream);
 
+// Paged prefill on tcgen05 (prefill_tc.cu).
+bool prefill_supported(int group, int head_dim, pa_dtype dtype, int block_size);
+cudaError_t launch_prefill_tc(void* out, const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* block_tables, int max_blocks_per_seq,
+                              const int32_t* context_lens, const int32_t* query_start, int num_seqs,
+                              int num_tokens, int max_query_len, int num_heads, int num_kv_heads,
+                              int block_size, int num_blocks, float scale, pa_dtype dtype,
+                              int32_t* debug_err, cudaStream_t stream);
+
 // Per-layer pool pointers of one swap, all device-accessible.
 struct SwapPools {
   const void* src[2][PA_SWAP_MAX_LAYERS];  // [K, V][layer]

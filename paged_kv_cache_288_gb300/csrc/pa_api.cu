@@ -282,6 +282,35 @@ pa_status pa_copy_blocks(void* const* k_caches, void* const* v_caches, int32_t n
                    "copy_blocks launch");
 }
 
+pa_status pa_prefill(void* out, const void* q, const void* k_cache, const void* v_cache,
+                     const int32_t* block_tables, int32_t max_blocks_per_seq,
+                     const int32_t* context_lens, const int32_t* query_start, int32_t num_seqs,
+                     int32_t num_tokens, int32_t max_query_len, int32_t num_heads,
+                     int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                     float scale, pa_dtype dtype, int32_t* debug_err, cudaStream_t stream) {
+  if (num_seqs < 0 || num_tokens < 0 || max_query_len < 0) return fail(PA_ERR_INVALID, "negative count");
+  if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0)
+    return fail(PA_ERR_INVALID, "num_heads must be a positive multiple of num_kv_heads");
+  if (block_size != 8 && block_size != 16 && block_size != 32 && block_size != 64)
+    return fail(PA_ERR_UNSUPPORTED, "block_size %d not in {8, 16, 32, 64}", block_size);
+  if (num_blocks <= 0 || max_blocks_per_seq <= 0) return fail(PA_ERR_INVALID, "empty pool or table");
+  if (dtype != PA_F16 && dtype != PA_BF16) return fail(PA_ERR_UNSUPPORTED, "prefill takes f16 or bf16");
+  if (!pa::prefill_supported(num_heads / num_kv_heads, head_dim, dtype, block_size))
+    return fail(PA_ERR_UNSUPPORTED, "prefill supports head_dim 128 and groups 1, 2, 4, 8");
+  if (num_seqs == 0 || num_tokens == 0 || max_query_len == 0) return PA_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !query_start)
+    return fail(PA_ERR_INVALID, "null pointer");
+  if (reinterpret_cast<uintptr_t>(q) % 16 || reinterpret_cast<uintptr_t>(out) % 16 ||
+      reinterpret_cast<uintptr_t>(k_cache) % 16 || reinterpret_cast<uintptr_t>(v_cache) % 16)
+    return fail(PA_ERR_INVALID, "q, out and the caches must be 16-byte aligned");
+  if (num_seqs > 65535) return fail(PA_ERR_UNSUPPORTED, "more than 65535 sequences");
+  return from_cuda(pa::launch_prefill_tc(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                         context_lens, query_start, num_seqs, num_tokens, max_query_len,
+                                         num_heads, num_kv_heads, block_size, num_blocks, scale, dtype,
+                                         debug_err, stream),
+                   "prefill launch");
+}
+
 // The device-side address of `p` when the device can read and write it (device
 // or managed memory, or pinned host memory mapped into the device's address
 // space), else nullptr.

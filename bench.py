@@ -519,6 +519,187 @@ def run_ours(args, world, rank, local):
 
 
 # ----------------------------------------------------------------------------
+# chunked prefill (pa_reshape_and_cache of the chunks + pa_prefill)
+
+PREFILL_METRIC = "pa_prefill TFLOP/s (causal chunked prefill over the paged cache)"
+
+
+def prefill_flops(case):
+    """Algorithmic FLOPs of one pa_prefill: per query at position p and head,
+    2*d*(p+1) for q.K and as many for P.V."""
+    total = 0
+    for i in range(case.num_seqs):
+        n = int(case.query_start[i + 1] - case.query_start[i])
+        ctx = int(case.context_lens[i])
+        keys = n * (ctx - n) + n * (n + 1) // 2  # sum over j of (ctx - n + j + 1)
+        total += 4 * case.head_dim * keys * case.num_heads
+    return total
+
+
+def run_prefill(args, world, rank, local):
+    import paged_kv_cache_288_gb300 as pa
+    from paged_kv_cache_288_gb300 import build
+
+    build.build_library()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    case = workloads.prefill_llama8b(seed=rank_seed(1011, rank))
+
+    def to_dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(torch.bfloat16)
+
+    q, kc, vc = to_dev(case.q), to_dev(case.k_cache), to_dev(case.v_cache)
+    nk, nv = to_dev(case.new_key), to_dev(case.new_value)
+    slots = torch.from_numpy(case.slot_mapping).to(device)
+    tables = torch.from_numpy(case.block_tables).to(device)
+    lens = torch.from_numpy(case.context_lens).to(device)
+    qs = torch.from_numpy(case.query_start).to(device)
+    out = torch.empty_like(q)
+    err = torch.zeros(1, dtype=torch.int32, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    mq = case.max_query_len
+
+    def step():
+        pa.reshape_and_cache(nk, nv, kc, vc, slots, debug_err=err)
+        pa.prefill(out, q, kc, vc, tables, lens, qs, case.scale, mq, debug_err=err)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        flush.sum()
+        step()
+    torch.cuda.synchronize()
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    n0 = pa.lib().pa_kernel_launch_count()
+    t0 = time.time()
+    for k in range(K):
+        flush.zero_()
+        flush.sum()
+        ev[k][0].record(stream)
+        pa.reshape_and_cache(nk, nv, kc, vc, slots, debug_err=err)
+        ev[k][1].record(stream)
+        pa.prefill(out, q, kc, vc, tables, lens, qs, case.scale, mq, debug_err=err)
+        ev[k][2].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier(world)
+    n1 = pa.lib().pa_kernel_launch_count()
+    sampler.stop()
+    assert err.item() == 0, "a kernel flagged an out-of-range index"
+    step_ms = [ev[k][0].elapsed_time(ev[k][2]) for k in range(K)]
+    pf_ms = statistics.mean(ev[k][1].elapsed_time(ev[k][2]) for k in range(K))
+    total_ms = max_over_ranks(sum(step_ms), world, device)
+    flops = prefill_flops(case)
+    value = world * flops * K / (total_ms / 1e3) / 1e12
+    achieved = flops / (pf_ms / 1e3) / 1e12
+
+    # end to end: queries and the chunks' K/V from pinned host memory, output back
+    h_q, h_nk, h_nv = q.cpu().pin_memory(), nk.cpu().pin_memory(), nv.cpu().pin_memory()
+    h_out = torch.empty_like(out, device="cpu").pin_memory()
+    Ke = min(K, 50)
+    eev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Ke)]
+    for k in range(Ke):
+        flush.zero_()
+        flush.sum()
+        eev[k][0].record(stream)
+        q.copy_(h_q, non_blocking=True)
+        nk.copy_(h_nk, non_blocking=True)
+        nv.copy_(h_nv, non_blocking=True)
+        step()
+        h_out.copy_(out, non_blocking=True)
+        eev[k][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(sum(eev[k][0].elapsed_time(eev[k][1]) for k in range(Ke)), world, device)
+    if rank != 0:
+        return None
+    peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    peaks = json.load(open(peaks_path)) if os.path.exists(peaks_path) else {}
+    peak = peaks.get("bf16_tflops", 1900.0)
+    line = {
+        "metric": PREFILL_METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(total_ms / K, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) K/V/q, shuffled physical blocks)",
+        "config": {"workload": args.workload, "num_seqs": case.num_seqs, "num_heads": case.num_heads,
+                   "num_kv_heads": case.num_kv_heads, "head_dim": case.head_dim,
+                   "block_size": case.block_size, "chunk_tokens": int(case.query_start[-1]),
+                   "context_tokens": int(case.context_lens.sum()),
+                   "l2": "flushed between steps: 256 MiB written then read back, outside the timed events",
+                   "parallelism": f"{world} independent replica(s), one per GPU"},
+        "prefill_us": round(pf_ms * 1e3, 1),
+        "flops_per_step": flops,
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
+                     "peak_source": "measured" if "bf16_tflops" in peaks else "fallback",
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                     "kernel": "prefill_tc_kernel"},
+        "e2e": {"value": round(world * flops * Ke / (e2e_ms / 1e3) / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": 3 * 0 + (h_q.numel() + h_nk.numel() + h_nv.numel()) * 2,
+                "d2h_bytes_per_step": h_out.numel() * 2, "steps": Ke},
+        "clocks": sampler.summary(t0, t1), "gpu_launches": n1 - n0, "launches_per_step": (n1 - n0) / K,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = prefill_cpu_baseline(case)
+    return line
+
+
+def prefill_oracle_tflops(case, seqs, target_s):
+    """The oracle on the first rows of a few sequences' chunks, about target_s."""
+    import oracle
+    flops, t_used, rows_done = 0, 0.0, 0
+    for i in range(seqs):
+        q0 = int(case.query_start[i])
+        for rows in (1, 2, 4, 8, 16, 32, 64, 128):
+            sub = workloads.PrefillCase(**{**case.__dict__})
+            sub.num_seqs = 1
+            sub.block_tables = case.block_tables[i:i + 1]
+            n = int(case.query_start[i + 1] - case.query_start[i])
+            rows = min(rows, n)
+            # the first `rows` queries of the chunk: a chunk of `rows` at the same place
+            sub.context_lens = np.array([int(case.context_lens[i]) - n + rows], np.int32)
+            sub.query_start = np.array([0, rows], np.int32)
+            sub.q = case.q[q0:q0 + rows]
+            t = time.perf_counter()
+            oracle.paged_prefill(sub.q, case.k_cache, case.v_cache, sub.block_tables, sub.context_lens,
+                                 sub.query_start, case.scale, case.block_size, case.dtype, case.dtype)
+            dt = time.perf_counter() - t
+            flops += prefill_flops(sub)
+            t_used += dt
+            rows_done += rows
+            if t_used > target_s:
+                return flops / t_used / 1e12, rows_done, t_used
+    return flops / t_used / 1e12, rows_done, t_used
+
+
+def prefill_cpu_baseline(case):
+    value, rows, secs = prefill_oracle_tflops(case, case.num_seqs, 10.0)
+    return {"value": round(value, 6), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": f"fp64 numpy oracle pa_prefill on {rows} query rows (chunk starts of the batch's "
+                      f"sequences), {secs:.1f} s, 1 thread"}
+
+
+def run_prefill_reference(args, world, rank):
+    if rank != 0:
+        return None
+    case = workloads.prefill_llama8b(seed=rank_seed(1011, 0))
+    value, rows, secs = prefill_oracle_tflops(case, case.num_seqs, 2.0 * (args.steps + args.warmup) / 10)
+    return {"impl": "reference", "metric": PREFILL_METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * secs / max(1, args.steps + args.warmup), 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+            "data": "synthetic", "config": {"workload": args.workload, "sample_rows": rows},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                             "sample": f"fp64 numpy oracle on {rows} query rows, {secs:.1f} s, 1 thread"},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+# ----------------------------------------------------------------------------
 # beam search: fork + copy-on-write + decode
 
 
@@ -998,7 +1179,11 @@ def main():
     world, rank, local = setup_dist()
     swap = args.workload.startswith("swap")
     beam = args.workload.startswith("beam")
-    if args.impl == "reference":
+    prefill = args.workload.startswith("prefill")
+    if prefill:
+        line = (run_prefill_reference(args, world, rank) if args.impl == "reference"
+                else run_prefill(args, world, rank, local))
+    elif args.impl == "reference":
         if beam:
             line = run_beam_reference(args, world, rank)
         else:

@@ -9,9 +9,11 @@
 // (LLM 추론 확장, 품질·비용 절충 필수, the prefill / decode split), which makes
 // QK^T and PV dense tiles.
 //
-// One CTA of 4 warps per (query tile, KV head, sequence). A tile is 128 MMA
+// One CTA of 8 warps per (query tile, KV head, sequence). A tile is 128 MMA
 // rows: 128/G query tokens x the G query heads of the KV head, row r = token
-// r/G, head r%G. Thread r owns row r (TMEM lane r). Per 128-key tile:
+// r/G, head r%G. Row r (TMEM lane r) belongs to two threads, one per half of
+// the columns: warp w takes lanes 32(w%4)..+31 and columns 64(w/4)..+63 of
+// S and of O. Per 128-key tile:
 //   S = Q K^T   tcgen05.mma, M=128, N=128, K=128 (8 steps), Q and K tiles
 //               K-major with 128-byte swizzle, loaded by TMA (K block by block
 //               through the block table), S in TMEM columns 0..127;
@@ -35,14 +37,15 @@
 namespace pa {
 namespace {
 
-constexpr int kPfThreads = 128;
+constexpr int kSoftThreads = 256;               // 8 softmax warps
+constexpr int kPfThreads = kSoftThreads + 128;  // + 4 role warps: K loads, V loads, S issue, PV issue
 constexpr int kPfRows = 128;                   // MMA M
 constexpr int kPfKeys = 128;                   // keys per KV tile
 constexpr int kPfD = 128;                      // head dim
 constexpr int kHalf = kPfRows * 128;           // a 64-column half of a 128-row 16-bit tile
 constexpr int kTile = 2 * kHalf;               // 32 KiB
-constexpr int kSmemBytes = 1024 + 6 * kTile;   // Q, P, K[2], V[2] + alignment slack
-constexpr uint32_t kTmemCols = 256;            // S: 0..127, O: 128..255
+constexpr int kSmemBytes = 1024 + 7 * kTile;   // Q, P[2], K[2], V[2] + alignment slack
+constexpr uint32_t kTmemCols = 512;            // S[0], S[1]: 0..255, O: 256..383
 constexpr float kLazyRescale = 8.f;            // log2 units
 
 struct PfParams {
@@ -81,6 +84,25 @@ __device__ __forceinline__ uint32_t sw128_chunk(int r, int c) {
   return (c >> 3) * kHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4);
 }
 
+// A wait on an mbarrier that gives up after kWaitLimitNs, or as soon as
+// another thread of the CTA has given up (*abort set).
+__device__ __forceinline__ bool pf_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *abort = 1;
+      return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ void named_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
@@ -101,242 +123,295 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     if (ctx < n) return;
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r = threadIdx.x;  // this thread's row
 
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                        ~static_cast<uintptr_t>(1023));
+  // Q | P[2] | K[2] | V[2], 32 KiB each
   const uint32_t sQ = smem_u32(sm);
-  const uint32_t sP = sQ + kTile;
-  const uint32_t sK0 = sQ + 2 * kTile;  // K[stage] = sK0 + stage * kTile
-  const uint32_t sV0 = sQ + 4 * kTile;
-  unsigned char* const pP = sm + kTile;
-  unsigned char* const pV0 = sm + 4 * kTile;
-  __shared__ uint64_t bars[5];  // Q, KV[0], KV[1], S done, PV done
+  const uint32_t sP0 = sQ + kTile;
+  const uint32_t sK0 = sQ + 3 * kTile;
+  const uint32_t sV0 = sQ + 5 * kTile;
+  unsigned char* const pP0 = sm + kTile;
+  unsigned char* const pV0 = sm + 5 * kTile;
+  // full/free pairs per double buffer; arrival counts: 1 for TMA and tensor
+  // core completions, kSoftThreads for the softmax threads' signals
+  enum { kQ, kKFull, kVFull = kKFull + 2, kSFull = kVFull + 2, kOFull = kSFull + 2, kKFree = kOFull + 2,
+         kVFree = kKFree + 2, kSFree = kVFree + 2, kPFull = kSFree + 2, kNumBars = kPFull + 2 };
+  __shared__ uint64_t bars[kNumBars];
   __shared__ uint32_t tmem_slot;
-  const uint32_t bar_q = smem_u32(&bars[0]);
-  const uint32_t bar_kv0 = smem_u32(&bars[1]);
-  const uint32_t bar_s = smem_u32(&bars[3]);
-  const uint32_t bar_o = smem_u32(&bars[4]);
+  __shared__ int s_abort;
+  __shared__ float s_half[2][kPfRows];  // per row: each half's max, then its sum
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  volatile int* abort = &s_abort;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 5; ++i) mbar_init(smem_u32(&bars[i]), 1);
+    for (int i = 0; i < kNumBars; ++i) {
+      uint32_t count = 1;
+      if (i >= kSFree) count = kSoftThreads;       // softmax threads' signals
+      mbar_init(bar(i), count);
+    }
     mbar_init_fence();
+    s_abort = 0;
   }
   if (warp == 0) tmem_alloc(smem_u32(&tmem_slot), kTmemCols);
-  tc05_fence_before();
-  __syncthreads();
-  tc05_fence_after();
-  const uint32_t tmem = tmem_slot;
-  const uint32_t tmem_s = tmem, tmem_o = tmem + 128;
-  const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-
   // the keys this tile needs: 0 .. position of its last query
   const int t_last = min(t0 + TQ, n) - 1;
   const int pos_last = ctx - n + t_last;
   const int nkt = pos_last / kPfKeys + 1;
-  // this row's query position (rows past the chunk repeat the last position;
-  // they are not stored)
-  const int my_t = min(t0 + r / G, n - 1);
-  const int my_pos = ctx - n + my_t;
-
-  constexpr uint32_t kAB = std::is_same<T, bf16>::value ? 1u : 0u;
-  constexpr uint32_t idesc_s = mma_idesc_f16(kAB, 0, kPfRows, kPfKeys);
-  constexpr uint32_t idesc_o = mma_idesc_f16(kAB, 1, kPfRows, kPfD);
+  const int pos_first = ctx - n + t0;  // the tile's earliest query position
   const int blocks_per_tile = kPfKeys / bs;
+  const int32_t* trow0 = p.block_tables + static_cast<int64_t>(seq) * p.max_blocks_per_seq;
+  tc05_fence_before();
+  __syncthreads();
+  tc05_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const uint32_t tmem_o = tmem + 2 * kPfKeys;  // S[0], S[1]: columns 0..255; O: 256..383
 
-  // TMA loads of key tile kt into stage st (thread 0): every block of the
-  // tile that holds tokens of the context, both 64-column halves, K and V.
-  auto issue_kv = [&](int kt, int st) {
-    const uint32_t bar = bar_kv0 + st * 8;
-    const int lb0 = kt * blocks_per_tile;
-    int phys[kPfKeys / 8];
-    int nload = 0;
-    for (int j = 0; j < blocks_per_tile; ++j) {
-      phys[j] = -1;
-      const int lb = lb0 + j;
-      if (lb * bs >= ctx) continue;
-      const int b = p.block_tables[static_cast<int64_t>(seq) * p.max_blocks_per_seq + lb];
-      if (b < 0 || b >= p.num_blocks) {
-        flag_error(p.debug_err, PA_DEVERR_BLOCK_RANGE);
-        continue;
+  if (warp >= kSoftThreads / 32) {
+    // ====== one thread per role: K loads (+Q), V loads, S issue, PV issue ======
+    const int role = warp - kSoftThreads / 32;
+    if (role <= 1 && lane == 0) {
+      // role 0: Q once, then the K tiles; role 1: the V tiles. TMA, one
+      // 64-column box per block and half, into a double buffer refilled when
+      // the product that read it is complete. A tile's table entries are
+      // read (all loads in flight) before waiting for its buffer.
+      const bool is_k = role == 0;
+      const CUtensorMap* map = is_k ? &tmap_k : &tmap_v;
+      const uint32_t dst0 = is_k ? sK0 : sV0;
+      const int full = is_k ? kKFull : kVFull, freed = is_k ? kKFree : kVFree;
+      if (is_k) {
+        mbar_arrive_expect_tx(bar(kQ), 2u * kHalf);
+        for (int h = 0; h < 2; ++h) tma_load_3d(sQ + h * kHalf, &tmap_q, h * 64, kvh * G, q0 + t0, bar(kQ));
       }
-      phys[j] = b;
-      ++nload;
-    }
-    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nload) * 4u * bs * 128u);
-    for (int j = 0; j < blocks_per_tile; ++j) {
-      if (phys[j] < 0) continue;
-      const int z = phys[j] * p.num_kv_heads + kvh;
-      for (int h = 0; h < 2; ++h) {
-        const uint32_t off = st * kTile + h * kHalf + j * bs * 128;
-        tma_load_3d(sK0 + off, &tmap_k, h * 64, 0, z, bar);
-        tma_load_3d(sV0 + off, &tmap_v, h * 64, 0, z, bar);
+      for (int kt = 0; kt < nkt; ++kt) {
+        const int b = kt & 1;
+        const int lb0 = kt * blocks_per_tile;
+        int ent[kPfKeys / 8];
+        bool use[kPfKeys / 8];
+#pragma unroll
+        for (int j = 0; j < kPfKeys / 8; ++j) {
+          use[j] = j < blocks_per_tile && (lb0 + j) * bs < ctx;
+          ent[j] = use[j] ? __ldg(trow0 + lb0 + j) : 0;
+        }
+        uint32_t nload = 0;
+#pragma unroll
+        for (int j = 0; j < kPfKeys / 8; ++j) {
+          if (use[j] && (ent[j] < 0 || ent[j] >= p.num_blocks)) {
+            flag_error(p.debug_err, PA_DEVERR_BLOCK_RANGE);
+            use[j] = false;
+          }
+          nload += use[j] ? 1u : 0u;
+        }
+        if (kt >= 2 && !pf_wait(bar(freed + b), ((kt - 2) >> 1) & 1, abort)) break;
+        mbar_arrive_expect_tx(bar(full + b), nload * 2u * bs * 128u);
+#pragma unroll
+        for (int j = 0; j < kPfKeys / 8; ++j) {
+          if (!use[j]) continue;
+          const int z = ent[j] * p.num_kv_heads + kvh;
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            tma_load_3d(dst0 + b * kTile + h * kHalf + j * bs * 128, map, h * 64, 0, z, bar(full + b));
+        }
       }
-    }
-  };
-
-  if (threadIdx.x == 0) {
-    mbar_arrive_expect_tx(bar_q, 2u * kHalf);
-    for (int h = 0; h < 2; ++h) tma_load_3d(sQ + h * kHalf, &tmap_q, h * 64, kvh * G, q0 + t0, bar_q);
-    issue_kv(0, 0);
-    if (nkt > 1) issue_kv(1, 1);
-  }
-
-  float m_run = -INFINITY, l_run = 0.f;
-  bool ok = true, aborted = false;
-  for (int kt = 0; kt < nkt; ++kt) {
-    const int st = kt & 1;
-    const uint32_t kv_parity = (kt >> 1) & 1;
-    // ---- S = Q K^T ----
-    if (threadIdx.x == 0) {
-      ok = (kt > 0 || mbar_wait_bounded(bar_q, 0)) && mbar_wait_bounded(bar_kv0 + st * 8, kv_parity);
-      if (ok) {
+    } else if (lane == 0 && role == 2) {
+      // S[b] = Q K[b]^T once K arrived and the softmax two tiles back has read S[b]
+      constexpr uint32_t kAB = std::is_same<T, bf16>::value ? 1u : 0u;
+      constexpr uint32_t idesc_s = mma_idesc_f16(kAB, 0, kPfRows, kPfKeys);
+      bool go = pf_wait(bar(kQ), 0, abort);
+      for (int kt = 0; go && kt < nkt; ++kt) {
+        const int b = kt & 1;
+        go = pf_wait(bar(kKFull + b), (kt >> 1) & 1, abort) &&
+             (kt < 2 || pf_wait(bar(kSFree + b), ((kt - 2) >> 1) & 1, abort));
+        if (!go) break;
         tc05_fence_after();
 #pragma unroll
         for (int k = 0; k < kPfD / 16; ++k) {
           const uint32_t koff = (k >> 2) * kHalf + (k & 3) * 32;
-          tc05_mma_ss(tmem_s, smem_desc_sw128(sQ + koff, 16, 1024),
-                      smem_desc_sw128(sK0 + st * kTile + koff, 16, 1024), idesc_s, k > 0);
+          tc05_mma_ss(tmem + b * kPfKeys, smem_desc_sw128(sQ + koff, 16, 1024),
+                      smem_desc_sw128(sK0 + b * kTile + koff, 16, 1024), idesc_s, k > 0);
         }
-        tc05_commit(bar_s);
+        tc05_commit(bar(kSFull + b));
+        tc05_commit(bar(kKFree + b));
       }
-    }
-    ok = mbar_wait_bounded(bar_s, kt & 1) && mbar_wait_bounded(bar_kv0 + st * 8, kv_parity);
-    if (__syncthreads_or(!ok)) {
-      aborted = true;
-      break;
-    }
-    tc05_fence_after();
-
-    // ---- softmax of this thread's row ----
-    float s[kPfKeys];
+    } else if (lane == 0 && role == 3) {
+      // O += P[b] V[b] once the softmax wrote P[b] and V arrived
+      constexpr uint32_t kAB = std::is_same<T, bf16>::value ? 1u : 0u;
+      constexpr uint32_t idesc_o = mma_idesc_f16(kAB, 1, kPfRows, kPfD);
+      for (int kt = 0; kt < nkt; ++kt) {
+        const int b = kt & 1;
+        const uint32_t par = (kt >> 1) & 1;
+        if (!pf_wait(bar(kPFull + b), par, abort) || !pf_wait(bar(kVFull + b), par, abort)) break;
+        tc05_fence_after();
 #pragma unroll
-    for (int c = 0; c < kPfKeys; c += 32) {
-      uint32_t v[32];
-      tmem_ld32(tmem_s + lane_base + c, v);
-      tmem_wait_ld();
-#pragma unroll
-      for (int j = 0; j < 32; ++j) s[c + j] = __uint_as_float(v[j]);
-    }
-    const int key0 = kt * kPfKeys;
-    float mx = -INFINITY;
-#pragma unroll
-    for (int c = 0; c < kPfKeys; ++c) {
-      s[c] = key0 + c <= my_pos ? s[c] * p.scale_log2 : -INFINITY;
-      mx = fmaxf(mx, s[c]);
-    }
-    float m_use = m_run, alpha = 1.f;
-    if (mx > m_run + kLazyRescale || m_run == -INFINITY) {
-      m_use = fmaxf(m_run, mx);
-      alpha = m_run == -INFINITY ? 0.f : exp2f(m_run - m_use);
-    }
-    const float base = m_use == -INFINITY ? 0.f : m_use;
-    float sum = 0.f;
-#pragma unroll
-    for (int c = 0; c < kPfKeys; ++c) {
-      s[c] = exp2f(s[c] - base);
-      sum += s[c];
-    }
-    l_run = l_run * alpha + sum;
-    m_run = m_use;
-
-    // the previous PV product is complete: P, O and the other K/V buffer are free
-    if (kt > 0) {
-      ok = mbar_wait_bounded(bar_o, (kt - 1) & 1);
-      if (__syncthreads_or(!ok)) {
-        aborted = true;
-        break;
-      }
-      tc05_fence_after();
-      if (threadIdx.x == 0 && kt + 1 < nkt) issue_kv(kt + 1, (kt + 1) & 1);
-      // rescale O where this row's max moved (warps with no such row skip)
-      if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-        for (int c = 0; c < kPfD; c += 32) {
-          uint32_t v[32];
-          tmem_ld32(tmem_o + lane_base + c, v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
-          tmem_st32(tmem_o + lane_base + c, v);
+        for (int k = 0; k < kPfKeys / 16; ++k) {
+          tc05_mma_ss(tmem_o, smem_desc_sw128(sP0 + b * kTile + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024),
+                      smem_desc_sw128(sV0 + b * kTile + k * 16 * 128, kHalf, 1024), idesc_o,
+                      (kt > 0 || k > 0) ? 1u : 0u);
         }
-        tmem_wait_st();
-      }
-    }
-    // keys past the context in the last tile: zero their V rows (stale or
-    // unwritten shared memory must not meet a zero weight as NaN)
-    const int valid = ctx - key0;
-    if (valid < kPfKeys) {
-      unsigned char* vt = pV0 + st * kTile;
-      for (int i = threadIdx.x; i < (kPfKeys - valid) * 16; i += kPfThreads) {
-        const int row = valid + i / 16, chunk = i % 16;
-        *reinterpret_cast<uint4*>(vt + (chunk >> 3) * kHalf + row * 128 + (((chunk & 7) ^ (row & 7)) << 4)) =
-            make_uint4(0u, 0u, 0u, 0u);
-      }
-    }
-    // P in the K-major swizzled layout of the PV product's A operand
-#pragma unroll
-    for (int c = 0; c < kPfKeys; c += 8) {
-      uint4 w;
-      w.x = pack2<T>(s[c], s[c + 1]);
-      w.y = pack2<T>(s[c + 2], s[c + 3]);
-      w.z = pack2<T>(s[c + 4], s[c + 5]);
-      w.w = pack2<T>(s[c + 6], s[c + 7]);
-      *reinterpret_cast<uint4*>(pP + sw128_chunk(r, c >> 3)) = w;
-    }
-    fence_proxy_async_smem();
-    tc05_fence_before();
-    __syncthreads();
-
-    // ---- O += P V ----
-    if (threadIdx.x == 0) {
-      tc05_fence_after();
-#pragma unroll
-      for (int k = 0; k < kPfKeys / 16; ++k) {
-        tc05_mma_ss(tmem_o, smem_desc_sw128(sP + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024),
-                    smem_desc_sw128(sV0 + st * kTile + k * 16 * 128, kHalf, 1024), idesc_o,
-                    (kt > 0 || k > 0) ? 1u : 0u);
-      }
-      tc05_commit(bar_o);
-    }
-  }
-
-  if (!aborted) aborted = __syncthreads_or(!mbar_wait_bounded(bar_o, (nkt - 1) & 1));
-  if (!aborted) {
-    tc05_fence_after();
-    // ---- out = O / l for the rows of the chunk ----
-    const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-    const int tok = t0 + r / G;
-    T* orow = static_cast<T*>(p.out) +
-              (static_cast<int64_t>(q0 + min(tok, n - 1)) * p.num_heads + kvh * G + r % G) * kPfD;
-#pragma unroll
-    for (int c = 0; c < kPfD; c += 32) {
-      uint32_t v[32];
-      tmem_ld32(tmem_o + lane_base + c, v);
-      tmem_wait_ld();
-      if (tok < n) {
-#pragma unroll
-        for (int j = 0; j < 32; j += 8) {
-          uint4 w;
-          w.x = pack2<T>(__uint_as_float(v[j]) * inv, __uint_as_float(v[j + 1]) * inv);
-          w.y = pack2<T>(__uint_as_float(v[j + 2]) * inv, __uint_as_float(v[j + 3]) * inv);
-          w.z = pack2<T>(__uint_as_float(v[j + 4]) * inv, __uint_as_float(v[j + 5]) * inv);
-          w.w = pack2<T>(__uint_as_float(v[j + 6]) * inv, __uint_as_float(v[j + 7]) * inv);
-          *reinterpret_cast<uint4*>(orow + c + j) = w;
-        }
+        tc05_commit(bar(kOFull + b));
+        tc05_commit(bar(kVFree + b));
       }
     }
   } else {
+    // ================= softmax: 8 warps, two threads per row =================
+    const int r = (warp & 3) * 32 + lane;  // this thread's row
+    const int hc = warp >> 2;              // its half of the columns
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int c0 = hc * (kPfKeys / 2);  // first S column (key) of this thread
+    const int d0 = hc * (kPfD / 2);     // first O column of this thread
+    // this row's query position (rows past the chunk repeat the last
+    // position; they are not stored)
+    const int my_t = min(t0 + r / G, n - 1);
+    const int my_pos = ctx - n + my_t;
+    constexpr int kH = kPfKeys / 2;
+    float m_run = -INFINITY, l_run = 0.f;
+    // Every softmax thread runs all nkt iterations and every named barrier,
+    // also after a timeout (then it skips the work), so that no thread waits
+    // at a barrier for one that left; `ok` is kept warp-uniform for the
+    // warp-collective TMEM accesses.
+    bool ok = true;
+    for (int kt = 0; kt < nkt; ++kt) {
+      const int b = kt & 1;
+      const uint32_t par = (kt >> 1) & 1;
+      ok = __all_sync(0xffffffffu, ok && pf_wait(bar(kSFull + b), par, abort));
+      float sv[kH];
+      if (ok) {
+        tc05_fence_after();
+#pragma unroll
+        for (int c = 0; c < kH; c += 32) {
+          uint32_t v[32];
+          tmem_ld32(tmem + b * kPfKeys + lane_base + c0 + c, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) sv[c + j] = __uint_as_float(v[j]);
+        }
+        tc05_fence_before();
+        mbar_arrive(bar(kSFree + b));  // S[b] is read: the next S may go there
+      } else {
+#pragma unroll
+        for (int c = 0; c < kH; ++c) sv[c] = 0.f;
+      }
+      const int key0 = kt * kPfKeys;
+      // only tiles that reach past the tile's earliest query need the causal mask
+      if (key0 + kPfKeys - 1 > pos_first) {
+#pragma unroll
+        for (int c = 0; c < kH; ++c)
+          if (key0 + c0 + c > my_pos) sv[c] = -INFINITY;
+      }
+      float mraw = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kH; ++c) mraw = fmaxf(mraw, sv[c]);
+      s_half[hc][r] = mraw;
+      named_sync(1, kSoftThreads);
+      const float mx = fmaxf(s_half[0][r], s_half[1][r]) * p.scale_log2;  // scale > 0
+      float m_use = m_run, alpha = 1.f;
+      if (mx > m_run + kLazyRescale || m_run == -INFINITY) {
+        m_use = fmaxf(m_run, mx);
+        alpha = m_run == -INFINITY ? 0.f : exp2f(m_run - m_use);
+      }
+      const float base = m_use == -INFINITY ? 0.f : m_use;
+      float sum = 0.f;
+#pragma unroll
+      for (int c = 0; c < kH; ++c) {
+        sv[c] = exp2f(fmaf(sv[c], p.scale_log2, -base));
+        sum += sv[c];
+      }
+      l_run = l_run * alpha + sum;  // this half's share of the row sum
+      m_run = m_use;
+      // O may be rescaled only once the previous PV product is complete;
+      // P[b] is free once the PV product two tiles back is
+      const bool rescale = kt > 0 && __any_sync(0xffffffffu, alpha != 1.f);
+      if (rescale) ok = __all_sync(0xffffffffu, ok && pf_wait(bar(kOFull + (b ^ 1)), ((kt - 1) >> 1) & 1, abort));
+      if (kt >= 2) ok = __all_sync(0xffffffffu, ok && pf_wait(bar(kOFull + b), ((kt - 2) >> 1) & 1, abort));
+      if (ok && rescale) {
+        tc05_fence_after();
+#pragma unroll
+        for (int c = 0; c < kPfD / 2; c += 32) {
+          uint32_t v[32];
+          tmem_ld32(tmem_o + lane_base + d0 + c, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
+          tmem_st32(tmem_o + lane_base + d0 + c, v);
+        }
+        tmem_wait_st();
+        tc05_fence_before();
+      }
+      // keys past the context in the last tile: zero their V rows (stale or
+      // unwritten shared memory must not meet a zero weight as NaN)
+      const int valid = ctx - key0;
+      if (valid < kPfKeys) {
+        ok = ok && pf_wait(bar(kVFull + b), par, abort);
+        unsigned char* vt = pV0 + b * kTile;
+        const int tid = hc * kPfRows + r;
+        for (int i = tid; ok && i < (kPfKeys - valid) * 16; i += kSoftThreads) {
+          const int row = valid + i / 16, chunk = i % 16;
+          *reinterpret_cast<uint4*>(vt + (chunk >> 3) * kHalf + row * 128 + (((chunk & 7) ^ (row & 7)) << 4)) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      if (ok) {
+        // P in the K-major swizzled layout of the PV product's A operand (this
+        // thread's 64 keys are one half of the tile)
+        unsigned char* pp = pP0 + b * kTile;
+#pragma unroll
+        for (int c = 0; c < kH; c += 8) {
+          uint4 w;
+          w.x = pack2<T>(sv[c], sv[c + 1]);
+          w.y = pack2<T>(sv[c + 2], sv[c + 3]);
+          w.z = pack2<T>(sv[c + 4], sv[c + 5]);
+          w.w = pack2<T>(sv[c + 6], sv[c + 7]);
+          *reinterpret_cast<uint4*>(pp + sw128_chunk(r, (c0 + c) >> 3)) = w;
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bar(kPFull + b));
+      }
+    }
+    ok = __all_sync(0xffffffffu, ok && pf_wait(bar(kOFull + ((nkt - 1) & 1)), ((nkt - 1) >> 1) & 1, abort));
+    // ---- out = O / l for the rows of the chunk ----
+    s_half[hc][r] = l_run;
+    named_sync(1, kSoftThreads);
+    if (ok) {
+      tc05_fence_after();
+      const float l = s_half[0][r] + s_half[1][r];
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const int tok = t0 + r / G;
+      T* orow = static_cast<T*>(p.out) +
+                (static_cast<int64_t>(q0 + min(tok, n - 1)) * p.num_heads + kvh * G + r % G) * kPfD + d0;
+#pragma unroll
+      for (int c = 0; c < kPfD / 2; c += 32) {
+        uint32_t v[32];
+        tmem_ld32(tmem_o + lane_base + d0 + c, v);
+        tmem_wait_ld();
+        if (tok < n) {
+#pragma unroll
+          for (int j = 0; j < 32; j += 8) {
+            uint4 w;
+            w.x = pack2<T>(__uint_as_float(v[j]) * inv, __uint_as_float(v[j + 1]) * inv);
+            w.y = pack2<T>(__uint_as_float(v[j + 2]) * inv, __uint_as_float(v[j + 3]) * inv);
+            w.z = pack2<T>(__uint_as_float(v[j + 4]) * inv, __uint_as_float(v[j + 5]) * inv);
+            w.w = pack2<T>(__uint_as_float(v[j + 6]) * inv, __uint_as_float(v[j + 7]) * inv);
+            *reinterpret_cast<uint4*>(orow + c + j) = w;
+          }
+        }
+      }
+    }
+  }
+
+  tc05_fence_before();
+  __syncthreads();
+  if (s_abort) {
     if (threadIdx.x == 0) {
       flag_error(p.debug_err, PA_DEVERR_TIMEOUT);
       // let tensor-core work already issued finish before its TMEM goes away
-      mbar_wait_bounded(bar_s, 0, 10000000ull);
-      mbar_wait_bounded(bar_o, 0, 10000000ull);
+      for (int i = 0; i < 2; ++i) {
+        mbar_wait_bounded(bar(kSFull + i), 0, 10000000ull);
+        mbar_wait_bounded(bar(kOFull + i), 0, 10000000ull);
+      }
     }
+    __syncthreads();
   }
-  tc05_fence_before();
-  __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 

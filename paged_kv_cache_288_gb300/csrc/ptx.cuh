@@ -58,6 +58,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
 // Waits for the phase with the given parity to complete; false after
 // `limit_ns` without completion.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,

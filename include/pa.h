@@ -62,6 +62,7 @@ typedef enum {
 #define PA_DEVERR_BLOCK_RANGE 0x2   /* table entry or copy pair outside [0, num_blocks) */
 #define PA_DEVERR_CONTEXT_RANGE 0x4 /* context length above max_context_len or the table width */
 #define PA_DEVERR_TIMEOUT 0x8       /* a kernel gave up waiting for its own data copies (1 s) */
+#define PA_DEVERR_LAYOUT 0x10       /* a kernel found its shared memory misaligned; nothing computed */
 
 /* Library version, major*10000 + minor*100 + patch. */
 int pa_version(void);

@@ -17,6 +17,7 @@ DEVERR_SLOT_RANGE = 0x1
 DEVERR_BLOCK_RANGE = 0x2
 DEVERR_CONTEXT_RANGE = 0x4
 DEVERR_TIMEOUT = 0x8
+DEVERR_LAYOUT = 0x10
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libpa.so")

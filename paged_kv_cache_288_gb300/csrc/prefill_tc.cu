@@ -37,15 +37,18 @@
 namespace pa {
 namespace {
 
-constexpr int kSoftThreads = 256;               // 8 softmax warps
+constexpr int kGroups = 2;                      // query tiles per CTA (they share the K/V tiles)
+constexpr int kRowsPerGroup = 128;              // rows of a query tile
+constexpr int kGroupThreads = 2 * kRowsPerGroup;        // two softmax threads per row
+constexpr int kSoftThreads = kGroups * kGroupThreads;   // 16 softmax warps
 constexpr int kPfThreads = kSoftThreads + 128;  // + 4 role warps: K loads, V loads, S issue, PV issue
 constexpr int kPfRows = 128;                   // MMA M
 constexpr int kPfKeys = 128;                   // keys per KV tile
 constexpr int kPfD = 128;                      // head dim
 constexpr int kHalf = kPfRows * 128;           // a 64-column half of a 128-row 16-bit tile
 constexpr int kTile = 2 * kHalf;               // 32 KiB
-constexpr int kSmemBytes = 1024 + 7 * kTile;   // Q, P[2], K[2], V[2] + alignment slack
-constexpr uint32_t kTmemCols = 512;            // S[0], S[1]: 0..255, O: 256..383
+constexpr int kSmemBytes = 7 * kTile + 3072;   // Q[2], P[2], K, V[2]; barriers; row exchange (2 KiB)
+constexpr uint32_t kTmemCols = 512;            // per group: S (128 columns), O (128 columns)
 constexpr float kLazyRescale = 8.f;            // log2 units
 
 struct PfParams {
@@ -107,12 +110,12 @@ template <typename T>
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                       const __grid_constant__ CUtensorMap tmap_v, const PfParams p) {
-  const int tile = blockIdx.x, kvh = blockIdx.y, seq = blockIdx.z;
+  const int pair = blockIdx.x, kvh = blockIdx.y, seq = blockIdx.z;
   const int q0 = p.query_start[seq];
   const int n = p.query_start[seq + 1] - q0;
   const int G = p.group, TQ = p.tokens_per_tile;
-  const int t0 = tile * TQ;
-  if (t0 >= n) return;  // CTA-uniform, before any TMEM is held
+  const int t0 = pair * kGroups * TQ;  // first query of the CTA's two tiles
+  if (t0 >= n) return;                 // CTA-uniform, before any TMEM is held
   const int bs = p.block_size;
   int ctx = p.context_lens[seq];
   const int cap = p.max_blocks_per_seq * bs;
@@ -124,265 +127,284 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  extern __shared__ unsigned char smem_raw[];
-  unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                       ~static_cast<uintptr_t>(1023));
-  // Q | P[2] | K[2] | V[2], 32 KiB each
-  const uint32_t sQ = smem_u32(sm);
-  const uint32_t sP0 = sQ + kTile;
-  const uint32_t sK0 = sQ + 3 * kTile;
-  const uint32_t sV0 = sQ + 5 * kTile;
-  unsigned char* const pP0 = sm + kTile;
+  // All shared memory is dynamic (no static __shared__ variables), so its
+  // base is the start of the CTA's shared window, which is 1024-aligned as
+  // the 128-byte swizzle needs; the kernel checks rather than assumes it.
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) flag_error(p.debug_err, PA_DEVERR_LAYOUT);
+    return;
+  }
+  unsigned char* sm = smem_raw;
+  // Q[2] | P[2] | K | V[2], 32 KiB each (Q[g], P[g]: query tile g of the CTA),
+  // then the barriers and the row exchange
+  const uint32_t sQ0 = smem_u32(sm);
+  const uint32_t sP0 = sQ0 + 2 * kTile;
+  const uint32_t sK = sQ0 + 4 * kTile;
+  const uint32_t sV0 = sQ0 + 5 * kTile;
+  unsigned char* const pP0 = sm + 2 * kTile;
   unsigned char* const pV0 = sm + 5 * kTile;
-  // full/free pairs per double buffer; arrival counts: 1 for TMA and tensor
-  // core completions, kSoftThreads for the softmax threads' signals
-  enum { kQ, kKFull, kVFull = kKFull + 2, kSFull = kVFull + 2, kOFull = kSFull + 2, kKFree = kOFull + 2,
-         kVFree = kKFree + 2, kSFree = kVFree + 2, kPFull = kSFree + 2, kNumBars = kPFull + 2 };
-  __shared__ uint64_t bars[kNumBars];
-  __shared__ uint32_t tmem_slot;
-  __shared__ int s_abort;
-  __shared__ float s_half[2][kPfRows];  // per row: each half's max, then its sum
+  // barrier counts: 1 for TMA and tensor-core completions, 128 for one
+  // softmax group's threads
+  enum { kQ, kKFull, kKFree, kVFull, kVFree = kVFull + 2, kSFull = kVFree + 2, kOFull = kSFull + 2,
+         kSFree = kOFull + 2, kPFull = kSFree + 2, kNumBars = kPFull + 2 };
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + 7 * kTile);
+  uint32_t& tmem_slot = *reinterpret_cast<uint32_t*>(sm + 7 * kTile + 256);
+  int& s_abort = *reinterpret_cast<int*>(sm + 7 * kTile + 260);
+  // per row: each half's max, then its sum
+  float (*s_half)[2][kRowsPerGroup] = reinterpret_cast<float (*)[2][kRowsPerGroup]>(sm + 7 * kTile + 1024);
+  static_assert(kNumBars * 8 <= 256, "barriers fit their slot");
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   volatile int* abort = &s_abort;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kNumBars; ++i) {
-      uint32_t count = 1;
-      if (i >= kSFree) count = kSoftThreads;       // softmax threads' signals
-      mbar_init(bar(i), count);
-    }
+    for (int i = 0; i < kNumBars; ++i) mbar_init(bar(i), i >= kSFree ? static_cast<uint32_t>(kGroupThreads) : 1u);
     mbar_init_fence();
     s_abort = 0;
   }
   if (warp == 0) tmem_alloc(smem_u32(&tmem_slot), kTmemCols);
-  // the keys this tile needs: 0 .. position of its last query
-  const int t_last = min(t0 + TQ, n) - 1;
-  const int pos_last = ctx - n + t_last;
-  const int nkt = pos_last / kPfKeys + 1;
-  const int pos_first = ctx - n + t0;  // the tile's earliest query position
-  const int blocks_per_tile = kPfKeys / bs;
-  const int32_t* trow0 = p.block_tables + static_cast<int64_t>(seq) * p.max_blocks_per_seq;
   tc05_fence_before();
   __syncthreads();
   tc05_fence_after();
-  const uint32_t tmem = tmem_slot;
-  const uint32_t tmem_o = tmem + 2 * kPfKeys;  // S[0], S[1]: columns 0..255; O: 256..383
+  const uint32_t tmem = tmem_slot;  // group g: S at columns 256g .. +127, O at 256g + 128 .. +127
 
+  // the keys the CTA needs: 0 .. position of its last query
+  const int t_last = min(t0 + kGroups * TQ, n) - 1;
+  const int pos_last = ctx - n + t_last;
+  const int nkt = pos_last / kPfKeys + 1;
+  const int blocks_per_tile = kPfKeys / bs;
+  const int32_t* trow0 = p.block_tables + static_cast<int64_t>(seq) * p.max_blocks_per_seq;
+
+  // TMA of one K or V tile (thread): one 64-column box per block and half;
+  // the table entries are read (all loads in flight) before the buffer wait
+  auto load_tile = [&](const CUtensorMap* map, uint32_t dst, uint32_t full, uint32_t freed, uint32_t free_par,
+                       bool wait_free, int kt) -> bool {
+    const int lb0 = kt * blocks_per_tile;
+    int ent[kPfKeys / 8];
+    bool use[kPfKeys / 8];
+#pragma unroll
+    for (int j = 0; j < kPfKeys / 8; ++j) {
+      use[j] = j < blocks_per_tile && (lb0 + j) * bs < ctx;
+      ent[j] = use[j] ? __ldg(trow0 + lb0 + j) : 0;
+    }
+    uint32_t nload = 0;
+#pragma unroll
+    for (int j = 0; j < kPfKeys / 8; ++j) {
+      if (use[j] && (ent[j] < 0 || ent[j] >= p.num_blocks)) {
+        flag_error(p.debug_err, PA_DEVERR_BLOCK_RANGE);
+        use[j] = false;
+      }
+      nload += use[j] ? 1u : 0u;
+    }
+    if (wait_free && !pf_wait(freed, free_par, abort)) return false;
+    mbar_arrive_expect_tx(full, nload * 2u * bs * 128u);
+#pragma unroll
+    for (int j = 0; j < kPfKeys / 8; ++j) {
+      if (!use[j]) continue;
+      const int z = ent[j] * p.num_kv_heads + kvh;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) tma_load_3d(dst + h * kHalf + j * bs * 128, map, h * 64, 0, z, full);
+    }
+    return true;
+  };
+
+  constexpr uint32_t kAB = std::is_same<T, bf16>::value ? 1u : 0u;
   if (warp >= kSoftThreads / 32) {
     // ====== one thread per role: K loads (+Q), V loads, S issue, PV issue ======
     const int role = warp - kSoftThreads / 32;
-    if (role <= 1 && lane == 0) {
-      // role 0: Q once, then the K tiles; role 1: the V tiles. TMA, one
-      // 64-column box per block and half, into a double buffer refilled when
-      // the product that read it is complete. A tile's table entries are
-      // read (all loads in flight) before waiting for its buffer.
-      const bool is_k = role == 0;
-      const CUtensorMap* map = is_k ? &tmap_k : &tmap_v;
-      const uint32_t dst0 = is_k ? sK0 : sV0;
-      const int full = is_k ? kKFull : kVFull, freed = is_k ? kKFree : kVFree;
-      if (is_k) {
-        mbar_arrive_expect_tx(bar(kQ), 2u * kHalf);
-        for (int h = 0; h < 2; ++h) tma_load_3d(sQ + h * kHalf, &tmap_q, h * 64, kvh * G, q0 + t0, bar(kQ));
-      }
+    if (lane == 0 && role == 0) {
+      // Q of both tiles, then the K tiles into the single K buffer, each
+      // once both S products of the tile before have read it
+      mbar_arrive_expect_tx(bar(kQ), 4u * kHalf);
+      for (int g = 0; g < kGroups; ++g)
+        for (int h = 0; h < 2; ++h)
+          tma_load_3d(sQ0 + g * kTile + h * kHalf, &tmap_q, h * 64, kvh * G, q0 + t0 + g * TQ, bar(kQ));
+      for (int kt = 0; kt < nkt; ++kt)
+        if (!load_tile(&tmap_k, sK, bar(kKFull), bar(kKFree), (kt - 1) & 1, kt >= 1, kt)) break;
+    } else if (lane == 0 && role == 1) {
+      // the V tiles into a double buffer, refilled once both PV products of
+      // the tile two back have read it
       for (int kt = 0; kt < nkt; ++kt) {
         const int b = kt & 1;
-        const int lb0 = kt * blocks_per_tile;
-        int ent[kPfKeys / 8];
-        bool use[kPfKeys / 8];
-#pragma unroll
-        for (int j = 0; j < kPfKeys / 8; ++j) {
-          use[j] = j < blocks_per_tile && (lb0 + j) * bs < ctx;
-          ent[j] = use[j] ? __ldg(trow0 + lb0 + j) : 0;
-        }
-        uint32_t nload = 0;
-#pragma unroll
-        for (int j = 0; j < kPfKeys / 8; ++j) {
-          if (use[j] && (ent[j] < 0 || ent[j] >= p.num_blocks)) {
-            flag_error(p.debug_err, PA_DEVERR_BLOCK_RANGE);
-            use[j] = false;
-          }
-          nload += use[j] ? 1u : 0u;
-        }
-        if (kt >= 2 && !pf_wait(bar(freed + b), ((kt - 2) >> 1) & 1, abort)) break;
-        mbar_arrive_expect_tx(bar(full + b), nload * 2u * bs * 128u);
-#pragma unroll
-        for (int j = 0; j < kPfKeys / 8; ++j) {
-          if (!use[j]) continue;
-          const int z = ent[j] * p.num_kv_heads + kvh;
-#pragma unroll
-          for (int h = 0; h < 2; ++h)
-            tma_load_3d(dst0 + b * kTile + h * kHalf + j * bs * 128, map, h * 64, 0, z, bar(full + b));
-        }
+        if (!load_tile(&tmap_v, sV0 + b * kTile, bar(kVFull + b), bar(kVFree + b), ((kt - 2) >> 1) & 1, kt >= 2,
+                       kt))
+          break;
       }
     } else if (lane == 0 && role == 2) {
-      // S[b] = Q K[b]^T once K arrived and the softmax two tiles back has read S[b]
-      constexpr uint32_t kAB = std::is_same<T, bf16>::value ? 1u : 0u;
+      // S[g] = Q[g] K^T for both groups once K arrived and the group has read
+      // its previous S
       constexpr uint32_t idesc_s = mma_idesc_f16(kAB, 0, kPfRows, kPfKeys);
       bool go = pf_wait(bar(kQ), 0, abort);
       for (int kt = 0; go && kt < nkt; ++kt) {
-        const int b = kt & 1;
-        go = pf_wait(bar(kKFull + b), (kt >> 1) & 1, abort) &&
-             (kt < 2 || pf_wait(bar(kSFree + b), ((kt - 2) >> 1) & 1, abort));
-        if (!go) break;
-        tc05_fence_after();
+        go = pf_wait(bar(kKFull), kt & 1, abort);
+        for (int g = 0; go && g < kGroups; ++g) {
+          if (kt >= 1 && !(go = pf_wait(bar(kSFree + g), (kt - 1) & 1, abort))) break;
+          tc05_fence_after();
 #pragma unroll
-        for (int k = 0; k < kPfD / 16; ++k) {
-          const uint32_t koff = (k >> 2) * kHalf + (k & 3) * 32;
-          tc05_mma_ss(tmem + b * kPfKeys, smem_desc_sw128(sQ + koff, 16, 1024),
-                      smem_desc_sw128(sK0 + b * kTile + koff, 16, 1024), idesc_s, k > 0);
+          for (int k = 0; k < kPfD / 16; ++k) {
+            const uint32_t koff = (k >> 2) * kHalf + (k & 3) * 32;
+            tc05_mma_ss(tmem + g * 256, smem_desc_sw128(sQ0 + g * kTile + koff, 16, 1024),
+                        smem_desc_sw128(sK + koff, 16, 1024), idesc_s, k > 0);
+          }
+          tc05_commit(bar(kSFull + g));
         }
-        tc05_commit(bar(kSFull + b));
-        tc05_commit(bar(kKFree + b));
+        if (go) tc05_commit(bar(kKFree));
       }
     } else if (lane == 0 && role == 3) {
-      // O += P[b] V[b] once the softmax wrote P[b] and V arrived
-      constexpr uint32_t kAB = std::is_same<T, bf16>::value ? 1u : 0u;
+      // O[g] += P[g] V for both groups once V arrived and the group wrote P
       constexpr uint32_t idesc_o = mma_idesc_f16(kAB, 1, kPfRows, kPfD);
-      for (int kt = 0; kt < nkt; ++kt) {
+      bool go = true;
+      for (int kt = 0; go && kt < nkt; ++kt) {
         const int b = kt & 1;
-        const uint32_t par = (kt >> 1) & 1;
-        if (!pf_wait(bar(kPFull + b), par, abort) || !pf_wait(bar(kVFull + b), par, abort)) break;
-        tc05_fence_after();
+        go = pf_wait(bar(kVFull + b), (kt >> 1) & 1, abort);
+        for (int g = 0; go && g < kGroups; ++g) {
+          if (!(go = pf_wait(bar(kPFull + g), kt & 1, abort))) break;
+          tc05_fence_after();
 #pragma unroll
-        for (int k = 0; k < kPfKeys / 16; ++k) {
-          tc05_mma_ss(tmem_o, smem_desc_sw128(sP0 + b * kTile + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024),
-                      smem_desc_sw128(sV0 + b * kTile + k * 16 * 128, kHalf, 1024), idesc_o,
-                      (kt > 0 || k > 0) ? 1u : 0u);
+          for (int k = 0; k < kPfKeys / 16; ++k) {
+            tc05_mma_ss(tmem + g * 256 + 128,
+                        smem_desc_sw128(sP0 + g * kTile + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024),
+                        smem_desc_sw128(sV0 + b * kTile + k * 16 * 128, kHalf, 1024), idesc_o,
+                        (kt > 0 || k > 0) ? 1u : 0u);
+          }
+          tc05_commit(bar(kOFull + g));
         }
-        tc05_commit(bar(kOFull + b));
-        tc05_commit(bar(kVFree + b));
+        if (go) tc05_commit(bar(kVFree + b));
       }
     }
   } else {
-    // ================= softmax: 8 warps, two threads per row =================
-    const int r = (warp & 3) * 32 + lane;  // this thread's row
-    const int hc = warp >> 2;              // its half of the columns
-    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const int c0 = hc * (kPfKeys / 2);  // first S column (key) of this thread
-    const int d0 = hc * (kPfD / 2);     // first O column of this thread
+    // ====== softmax: group g = query tile g, two threads per row ======
+    const int g = warp / 8;
+    const int wg = warp % 8;
+    const int r = (wg & 3) * 32 + lane;  // this thread's row of the group's tile
+    const int hc = wg >> 2;              // its half of the columns
+    const uint32_t lane_base = static_cast<uint32_t>((wg & 3) * 32) << 16;
+    const uint32_t tmem_s = tmem + g * 256 + hc * (kPfKeys / 2);
+    const uint32_t tmem_o = tmem + g * 256 + 128 + hc * (kPfD / 2);
+    const int c0 = hc * (kPfKeys / 2);
+    const int tg0 = t0 + g * TQ;  // the group's first query
     // this row's query position (rows past the chunk repeat the last
     // position; they are not stored)
-    const int my_t = min(t0 + r / G, n - 1);
+    const int my_t = min(tg0 + r / G, n - 1);
     const int my_pos = ctx - n + my_t;
+    const int pos_first = ctx - n + min(tg0, n - 1);  // the group's earliest query position
     constexpr int kH = kPfKeys / 2;
     float m_run = -INFINITY, l_run = 0.f;
-    // Every softmax thread runs all nkt iterations and every named barrier,
-    // also after a timeout (then it skips the work), so that no thread waits
-    // at a barrier for one that left; `ok` is kept warp-uniform for the
-    // warp-collective TMEM accesses.
+    // All threads of a group run every iteration and every named barrier,
+    // also after a timeout (then they skip the work); `ok` is kept
+    // warp-uniform for the warp-collective TMEM accesses.
     bool ok = true;
     for (int kt = 0; kt < nkt; ++kt) {
-      const int b = kt & 1;
-      const uint32_t par = (kt >> 1) & 1;
-      ok = __all_sync(0xffffffffu, ok && pf_wait(bar(kSFull + b), par, abort));
-      float sv[kH];
+      ok = __all_sync(0xffffffffu, ok && pf_wait(bar(kSFull + g), kt & 1, abort));
+      const int key0 = kt * kPfKeys;
+      const bool masked = key0 + kPfKeys - 1 > pos_first;
+      // pass 1: this half's maximum (S read from TMEM 32 columns at a time)
+      float mraw = -INFINITY;
       if (ok) {
         tc05_fence_after();
 #pragma unroll
         for (int c = 0; c < kH; c += 32) {
           uint32_t v[32];
-          tmem_ld32(tmem + b * kPfKeys + lane_base + c0 + c, v);
+          tmem_ld32(tmem_s + lane_base + c, v);
           tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) sv[c + j] = __uint_as_float(v[j]);
+          for (int j = 0; j < 32; ++j) {
+            const float x = (masked && key0 + c0 + c + j > my_pos) ? -INFINITY : __uint_as_float(v[j]);
+            mraw = fmaxf(mraw, x);
+          }
         }
-        tc05_fence_before();
-        mbar_arrive(bar(kSFree + b));  // S[b] is read: the next S may go there
-      } else {
-#pragma unroll
-        for (int c = 0; c < kH; ++c) sv[c] = 0.f;
       }
-      const int key0 = kt * kPfKeys;
-      // only tiles that reach past the tile's earliest query need the causal mask
-      if (key0 + kPfKeys - 1 > pos_first) {
-#pragma unroll
-        for (int c = 0; c < kH; ++c)
-          if (key0 + c0 + c > my_pos) sv[c] = -INFINITY;
-      }
-      float mraw = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < kH; ++c) mraw = fmaxf(mraw, sv[c]);
-      s_half[hc][r] = mraw;
-      named_sync(1, kSoftThreads);
-      const float mx = fmaxf(s_half[0][r], s_half[1][r]) * p.scale_log2;  // scale > 0
+      s_half[g][hc][r] = mraw;
+      named_sync(1 + g, kGroupThreads);
+      const float mx = fmaxf(s_half[g][0][r], s_half[g][1][r]) * p.scale_log2;  // scale > 0
       float m_use = m_run, alpha = 1.f;
       if (mx > m_run + kLazyRescale || m_run == -INFINITY) {
         m_use = fmaxf(m_run, mx);
         alpha = m_run == -INFINITY ? 0.f : exp2f(m_run - m_use);
       }
       const float base = m_use == -INFINITY ? 0.f : m_use;
-      float sum = 0.f;
-#pragma unroll
-      for (int c = 0; c < kH; ++c) {
-        sv[c] = exp2f(fmaf(sv[c], p.scale_log2, -base));
-        sum += sv[c];
-      }
-      l_run = l_run * alpha + sum;  // this half's share of the row sum
-      m_run = m_use;
-      // O may be rescaled only once the previous PV product is complete;
-      // P[b] is free once the PV product two tiles back is
-      const bool rescale = kt > 0 && __any_sync(0xffffffffu, alpha != 1.f);
-      if (rescale) ok = __all_sync(0xffffffffu, ok && pf_wait(bar(kOFull + (b ^ 1)), ((kt - 1) >> 1) & 1, abort));
-      if (kt >= 2) ok = __all_sync(0xffffffffu, ok && pf_wait(bar(kOFull + b), ((kt - 2) >> 1) & 1, abort));
-      if (ok && rescale) {
+      // P and O of this group are free, and O may be rescaled, once the
+      // group's previous PV product is complete
+      if (kt > 0) ok = __all_sync(0xffffffffu, ok && pf_wait(bar(kOFull + g), (kt - 1) & 1, abort));
+      if (ok && kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
         tc05_fence_after();
 #pragma unroll
         for (int c = 0; c < kPfD / 2; c += 32) {
           uint32_t v[32];
-          tmem_ld32(tmem_o + lane_base + d0 + c, v);
+          tmem_ld32(tmem_o + lane_base + c, v);
           tmem_wait_ld();
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
-          tmem_st32(tmem_o + lane_base + d0 + c, v);
+          tmem_st32(tmem_o + lane_base + c, v);
         }
         tmem_wait_st();
-        tc05_fence_before();
       }
+      // pass 2: P = 2^(s * scale - m) into the K-major swizzled layout (this
+      // thread's 64 keys are one half of the tile)
+      float sum = 0.f;
+      if (ok) {
+        unsigned char* pp = pP0 + g * kTile;
+#pragma unroll
+        for (int c = 0; c < kH; c += 32) {
+          uint32_t v[32];
+          tmem_ld32(tmem_s + lane_base + c, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float x = (masked && key0 + c0 + c + j > my_pos) ? -INFINITY : __uint_as_float(v[j]);
+            const float e = exp2f(fmaf(x, p.scale_log2, -base));
+            sum += e;
+            v[j] = __float_as_uint(e);
+          }
+#pragma unroll
+          for (int j = 0; j < 32; j += 8) {
+            uint4 w;
+            w.x = pack2<T>(__uint_as_float(v[j]), __uint_as_float(v[j + 1]));
+            w.y = pack2<T>(__uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
+            w.z = pack2<T>(__uint_as_float(v[j + 4]), __uint_as_float(v[j + 5]));
+            w.w = pack2<T>(__uint_as_float(v[j + 6]), __uint_as_float(v[j + 7]));
+            *reinterpret_cast<uint4*>(pp + sw128_chunk(r, (c0 + c + j) >> 3)) = w;
+          }
+        }
+        tc05_fence_before();
+        mbar_arrive(bar(kSFree + g));  // S[g] is read: the next S may go there
+      }
+      l_run = l_run * alpha + sum;  // this half's share of the row sum
+      m_run = m_use;
       // keys past the context in the last tile: zero their V rows (stale or
-      // unwritten shared memory must not meet a zero weight as NaN)
+      // unwritten shared memory must not meet a zero weight as NaN); group 0
+      // does it, before its P is signalled, and the PV issuer serves group 0
+      // first
       const int valid = ctx - key0;
-      if (valid < kPfKeys) {
-        ok = ok && pf_wait(bar(kVFull + b), par, abort);
-        unsigned char* vt = pV0 + b * kTile;
-        const int tid = hc * kPfRows + r;
-        for (int i = tid; ok && i < (kPfKeys - valid) * 16; i += kSoftThreads) {
+      if (g == 0 && valid < kPfKeys) {
+        ok = ok && pf_wait(bar(kVFull + (kt & 1)), (kt >> 1) & 1, abort);
+        unsigned char* vt = pV0 + (kt & 1) * kTile;
+        for (int i = hc * kRowsPerGroup + r; ok && i < (kPfKeys - valid) * 16; i += kGroupThreads) {
           const int row = valid + i / 16, chunk = i % 16;
           *reinterpret_cast<uint4*>(vt + (chunk >> 3) * kHalf + row * 128 + (((chunk & 7) ^ (row & 7)) << 4)) =
               make_uint4(0u, 0u, 0u, 0u);
         }
       }
       if (ok) {
-        // P in the K-major swizzled layout of the PV product's A operand (this
-        // thread's 64 keys are one half of the tile)
-        unsigned char* pp = pP0 + b * kTile;
-#pragma unroll
-        for (int c = 0; c < kH; c += 8) {
-          uint4 w;
-          w.x = pack2<T>(sv[c], sv[c + 1]);
-          w.y = pack2<T>(sv[c + 2], sv[c + 3]);
-          w.z = pack2<T>(sv[c + 4], sv[c + 5]);
-          w.w = pack2<T>(sv[c + 6], sv[c + 7]);
-          *reinterpret_cast<uint4*>(pp + sw128_chunk(r, (c0 + c) >> 3)) = w;
-        }
         fence_proxy_async_smem();
-        mbar_arrive(bar(kPFull + b));
+        mbar_arrive(bar(kPFull + g));
       }
     }
-    ok = __all_sync(0xffffffffu, ok && pf_wait(bar(kOFull + ((nkt - 1) & 1)), ((nkt - 1) >> 1) & 1, abort));
+    ok = __all_sync(0xffffffffu, ok && pf_wait(bar(kOFull + g), (nkt - 1) & 1, abort));
     // ---- out = O / l for the rows of the chunk ----
-    s_half[hc][r] = l_run;
-    named_sync(1, kSoftThreads);
+    s_half[g][hc][r] = l_run;
+    named_sync(1 + g, kGroupThreads);
     if (ok) {
       tc05_fence_after();
-      const float l = s_half[0][r] + s_half[1][r];
+      const float l = s_half[g][0][r] + s_half[g][1][r];
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      const int tok = t0 + r / G;
+      const int tok = tg0 + r / G;
       T* orow = static_cast<T*>(p.out) +
-                (static_cast<int64_t>(q0 + min(tok, n - 1)) * p.num_heads + kvh * G + r % G) * kPfD + d0;
+                (static_cast<int64_t>(q0 + min(tok, n - 1)) * p.num_heads + kvh * G + r % G) * kPfD + hc * (kPfD / 2);
 #pragma unroll
       for (int c = 0; c < kPfD / 2; c += 32) {
         uint32_t v[32];
-        tmem_ld32(tmem_o + lane_base + d0 + c, v);
+        tmem_ld32(tmem_o + lane_base + c, v);
         tmem_wait_ld();
         if (tok < n) {
 #pragma unroll
@@ -405,7 +427,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     if (threadIdx.x == 0) {
       flag_error(p.debug_err, PA_DEVERR_TIMEOUT);
       // let tensor-core work already issued finish before its TMEM goes away
-      for (int i = 0; i < 2; ++i) {
+      for (int i = 0; i < kGroups; ++i) {
         mbar_wait_bounded(bar(kSFull + i), 0, 10000000ull);
         mbar_wait_bounded(bar(kOFull + i), 0, 10000000ull);
       }
@@ -482,7 +504,7 @@ cudaError_t launch_prefill_tc(void* out, const void* q, const void* k_cache, con
   if (!encode3d(&mk, k_cache, kdims, kstr, kbox) || !encode3d(&mv, v_cache, kdims, kstr, kbox))
     return cudaErrorInvalidValue;
   const int tiles = (max_query_len + pp.tokens_per_tile - 1) / pp.tokens_per_tile;
-  dim3 grid(tiles, num_kv_heads, num_seqs);
+  dim3 grid((tiles + kGroups - 1) / kGroups, num_kv_heads, num_seqs);
   cudaError_t err;
   if (dtype == PA_BF16) {
     static bool set = false;

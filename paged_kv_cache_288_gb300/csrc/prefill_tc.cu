@@ -42,13 +42,18 @@ constexpr int kRowsPerGroup = 128;              // rows of a query tile
 constexpr int kGroupThreads = 2 * kRowsPerGroup;        // two softmax threads per row
 constexpr int kSoftThreads = kGroups * kGroupThreads;   // 16 softmax warps
 constexpr int kPfThreads = kSoftThreads + 128;  // + 4 role warps: K loads, V loads, S issue, PV issue
-constexpr int kPfRows = 128;                   // MMA M
-constexpr int kPfKeys = 128;                   // keys per KV tile
+constexpr int kPfRows = 128;                   // MMA M: rows of a query tile
+constexpr int kPfKeys = 64;                    // keys per K/V tile (MMA N of S, K of PV)
 constexpr int kPfD = 128;                      // head dim
+constexpr int kStages = 4;                     // K and V tiles in flight
 constexpr int kHalf = kPfRows * 128;           // a 64-column half of a 128-row 16-bit tile
-constexpr int kTile = 2 * kHalf;               // 32 KiB
-constexpr int kSmemBytes = 7 * kTile + 3072;   // Q[2], P[2], K, V[2]; barriers; row exchange (2 KiB)
-constexpr uint32_t kTmemCols = 512;            // per group: S (128 columns), O (128 columns)
+constexpr int kTile = 2 * kHalf;               // a Q tile: 32 KiB
+constexpr int kPTile = kPfRows * 128;          // a P tile (128 rows x 64 keys): 16 KiB
+constexpr int kKVHalf = kPfKeys * 128;         // a 64-column half of a K/V tile: 8 KiB
+constexpr int kKVTile = 2 * kKVHalf;           // a K/V tile: 16 KiB
+// Q[2], P[2], K and V rings; barriers (512 B); row exchange (2 KiB), 227 KiB
+constexpr int kSmemBytes = 2 * kTile + 2 * kPTile + 2 * kStages * kKVTile + 1024 + 2048;
+constexpr uint32_t kTmemCols = 512;            // per group: S[2] (64 columns each), O (128 columns)
 constexpr float kLazyRescale = 8.f;            // log2 units
 
 struct PfParams {
@@ -135,25 +140,37 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     if (threadIdx.x == 0) flag_error(p.debug_err, PA_DEVERR_LAYOUT);
     return;
   }
-  unsigned char* sm = smem_raw;
-  // Q[2] | P[2] | K | V[2], 32 KiB each (Q[g], P[g]: query tile g of the CTA),
-  // then the barriers and the row exchange
+  unsigned char* const sm = smem_raw;
+  // Q[2] (32 KiB each) | P[2] (16 KiB) | K[kStages] | V[kStages] (16 KiB) |
+  // barriers | row exchange
   const uint32_t sQ0 = smem_u32(sm);
-  const uint32_t sP0 = sQ0 + 2 * kTile;
-  const uint32_t sK = sQ0 + 4 * kTile;
-  const uint32_t sV0 = sQ0 + 5 * kTile;
-  unsigned char* const pP0 = sm + 2 * kTile;
-  unsigned char* const pV0 = sm + 5 * kTile;
-  // barrier counts: 1 for TMA and tensor-core completions, 128 for one
-  // softmax group's threads
-  enum { kQ, kKFull, kKFree, kVFull, kVFree = kVFull + 2, kSFull = kVFree + 2, kOFull = kSFull + 2,
-         kSFree = kOFull + 2, kPFull = kSFree + 2, kNumBars = kPFull + 2 };
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + 7 * kTile);
-  uint32_t& tmem_slot = *reinterpret_cast<uint32_t*>(sm + 7 * kTile + 256);
-  int& s_abort = *reinterpret_cast<int*>(sm + 7 * kTile + 260);
+  const uint32_t sP0 = sQ0 + kGroups * kTile;
+  const uint32_t sK0 = sP0 + kGroups * kPTile;
+  const uint32_t sV0 = sK0 + kStages * kKVTile;
+  unsigned char* const pP0 = sm + kGroups * kTile;
+  unsigned char* const pV0 = sm + kGroups * kTile + kGroups * kPTile + kStages * kKVTile;
+  constexpr int kTiles = kGroups * kTile + kGroups * kPTile + 2 * kStages * kKVTile;
+  // barrier counts: 1 for TMA and tensor-core completions, kGroupThreads for
+  // one softmax group's threads
+  enum {
+    kQ,
+    kKFull,
+    kKFree = kKFull + kStages,
+    kVFull = kKFree + kStages,
+    kVFree = kVFull + kStages,
+    kSFull = kVFree + kStages,      // [group][S buffer]
+    kOFull = kSFull + 2 * kGroups,  // [group]
+    kSFree = kOFull + kGroups,      // [group][S buffer]
+    kPFull = kSFree + 2 * kGroups,  // [group]
+    kNumBars = kPFull + kGroups
+  };
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kTiles);
+  uint32_t& tmem_slot = *reinterpret_cast<uint32_t*>(sm + kTiles + 512);
+  int& s_abort = *reinterpret_cast<int*>(sm + kTiles + 516);
   // per row: each half's max, then its sum
-  float (*s_half)[2][kRowsPerGroup] = reinterpret_cast<float (*)[2][kRowsPerGroup]>(sm + 7 * kTile + 1024);
-  static_assert(kNumBars * 8 <= 256, "barriers fit their slot");
+  float(*s_half)[2][kRowsPerGroup] = reinterpret_cast<float(*)[2][kRowsPerGroup]>(sm + kTiles + 1024);
+  static_assert(kNumBars * 8 <= 512, "barriers fit their slot");
+  static_assert(kTiles + 1024 + kGroups * 2 * kRowsPerGroup * 4 <= kSmemBytes, "shared memory layout");
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   volatile int* abort = &s_abort;
 
@@ -166,7 +183,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   tc05_fence_before();
   __syncthreads();
   tc05_fence_after();
-  const uint32_t tmem = tmem_slot;  // group g: S at columns 256g .. +127, O at 256g + 128 .. +127
+  // group g: S[0], S[1] at columns 256g, 256g + 64 (64 each), O at 256g + 128
+  const uint32_t tmem = tmem_slot;
 
   // the keys the CTA needs: 0 .. position of its last query
   const int t_last = min(t0 + kGroups * TQ, n) - 1;
@@ -203,7 +221,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       if (!use[j]) continue;
       const int z = ent[j] * p.num_kv_heads + kvh;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) tma_load_3d(dst + h * kHalf + j * bs * 128, map, h * 64, 0, z, full);
+      for (int h = 0; h < 2; ++h) tma_load_3d(dst + h * kKVHalf + j * bs * 128, map, h * 64, 0, z, full);
     }
     return true;
   };
@@ -212,64 +230,67 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   if (warp >= kSoftThreads / 32) {
     // ====== one thread per role: K loads (+Q), V loads, S issue, PV issue ======
     const int role = warp - kSoftThreads / 32;
-    if (lane == 0 && role == 0) {
-      // Q of both tiles, then the K tiles into the single K buffer, each
-      // once both S products of the tile before have read it
-      mbar_arrive_expect_tx(bar(kQ), 4u * kHalf);
-      for (int g = 0; g < kGroups; ++g)
-        for (int h = 0; h < 2; ++h)
-          tma_load_3d(sQ0 + g * kTile + h * kHalf, &tmap_q, h * 64, kvh * G, q0 + t0 + g * TQ, bar(kQ));
-      for (int kt = 0; kt < nkt; ++kt)
-        if (!load_tile(&tmap_k, sK, bar(kKFull), bar(kKFree), (kt - 1) & 1, kt >= 1, kt)) break;
-    } else if (lane == 0 && role == 1) {
-      // the V tiles into a double buffer, refilled once both PV products of
-      // the tile two back have read it
+    if (lane == 0 && role <= 1) {
+      // K (role 0, which also loads Q) or V (role 1) tiles into a ring of
+      // kStages buffers, each refilled once both products of the tile
+      // kStages back have read it
+      const bool is_k = role == 0;
+      if (is_k) {
+        mbar_arrive_expect_tx(bar(kQ), 4u * kHalf);
+        for (int g = 0; g < kGroups; ++g)
+          for (int h = 0; h < 2; ++h)
+            tma_load_3d(sQ0 + g * kTile + h * kHalf, &tmap_q, h * 64, kvh * G, q0 + t0 + g * TQ, bar(kQ));
+      }
+      const CUtensorMap* map = is_k ? &tmap_k : &tmap_v;
+      const uint32_t dst0 = is_k ? sK0 : sV0;
+      const int full = is_k ? kKFull : kVFull, freed = is_k ? kKFree : kVFree;
       for (int kt = 0; kt < nkt; ++kt) {
-        const int b = kt & 1;
-        if (!load_tile(&tmap_v, sV0 + b * kTile, bar(kVFull + b), bar(kVFree + b), ((kt - 2) >> 1) & 1, kt >= 2,
-                       kt))
+        const int st = kt % kStages;
+        if (!load_tile(map, dst0 + st * kKVTile, bar(full + st), bar(freed + st), ((kt / kStages) - 1) & 1,
+                       kt >= kStages, kt))
           break;
       }
     } else if (lane == 0 && role == 2) {
-      // S[g] = Q[g] K^T for both groups once K arrived and the group has read
-      // its previous S
+      // S[g][kt % 2] = Q[g] K^T for both groups once K arrived and the group
+      // has read that S buffer two tiles back
       constexpr uint32_t idesc_s = mma_idesc_f16(kAB, 0, kPfRows, kPfKeys);
       bool go = pf_wait(bar(kQ), 0, abort);
       for (int kt = 0; go && kt < nkt; ++kt) {
-        go = pf_wait(bar(kKFull), kt & 1, abort);
+        const int st = kt % kStages, b = kt & 1;
+        go = pf_wait(bar(kKFull + st), (kt / kStages) & 1, abort);
         for (int g = 0; go && g < kGroups; ++g) {
-          if (kt >= 1 && !(go = pf_wait(bar(kSFree + g), (kt - 1) & 1, abort))) break;
+          if (kt >= 2 && !(go = pf_wait(bar(kSFree + 2 * g + b), ((kt - 2) >> 1) & 1, abort))) break;
           tc05_fence_after();
 #pragma unroll
           for (int k = 0; k < kPfD / 16; ++k) {
-            const uint32_t koff = (k >> 2) * kHalf + (k & 3) * 32;
-            tc05_mma_ss(tmem + g * 256, smem_desc_sw128(sQ0 + g * kTile + koff, 16, 1024),
-                        smem_desc_sw128(sK + koff, 16, 1024), idesc_s, k > 0);
+            tc05_mma_ss(tmem + g * 256 + b * kPfKeys,
+                        smem_desc_sw128(sQ0 + g * kTile + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024),
+                        smem_desc_sw128(sK0 + st * kKVTile + (k >> 2) * kKVHalf + (k & 3) * 32, 16, 1024),
+                        idesc_s, k > 0);
           }
-          tc05_commit(bar(kSFull + g));
+          tc05_commit(bar(kSFull + 2 * g + b));
         }
-        if (go) tc05_commit(bar(kKFree));
+        if (go) tc05_commit(bar(kKFree + st));
       }
     } else if (lane == 0 && role == 3) {
       // O[g] += P[g] V for both groups once V arrived and the group wrote P
       constexpr uint32_t idesc_o = mma_idesc_f16(kAB, 1, kPfRows, kPfD);
       bool go = true;
       for (int kt = 0; go && kt < nkt; ++kt) {
-        const int b = kt & 1;
-        go = pf_wait(bar(kVFull + b), (kt >> 1) & 1, abort);
+        const int st = kt % kStages;
+        go = pf_wait(bar(kVFull + st), (kt / kStages) & 1, abort);
         for (int g = 0; go && g < kGroups; ++g) {
           if (!(go = pf_wait(bar(kPFull + g), kt & 1, abort))) break;
           tc05_fence_after();
 #pragma unroll
           for (int k = 0; k < kPfKeys / 16; ++k) {
-            tc05_mma_ss(tmem + g * 256 + 128,
-                        smem_desc_sw128(sP0 + g * kTile + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024),
-                        smem_desc_sw128(sV0 + b * kTile + k * 16 * 128, kHalf, 1024), idesc_o,
+            tc05_mma_ss(tmem + g * 256 + 128, smem_desc_sw128(sP0 + g * kPTile + k * 32, 16, 1024),
+                        smem_desc_sw128(sV0 + st * kKVTile + k * 16 * 128, kKVHalf, 1024), idesc_o,
                         (kt > 0 || k > 0) ? 1u : 0u);
           }
           tc05_commit(bar(kOFull + g));
         }
-        if (go) tc05_commit(bar(kVFree + b));
+        if (go) tc05_commit(bar(kVFree + st));
       }
     }
   } else {
@@ -279,41 +300,46 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int r = (wg & 3) * 32 + lane;  // this thread's row of the group's tile
     const int hc = wg >> 2;              // its half of the columns
     const uint32_t lane_base = static_cast<uint32_t>((wg & 3) * 32) << 16;
-    const uint32_t tmem_s = tmem + g * 256 + hc * (kPfKeys / 2);
     const uint32_t tmem_o = tmem + g * 256 + 128 + hc * (kPfD / 2);
-    const int c0 = hc * (kPfKeys / 2);
-    const int tg0 = t0 + g * TQ;  // the group's first query
+    const int c0 = hc * (kPfKeys / 2);  // this thread's 32 keys of a tile
+    const int tg0 = t0 + g * TQ;        // the group's first query
     // this row's query position (rows past the chunk repeat the last
     // position; they are not stored)
     const int my_t = min(tg0 + r / G, n - 1);
     const int my_pos = ctx - n + my_t;
     const int pos_first = ctx - n + min(tg0, n - 1);  // the group's earliest query position
-    constexpr int kH = kPfKeys / 2;
     float m_run = -INFINITY, l_run = 0.f;
     // All threads of a group run every iteration and every named barrier,
     // also after a timeout (then they skip the work); `ok` is kept
     // warp-uniform for the warp-collective TMEM accesses.
     bool ok = true;
     for (int kt = 0; kt < nkt; ++kt) {
-      ok = __all_sync(0xffffffffu, ok && pf_wait(bar(kSFull + g), kt & 1, abort));
+      const int b = kt & 1, st = kt % kStages;
+      ok = __all_sync(0xffffffffu, ok && pf_wait(bar(kSFull + 2 * g + b), (kt >> 1) & 1, abort));
       const int key0 = kt * kPfKeys;
-      const bool masked = key0 + kPfKeys - 1 > pos_first;
-      // pass 1: this half's maximum (S read from TMEM 32 columns at a time)
-      float mraw = -INFINITY;
+      float x[32];
       if (ok) {
         tc05_fence_after();
+        uint32_t v[32];
+        tmem_ld32(tmem + g * 256 + b * kPfKeys + c0 + lane_base, v);
+        tmem_wait_ld();
+        tc05_fence_before();
+        mbar_arrive(bar(kSFree + 2 * g + b));  // S[g][b] is read: the next S may go there
 #pragma unroll
-        for (int c = 0; c < kH; c += 32) {
-          uint32_t v[32];
-          tmem_ld32(tmem_s + lane_base + c, v);
-          tmem_wait_ld();
+        for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(v[j]);
+      } else {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float x = (masked && key0 + c0 + c + j > my_pos) ? -INFINITY : __uint_as_float(v[j]);
-            mraw = fmaxf(mraw, x);
-          }
-        }
+        for (int j = 0; j < 32; ++j) x[j] = 0.f;
       }
+      // only tiles that reach past the group's earliest query need the mask
+      if (key0 + kPfKeys - 1 > pos_first) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (key0 + c0 + j > my_pos) x[j] = -INFINITY;
+      }
+      float mraw = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) mraw = fmaxf(mraw, x[j]);
       s_half[g][hc][r] = mraw;
       named_sync(1 + g, kGroupThreads);
       const float mx = fmaxf(s_half[g][0][r], s_half[g][1][r]) * p.scale_log2;  // scale > 0
@@ -323,6 +349,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         alpha = m_run == -INFINITY ? 0.f : exp2f(m_run - m_use);
       }
       const float base = m_use == -INFINITY ? 0.f : m_use;
+      float sum = 0.f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        x[j] = exp2f(fmaf(x[j], p.scale_log2, -base));
+        sum += x[j];
+      }
+      l_run = l_run * alpha + sum;  // this half's share of the row sum
+      m_run = m_use;
       // P and O of this group are free, and O may be rescaled, once the
       // group's previous PV product is complete
       if (kt > 0) ok = __all_sync(0xffffffffu, ok && pf_wait(bar(kOFull + g), (kt - 1) & 1, abort));
@@ -339,53 +373,32 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         tmem_wait_st();
       }
-      // pass 2: P = 2^(s * scale - m) into the K-major swizzled layout (this
-      // thread's 64 keys are one half of the tile)
-      float sum = 0.f;
-      if (ok) {
-        unsigned char* pp = pP0 + g * kTile;
-#pragma unroll
-        for (int c = 0; c < kH; c += 32) {
-          uint32_t v[32];
-          tmem_ld32(tmem_s + lane_base + c, v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float x = (masked && key0 + c0 + c + j > my_pos) ? -INFINITY : __uint_as_float(v[j]);
-            const float e = exp2f(fmaf(x, p.scale_log2, -base));
-            sum += e;
-            v[j] = __float_as_uint(e);
-          }
-#pragma unroll
-          for (int j = 0; j < 32; j += 8) {
-            uint4 w;
-            w.x = pack2<T>(__uint_as_float(v[j]), __uint_as_float(v[j + 1]));
-            w.y = pack2<T>(__uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
-            w.z = pack2<T>(__uint_as_float(v[j + 4]), __uint_as_float(v[j + 5]));
-            w.w = pack2<T>(__uint_as_float(v[j + 6]), __uint_as_float(v[j + 7]));
-            *reinterpret_cast<uint4*>(pp + sw128_chunk(r, (c0 + c + j) >> 3)) = w;
-          }
-        }
-        tc05_fence_before();
-        mbar_arrive(bar(kSFree + g));  // S[g] is read: the next S may go there
-      }
-      l_run = l_run * alpha + sum;  // this half's share of the row sum
-      m_run = m_use;
       // keys past the context in the last tile: zero their V rows (stale or
       // unwritten shared memory must not meet a zero weight as NaN); group 0
       // does it, before its P is signalled, and the PV issuer serves group 0
       // first
       const int valid = ctx - key0;
       if (g == 0 && valid < kPfKeys) {
-        ok = ok && pf_wait(bar(kVFull + (kt & 1)), (kt >> 1) & 1, abort);
-        unsigned char* vt = pV0 + (kt & 1) * kTile;
+        ok = ok && pf_wait(bar(kVFull + st), (kt / kStages) & 1, abort);
+        unsigned char* vt = pV0 + st * kKVTile;
         for (int i = hc * kRowsPerGroup + r; ok && i < (kPfKeys - valid) * 16; i += kGroupThreads) {
           const int row = valid + i / 16, chunk = i % 16;
-          *reinterpret_cast<uint4*>(vt + (chunk >> 3) * kHalf + row * 128 + (((chunk & 7) ^ (row & 7)) << 4)) =
+          *reinterpret_cast<uint4*>(vt + (chunk >> 3) * kKVHalf + row * 128 + (((chunk & 7) ^ (row & 7)) << 4)) =
               make_uint4(0u, 0u, 0u, 0u);
         }
       }
       if (ok) {
+        // P: 128 rows x 64 keys, K-major swizzled (one 64-column half)
+        unsigned char* pp = pP0 + g * kPTile;
+#pragma unroll
+        for (int j = 0; j < 32; j += 8) {
+          uint4 w;
+          w.x = pack2<T>(x[j], x[j + 1]);
+          w.y = pack2<T>(x[j + 2], x[j + 3]);
+          w.z = pack2<T>(x[j + 4], x[j + 5]);
+          w.w = pack2<T>(x[j + 6], x[j + 7]);
+          *reinterpret_cast<uint4*>(pp + r * 128 + ((((c0 + j) >> 3) ^ (r & 7)) << 4)) = w;
+        }
         fence_proxy_async_smem();
         mbar_arrive(bar(kPFull + g));
       }
@@ -427,10 +440,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     if (threadIdx.x == 0) {
       flag_error(p.debug_err, PA_DEVERR_TIMEOUT);
       // let tensor-core work already issued finish before its TMEM goes away
-      for (int i = 0; i < kGroups; ++i) {
-        mbar_wait_bounded(bar(kSFull + i), 0, 10000000ull);
-        mbar_wait_bounded(bar(kOFull + i), 0, 10000000ull);
-      }
+      for (int i = 0; i < kGroups; ++i) mbar_wait_bounded(bar(kOFull + i), 0, 10000000ull);
+      for (int i = 0; i < 2 * kGroups; ++i) mbar_wait_bounded(bar(kSFull + i), 0, 10000000ull);
     }
     __syncthreads();
   }

@@ -9,25 +9,28 @@
 // (LLM 추론 확장, 품질·비용 절충 필수, the prefill / decode split), which makes
 // QK^T and PV dense tiles.
 //
-// One CTA of 8 warps per (query tile, KV head, sequence). A tile is 128 MMA
-// rows: 128/G query tokens x the G query heads of the KV head, row r = token
-// r/G, head r%G. Row r (TMEM lane r) belongs to two threads, one per half of
-// the columns: warp w takes lanes 32(w%4)..+31 and columns 64(w/4)..+63 of
-// S and of O. Per 128-key tile:
-//   S = Q K^T   tcgen05.mma, M=128, N=128, K=128 (8 steps), Q and K tiles
-//               K-major with 128-byte swizzle, loaded by TMA (K block by block
-//               through the block table), S in TMEM columns 0..127;
-//   softmax     each thread reads its row of S from TMEM, masks keys past its
-//               position, keeps a running max in log2 units (the accumulator
-//               is rescaled only when the max grows by more than 2^8), and
-//               writes P (16-bit) to shared memory in the K-major swizzled
-//               layout;
+// One CTA of 20 warps per (pair of query tiles, KV head, sequence). A query
+// tile is 128 MMA rows: 128/G query tokens x the G query heads of the KV
+// head, row r = token r/G, head r%G; the two tiles of a CTA share every K/V
+// tile, which halves the TMA boxes per FLOP. Per 64-key tile:
+//   S = Q K^T   tcgen05.mma, M=128, N=64, K=128 (8 steps) per query tile; Q
+//               and K K-major with the 128-byte swizzle, loaded by TMA (K one
+//               box per 16-token block and 64-column half, through the block
+//               table); S double-buffered in TMEM (two 64-column buffers per
+//               query tile), so the next S is computed during the softmax;
+//   softmax     16 warps, two threads per row (32 keys each): read the row of
+//               S from TMEM, mask keys past the row's position, keep a running
+//               max in log2 units (O is rescaled only when the max grows by
+//               more than 2^8), and write P (16-bit) to shared memory in the
+//               K-major swizzled layout;
 //   O += P V    tcgen05.mma with V as an MN-major operand straight from its
-//               TMA tile, O in TMEM columns 128..255.
-// K/V tiles are double-buffered; the next tile's TMA loads go out as soon as
-// the MMA that read the buffer has completed. Every wait is bounded: on a
-// timeout the CTA sets PA_DEVERR_TIMEOUT, waits briefly for its own tensor
-// core work, frees its TMEM and returns.
+//               TMA tile, O in TMEM (128 columns per query tile).
+// Warp roles: one thread each loads K (and Q), loads V, issues S, issues PV.
+// K and V tiles go through rings of 4 buffers, each refilled once the
+// products that read it have completed. CTAs take the heaviest work first
+// (see the work order below). Every wait is bounded: on a timeout the CTA
+// sets PA_DEVERR_TIMEOUT, waits briefly for its own tensor core work, frees
+// its TMEM and returns.
 #include "common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
@@ -55,6 +58,7 @@ constexpr int kKVTile = 2 * kKVHalf;           // a K/V tile: 16 KiB
 constexpr int kSmemBytes = 2 * kTile + 2 * kPTile + 2 * kStages * kKVTile + 1024 + 2048;
 constexpr uint32_t kTmemCols = 512;            // per group: S[2] (64 columns each), O (128 columns)
 constexpr float kLazyRescale = 8.f;            // log2 units
+constexpr int kRankMaxSeqs = 256;              // batches up to this size are ordered by work
 
 struct PfParams {
   void* out;
@@ -85,13 +89,6 @@ __device__ __forceinline__ uint32_t pack2<f16>(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Byte offset of the 16-byte chunk holding columns 8c..8c+7 of row r in a
-// 128-row K-major tile stored as two 64-column halves with the 128-byte
-// swizzle (the layout TMA writes and the MMA descriptors describe).
-__device__ __forceinline__ uint32_t sw128_chunk(int r, int c) {
-  return (c >> 3) * kHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4);
-}
-
 // A wait on an mbarrier that gives up after kWaitLimitNs, or as soon as
 // another thread of the CTA has given up (*abort set).
 __device__ __forceinline__ bool pf_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
@@ -111,11 +108,88 @@ __device__ __forceinline__ void named_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+__device__ __forceinline__ void named_arrive(int id, int threads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// 2^x of the special function unit, subnormal results flushed to zero (a
+// softmax weight below 2^-126 is rounded to zero in 16 bits anyway)
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// (x0, x1) = (x0 * b + c, x1 * b + c) in one packed two-lane FMA
+__device__ __forceinline__ void exp_arg2(float& x0, float& x1, float b, float c) {
+  asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
+      "mov.b64 ra, {%0, %1};\n\tmov.b64 rb, {%2, %2};\n\tmov.b64 rc, {%3, %3};\n\t"
+      "fma.rn.f32x2 ra, ra, rb, rc;\n\tmov.b64 {%0, %1}, ra;\n\t}"
+      : "+f"(x0), "+f"(x1)
+      : "f"(b), "f"(c));
+}
+
+// (s0, s1) += (x0, x1) in one packed two-lane add
+__device__ __forceinline__ void add2(float& s0, float& s1, float x0, float x1) {
+  asm("{\n\t.reg .b64 ra, rb;\n\t"
+      "mov.b64 ra, {%0, %1};\n\tmov.b64 rb, {%2, %3};\n\t"
+      "add.rn.f32x2 ra, ra, rb;\n\tmov.b64 {%0, %1}, ra;\n\t}"
+      : "+f"(s0), "+f"(s1)
+      : "f"(x0), "f"(x1));
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                       const __grid_constant__ CUtensorMap tmap_v, const PfParams p) {
-  const int pair = blockIdx.x, kvh = blockIdx.y, seq = blockIdx.z;
+  // All shared memory is dynamic (no static __shared__ variables), so its
+  // base is the start of the CTA's shared window, which is 1024-aligned as
+  // the 128-byte swizzle needs; the kernel checks rather than assumes it.
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) flag_error(p.debug_err, PA_DEVERR_LAYOUT);
+    return;
+  }
+  unsigned char* const sm = smem_raw;
+
+  // Work order. CTAs start in launch order (x fastest), so the launch index
+  // L is mapped to the heaviest work first: sequences by decreasing work
+  // n (2 ctx - n), within a sequence the query-tile pairs from the last (the
+  // most keys) down, the KV heads fastest. This is list scheduling in
+  // decreasing order, which keeps long CTAs out of the last wave.
+  const int L = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+  const int kvh = L % gridDim.y;
+  const int pair = gridDim.x - 1 - (L / gridDim.y) % gridDim.x;
+  int seq = L / (gridDim.x * gridDim.y);
+  if (gridDim.z > 1 && gridDim.z <= kRankMaxSeqs) {
+    // the K ring is not in use yet: it holds each sequence's work
+    unsigned long long* w = reinterpret_cast<unsigned long long*>(sm + kGroups * kTile + kGroups * kPTile);
+    int& s_seq = *reinterpret_cast<int*>(sm + kGroups * kTile + kGroups * kPTile + kRankMaxSeqs * 8);
+    const int nseq = gridDim.z;
+    for (int i = threadIdx.x; i < nseq; i += blockDim.x) {
+      const int ni = p.query_start[i + 1] - p.query_start[i], ci = p.context_lens[i];
+      w[i] = (ni > 0 && ci >= ni) ? static_cast<unsigned long long>(ni) * (2ull * ci - ni) : 0ull;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < nseq; i += blockDim.x) {
+      const unsigned long long wi = w[i];
+      int rank = 0;
+      for (int j = 0; j < nseq; ++j) {
+        const unsigned long long wj = w[j];
+        rank += (wj > wi || (wj == wi && j < i)) ? 1 : 0;
+      }
+      if (rank == seq) s_seq = i;  // ranks are a permutation: one writer
+    }
+    fence_proxy_async_smem();  // the ring is written by TMA later
+    __syncthreads();
+    seq = s_seq;
+  }
   const int q0 = p.query_start[seq];
   const int n = p.query_start[seq + 1] - q0;
   const int G = p.group, TQ = p.tokens_per_tile;
@@ -131,16 +205,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     if (ctx < n) return;
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  // All shared memory is dynamic (no static __shared__ variables), so its
-  // base is the start of the CTA's shared window, which is 1024-aligned as
-  // the 128-byte swizzle needs; the kernel checks rather than assumes it.
-  extern __shared__ __align__(1024) unsigned char smem_raw[];
-  if (smem_u32(smem_raw) & 1023u) {
-    if (threadIdx.x == 0) flag_error(p.debug_err, PA_DEVERR_LAYOUT);
-    return;
-  }
-  unsigned char* const sm = smem_raw;
   // Q[2] (32 KiB each) | P[2] (16 KiB) | K[kStages] | V[kStages] (16 KiB) |
   // barriers | row exchange
   const uint32_t sQ0 = smem_u32(sm);
@@ -302,6 +366,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>((wg & 3) * 32) << 16;
     const uint32_t tmem_o = tmem + g * 256 + 128 + hc * (kPfD / 2);
     const int c0 = hc * (kPfKeys / 2);  // this thread's 32 keys of a tile
+    // named barriers 3 + 2g + h: half h's exchange slot has been read by
+    // the other half (half h waits on it before rewriting the slot)
+    const int bar_mine = 3 + 2 * g + hc, bar_other = 3 + 2 * g + (1 - hc);
     const int tg0 = t0 + g * TQ;        // the group's first query
     // this row's query position (rows past the chunk repeat the last
     // position; they are not stored)
@@ -337,42 +404,36 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         for (int j = 0; j < 32; ++j)
           if (key0 + c0 + j > my_pos) x[j] = -INFINITY;
       }
-      float mraw = -INFINITY;
+      float mraw = max3(x[0], x[1], x[2]);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) mraw = fmaxf(mraw, x[j]);
+      for (int j = 3; j < 31; j += 2) mraw = max3(mraw, x[j], x[j + 1]);
+      mraw = fmaxf(mraw, x[31]);
+      // the row's two halves exchange their maxima through one slot each: a
+      // slot is rewritten only after the other half has read it (bar_read)
+      if (kt > 0) named_sync(bar_mine, kGroupThreads);
       s_half[g][hc][r] = mraw;
       named_sync(1 + g, kGroupThreads);
       const float mx = fmaxf(s_half[g][0][r], s_half[g][1][r]) * p.scale_log2;  // scale > 0
+      named_arrive(bar_other, kGroupThreads);
       float m_use = m_run, alpha = 1.f;
       if (mx > m_run + kLazyRescale || m_run == -INFINITY) {
         m_use = fmaxf(m_run, mx);
-        alpha = m_run == -INFINITY ? 0.f : exp2f(m_run - m_use);
+        alpha = m_run == -INFINITY ? 0.f : ex2_ftz(m_run - m_use);
       }
-      const float base = m_use == -INFINITY ? 0.f : m_use;
-      float sum = 0.f;
+      const float nbase = m_use == -INFINITY ? 0.f : -m_use;
+      float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        x[j] = exp2f(fmaf(x[j], p.scale_log2, -base));
-        sum += x[j];
+      for (int j = 0; j < 32; j += 2) {
+        exp_arg2(x[j], x[j + 1], p.scale_log2, nbase);
+        x[j] = ex2_ftz(x[j]);
+        x[j + 1] = ex2_ftz(x[j + 1]);
+        add2(s0, s1, x[j], x[j + 1]);
       }
-      l_run = l_run * alpha + sum;  // this half's share of the row sum
+      l_run = l_run * alpha + (s0 + s1);  // this half's share of the row sum
       m_run = m_use;
       // P and O of this group are free, and O may be rescaled, once the
       // group's previous PV product is complete
       if (kt > 0) ok = __all_sync(0xffffffffu, ok && pf_wait(bar(kOFull + g), (kt - 1) & 1, abort));
-      if (ok && kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        tc05_fence_after();
-#pragma unroll
-        for (int c = 0; c < kPfD / 2; c += 32) {
-          uint32_t v[32];
-          tmem_ld32(tmem_o + lane_base + c, v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
-          tmem_st32(tmem_o + lane_base + c, v);
-        }
-        tmem_wait_st();
-      }
       // keys past the context in the last tile: zero their V rows (stale or
       // unwritten shared memory must not meet a zero weight as NaN); group 0
       // does it, before its P is signalled, and the PV issuer serves group 0
@@ -400,11 +461,30 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           *reinterpret_cast<uint4*>(pp + r * 128 + ((((c0 + j) >> 3) ^ (r & 7)) << 4)) = w;
         }
         fence_proxy_async_smem();
+      }
+      // O *= alpha, after P is written so that the weights are no longer
+      // held in registers
+      if (ok && kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        tc05_fence_after();
+#pragma unroll
+        for (int c = 0; c < kPfD / 2; c += 32) {
+          uint32_t v[32];
+          tmem_ld32(tmem_o + lane_base + c, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
+          tmem_st32(tmem_o + lane_base + c, v);
+        }
+        tmem_wait_st();
+      }
+      if (ok) {
+        tc05_fence_before();
         mbar_arrive(bar(kPFull + g));
       }
     }
     ok = __all_sync(0xffffffffu, ok && pf_wait(bar(kOFull + g), (nkt - 1) & 1, abort));
     // ---- out = O / l for the rows of the chunk ----
+    named_sync(bar_mine, kGroupThreads);
     s_half[g][hc][r] = l_run;
     named_sync(1 + g, kGroupThreads);
     if (ok) {

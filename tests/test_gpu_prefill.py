@@ -114,6 +114,25 @@ def test_prefill_flags_contexts_shorter_than_the_chunk():
     _check(out, ref, case, "the valid sequence", rows=slice(0, q1))
 
 
+@pytest.mark.parametrize("num_seqs", [9, 260])
+def test_prefill_work_order_covers_every_sequence(num_seqs):
+    """CTAs take the heaviest sequences first (by n (2 ctx - n)) when the batch
+    has at most 256 sequences, and launch order beyond that. Sequences of
+    equal work (ties, broken by index) and a batch past that limit must each
+    still land on their own rows; their data differ, so a swap shows."""
+    rng = np.random.default_rng(num_seqs)
+    if num_seqs == 9:
+        prefix = [40, 40, 40, 0, 300, 40, 7, 300, 0]
+        chunk = [33, 33, 33, 1, 70, 33, 90, 70, 1]
+    else:
+        prefix = rng.integers(0, 40, num_seqs).tolist()
+        chunk = rng.integers(0, 4, num_seqs).tolist()
+    case = workloads.prefill_case(72 + num_seqs, prefix, chunk, 8, 2, 128, 16, BF16)
+    out, err = _run(case)
+    assert err.item() == 0
+    _check(out, _oracle(case), case, f"{num_seqs} sequences")
+
+
 def test_prefill_llama8b_shape_sampled():
     """The bench's chunked-prefill batch (16 x 512-token chunks after prefixes
     up to 2048, 32/8/128 bf16): rows sampled across every sequence, checked

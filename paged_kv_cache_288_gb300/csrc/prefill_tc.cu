@@ -51,14 +51,20 @@ constexpr int kPfD = 128;                      // head dim
 constexpr int kStages = 4;                     // K and V tiles in flight
 constexpr int kHalf = kPfRows * 128;           // a 64-column half of a 128-row 16-bit tile
 constexpr int kTile = 2 * kHalf;               // a Q tile: 32 KiB
-constexpr int kPTile = kPfRows * 128;          // a P tile (128 rows x 64 keys): 16 KiB
 constexpr int kKVHalf = kPfKeys * 128;         // a 64-column half of a K/V tile: 8 KiB
 constexpr int kKVTile = 2 * kKVHalf;           // a K/V tile: 16 KiB
-// Q[2], P[2], K and V rings; barriers (512 B); row exchange (2 KiB), 227 KiB
-constexpr int kSmemBytes = 2 * kTile + 2 * kPTile + 2 * kStages * kKVTile + 1024 + 2048;
-constexpr uint32_t kTmemCols = 512;            // per group: S[2] (64 columns each), O (128 columns)
+// Q[2], K and V rings; barriers (512 B); row exchange (2 KiB)
+constexpr int kSmemBytes = 2 * kTile + 2 * kStages * kKVTile + 1024 + 2048;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+// per group: S[2] (64 columns each; P, 16-bit, replaces its S in the first
+// 32 columns), O (128 columns)
+constexpr uint32_t kTmemCols = 512;
 constexpr float kLazyRescale = 8.f;            // log2 units
 constexpr int kRankMaxSeqs = 256;              // batches up to this size are ordered by work
+// lanes of each loader warp that issue a tile's TMA boxes: one thread issues
+// only a few 2 KiB boxes per microsecond, so a tile's boxes are spread over
+// several lanes (box i = 2 * block + half goes to lane i % kLoadLanes)
+constexpr int kLoadLanes = 2;
 
 struct PfParams {
   void* out;
@@ -169,8 +175,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   int seq = L / (gridDim.x * gridDim.y);
   if (gridDim.z > 1 && gridDim.z <= kRankMaxSeqs) {
     // the K ring is not in use yet: it holds each sequence's work
-    unsigned long long* w = reinterpret_cast<unsigned long long*>(sm + kGroups * kTile + kGroups * kPTile);
-    int& s_seq = *reinterpret_cast<int*>(sm + kGroups * kTile + kGroups * kPTile + kRankMaxSeqs * 8);
+    unsigned long long* w = reinterpret_cast<unsigned long long*>(sm + kGroups * kTile);
+    int& s_seq = *reinterpret_cast<int*>(sm + kGroups * kTile + kRankMaxSeqs * 8);
     const int nseq = gridDim.z;
     for (int i = threadIdx.x; i < nseq; i += blockDim.x) {
       const int ni = p.query_start[i + 1] - p.query_start[i], ci = p.context_lens[i];
@@ -205,28 +211,27 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     if (ctx < n) return;
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // Q[2] (32 KiB each) | P[2] (16 KiB) | K[kStages] | V[kStages] (16 KiB) |
-  // barriers | row exchange
+  // Q[2] (32 KiB each) | K[kStages] | V[kStages] (16 KiB each) | barriers |
+  // row exchange
   const uint32_t sQ0 = smem_u32(sm);
-  const uint32_t sP0 = sQ0 + kGroups * kTile;
-  const uint32_t sK0 = sP0 + kGroups * kPTile;
+  const uint32_t sK0 = sQ0 + kGroups * kTile;
   const uint32_t sV0 = sK0 + kStages * kKVTile;
-  unsigned char* const pP0 = sm + kGroups * kTile;
-  unsigned char* const pV0 = sm + kGroups * kTile + kGroups * kPTile + kStages * kKVTile;
-  constexpr int kTiles = kGroups * kTile + kGroups * kPTile + 2 * kStages * kKVTile;
-  // barrier counts: 1 for TMA and tensor-core completions, kGroupThreads for
-  // one softmax group's threads
+  unsigned char* const pV0 = sm + kGroups * kTile + kStages * kKVTile;
+  constexpr int kTiles = kGroups * kTile + 2 * kStages * kKVTile;
+  // barrier counts: kLoadLanes for a K or V tile (one arrival per issuing
+  // lane), 1 for Q and the tensor-core completions, kGroupThreads for one
+  // softmax group's threads (P written)
   enum {
     kQ,
     kKFull,
     kKFree = kKFull + kStages,
     kVFull = kKFree + kStages,
     kVFree = kVFull + kStages,
-    kSFull = kVFree + kStages,      // [group][S buffer]
-    kOFull = kSFull + 2 * kGroups,  // [group]
-    kSFree = kOFull + kGroups,      // [group][S buffer]
-    kPFull = kSFree + 2 * kGroups,  // [group]
-    kNumBars = kPFull + kGroups
+    kSFull = kVFree + kStages,      // [group][S buffer]: S computed
+    kOFull = kSFull + 2 * kGroups,  // [group]: the group's PV products so far done
+    kSFree = kOFull + kGroups,      // [group][S buffer]: the PV that read its P done
+    kPFull = kSFree + 2 * kGroups,  // [group][S buffer]: P written
+    kNumBars = kPFull + 2 * kGroups
   };
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kTiles);
   uint32_t& tmem_slot = *reinterpret_cast<uint32_t*>(sm + kTiles + 512);
@@ -239,7 +244,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   volatile int* abort = &s_abort;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kNumBars; ++i) mbar_init(bar(i), i >= kSFree ? static_cast<uint32_t>(kGroupThreads) : 1u);
+    for (int i = 0; i < kNumBars; ++i) {
+      const bool tile_full = (i >= kKFull && i < kKFree) || (i >= kVFull && i < kVFree);
+      mbar_init(bar(i), i >= kPFull ? static_cast<uint32_t>(kGroupThreads) : tile_full ? kLoadLanes : 1u);
+    }
     mbar_init_fence();
     s_abort = 0;
   }
@@ -247,7 +255,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   tc05_fence_before();
   __syncthreads();
   tc05_fence_after();
-  // group g: S[0], S[1] at columns 256g, 256g + 64 (64 each), O at 256g + 128
+  // group g: S[0], S[1] at columns 256g, 256g + 64 (64 each), O at 256g + 128;
+  // P of S buffer b in its first 32 columns
   const uint32_t tmem = tmem_slot;
 
   // the keys the CTA needs: 0 .. position of its last query
@@ -257,35 +266,45 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const int blocks_per_tile = kPfKeys / bs;
   const int32_t* trow0 = p.block_tables + static_cast<int64_t>(seq) * p.max_blocks_per_seq;
 
-  // TMA of one K or V tile (thread): one 64-column box per block and half;
-  // the table entries are read (all loads in flight) before the buffer wait
+  // Block-table entries reach the loaders 32 at a time (lane l of a loader
+  // warp holds entry 32c + l of chunk c, one chunk read ahead), so the table
+  // read's latency is not paid once per tile. A tile's entries are lanes
+  // (kt % tiles_per_chunk) * blocks_per_tile + j.
+  const int tiles_per_chunk = 32 / blocks_per_tile;  // block_size in {8, 16, 32, 64}
+  const int nblk = (ctx + bs - 1) / bs;
+  auto fetch_chunk = [&](int c) -> int {
+    const int i = c * 32 + lane;
+    return i < nblk ? __ldg(trow0 + i) : 0;
+  };
+
+  // TMA of this lane's share of one K or V tile (lanes 0 .. kLoadLanes-1 of
+  // a loader warp): one 64-column box per block and half, box i = 2j + h
+  // issued by lane i % kLoadLanes; every such lane arrives on the full
+  // barrier once (its count), with the bytes of its own boxes
   auto load_tile = [&](const CUtensorMap* map, uint32_t dst, uint32_t full, uint32_t freed, uint32_t free_par,
-                       bool wait_free, int kt) -> bool {
+                       bool wait_free, int kt, const int (&ent)[kPfKeys / 8]) -> bool {
     const int lb0 = kt * blocks_per_tile;
-    int ent[kPfKeys / 8];
     bool use[kPfKeys / 8];
+    uint32_t nbox = 0;
 #pragma unroll
     for (int j = 0; j < kPfKeys / 8; ++j) {
-      use[j] = j < blocks_per_tile && (lb0 + j) * bs < ctx;
-      ent[j] = use[j] ? __ldg(trow0 + lb0 + j) : 0;
-    }
-    uint32_t nload = 0;
-#pragma unroll
-    for (int j = 0; j < kPfKeys / 8; ++j) {
+      use[j] = j < blocks_per_tile && lb0 + j < nblk;
       if (use[j] && (ent[j] < 0 || ent[j] >= p.num_blocks)) {
         flag_error(p.debug_err, PA_DEVERR_BLOCK_RANGE);
         use[j] = false;
       }
-      nload += use[j] ? 1u : 0u;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) nbox += (use[j] && (2 * j + h) % kLoadLanes == lane) ? 1u : 0u;
     }
     if (wait_free && !pf_wait(freed, free_par, abort)) return false;
-    mbar_arrive_expect_tx(full, nload * 2u * bs * 128u);
+    mbar_arrive_expect_tx(full, nbox * bs * 128u);
 #pragma unroll
     for (int j = 0; j < kPfKeys / 8; ++j) {
       if (!use[j]) continue;
       const int z = ent[j] * p.num_kv_heads + kvh;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) tma_load_3d(dst + h * kKVHalf + j * bs * 128, map, h * 64, 0, z, full);
+      for (int h = 0; h < 2; ++h)
+        if ((2 * j + h) % kLoadLanes == lane) tma_load_3d(dst + h * kKVHalf + j * bs * 128, map, h * 64, 0, z, full);
     }
     return true;
   };
@@ -294,12 +313,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   if (warp >= kSoftThreads / 32) {
     // ====== one thread per role: K loads (+Q), V loads, S issue, PV issue ======
     const int role = warp - kSoftThreads / 32;
-    if (lane == 0 && role <= 1) {
+    if (role <= 1) {
       // K (role 0, which also loads Q) or V (role 1) tiles into a ring of
       // kStages buffers, each refilled once both products of the tile
       // kStages back have read it
       const bool is_k = role == 0;
-      if (is_k) {
+      if (is_k && lane == 0) {
         mbar_arrive_expect_tx(bar(kQ), 4u * kHalf);
         for (int g = 0; g < kGroups; ++g)
           for (int h = 0; h < 2; ++h)
@@ -308,15 +327,25 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const CUtensorMap* map = is_k ? &tmap_k : &tmap_v;
       const uint32_t dst0 = is_k ? sK0 : sV0;
       const int full = is_k ? kKFull : kVFull, freed = is_k ? kKFree : kVFree;
+      int cur = fetch_chunk(0), nxt = fetch_chunk(1);
       for (int kt = 0; kt < nkt; ++kt) {
-        const int st = kt % kStages;
-        if (!load_tile(map, dst0 + st * kKVTile, bar(full + st), bar(freed + st), ((kt / kStages) - 1) & 1,
-                       kt >= kStages, kt))
-          break;
+        const int st = kt % kStages, slot = kt % tiles_per_chunk;
+        if (slot == 0 && kt > 0) {
+          cur = nxt;
+          nxt = fetch_chunk(kt / tiles_per_chunk + 1);
+        }
+        int ent[kPfKeys / 8];
+#pragma unroll
+        for (int j = 0; j < kPfKeys / 8; ++j) ent[j] = __shfl_sync(0xffffffffu, cur, (slot * blocks_per_tile + j) & 31);
+        bool go = true;
+        if (lane < kLoadLanes)
+          go = load_tile(map, dst0 + st * kKVTile, bar(full + st), bar(freed + st), ((kt / kStages) - 1) & 1,
+                         kt >= kStages, kt, ent);
+        if (!__all_sync(0xffffffffu, go)) break;
       }
     } else if (lane == 0 && role == 2) {
-      // S[g][kt % 2] = Q[g] K^T for both groups once K arrived and the group
-      // has read that S buffer two tiles back
+      // S[g][kt % 2] = Q[g] K^T for both groups once K arrived and the PV
+      // product that read the P in that S buffer two tiles back is done
       constexpr uint32_t idesc_s = mma_idesc_f16(kAB, 0, kPfRows, kPfKeys);
       bool go = pf_wait(bar(kQ), 0, abort);
       for (int kt = 0; go && kt < nkt; ++kt) {
@@ -338,21 +367,23 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
     } else if (lane == 0 && role == 3) {
       // O[g] += P[g] V for both groups once V arrived and the group wrote P
+      // (A = P from tensor memory, 16 keys = 8 columns per step)
       constexpr uint32_t idesc_o = mma_idesc_f16(kAB, 1, kPfRows, kPfD);
       bool go = true;
       for (int kt = 0; go && kt < nkt; ++kt) {
-        const int st = kt % kStages;
+        const int st = kt % kStages, b = kt & 1;
         go = pf_wait(bar(kVFull + st), (kt / kStages) & 1, abort);
         for (int g = 0; go && g < kGroups; ++g) {
-          if (!(go = pf_wait(bar(kPFull + g), kt & 1, abort))) break;
+          if (!(go = pf_wait(bar(kPFull + 2 * g + b), (kt >> 1) & 1, abort))) break;
           tc05_fence_after();
 #pragma unroll
           for (int k = 0; k < kPfKeys / 16; ++k) {
-            tc05_mma_ss(tmem + g * 256 + 128, smem_desc_sw128(sP0 + g * kPTile + k * 32, 16, 1024),
+            tc05_mma_ts(tmem + g * 256 + 128, tmem + g * 256 + b * kPfKeys + k * 8,
                         smem_desc_sw128(sV0 + st * kKVTile + k * 16 * 128, kKVHalf, 1024), idesc_o,
                         (kt > 0 || k > 0) ? 1u : 0u);
           }
           tc05_commit(bar(kOFull + g));
+          tc05_commit(bar(kSFree + 2 * g + b));
         }
         if (go) tc05_commit(bar(kVFree + st));
       }
@@ -390,8 +421,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         uint32_t v[32];
         tmem_ld32(tmem + g * 256 + b * kPfKeys + c0 + lane_base, v);
         tmem_wait_ld();
-        tc05_fence_before();
-        mbar_arrive(bar(kSFree + 2 * g + b));  // S[g][b] is read: the next S may go there
 #pragma unroll
         for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(v[j]);
       } else {
@@ -412,7 +441,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       // slot is rewritten only after the other half has read it (bar_read)
       if (kt > 0) named_sync(bar_mine, kGroupThreads);
       s_half[g][hc][r] = mraw;
+      // this barrier also orders both halves' S loads before either half's
+      // P store into the same columns
+      tc05_fence_before();
       named_sync(1 + g, kGroupThreads);
+      tc05_fence_after();
       const float mx = fmaxf(s_half[g][0][r], s_half[g][1][r]) * p.scale_log2;  // scale > 0
       named_arrive(bar_other, kGroupThreads);
       float m_use = m_run, alpha = 1.f;
@@ -431,9 +464,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
       l_run = l_run * alpha + (s0 + s1);  // this half's share of the row sum
       m_run = m_use;
-      // P and O of this group are free, and O may be rescaled, once the
-      // group's previous PV product is complete
-      if (kt > 0) ok = __all_sync(0xffffffffu, ok && pf_wait(bar(kOFull + g), (kt - 1) & 1, abort));
+      // P, 16-bit, two keys per column: this half's 32 keys go to columns
+      // 16 hc .. 16 hc + 15 of the S buffer they came from
+      uint32_t pw[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) pw[j] = pack2<T>(x[2 * j], x[2 * j + 1]);
       // keys past the context in the last tile: zero their V rows (stale or
       // unwritten shared memory must not meet a zero weight as NaN); group 0
       // does it, before its P is signalled, and the PV issuer serves group 0
@@ -447,24 +482,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           *reinterpret_cast<uint4*>(vt + (chunk >> 3) * kKVHalf + row * 128 + (((chunk & 7) ^ (row & 7)) << 4)) =
               make_uint4(0u, 0u, 0u, 0u);
         }
+        fence_proxy_async_smem();  // the PV product reads these rows
+        ok = __all_sync(0xffffffffu, ok);
       }
-      if (ok) {
-        // P: 128 rows x 64 keys, K-major swizzled (one 64-column half)
-        unsigned char* pp = pP0 + g * kPTile;
-#pragma unroll
-        for (int j = 0; j < 32; j += 8) {
-          uint4 w;
-          w.x = pack2<T>(x[j], x[j + 1]);
-          w.y = pack2<T>(x[j + 2], x[j + 3]);
-          w.z = pack2<T>(x[j + 4], x[j + 5]);
-          w.w = pack2<T>(x[j + 6], x[j + 7]);
-          *reinterpret_cast<uint4*>(pp + r * 128 + ((((c0 + j) >> 3) ^ (r & 7)) << 4)) = w;
-        }
-        fence_proxy_async_smem();
-      }
-      // O *= alpha, after P is written so that the weights are no longer
-      // held in registers
-      if (ok && kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+      if (ok) tmem_st16(tmem + g * 256 + b * kPfKeys + hc * 16 + lane_base, pw);
+      // O *= alpha, once the group's previous PV product is complete. Only a
+      // warp whose running max moved waits for it; otherwise the softmax runs
+      // ahead of the PV products.
+      const bool resc = kt > 0 && __any_sync(0xffffffffu, alpha != 1.f);
+      if (resc) ok = __all_sync(0xffffffffu, ok && pf_wait(bar(kOFull + g), (kt - 1) & 1, abort));
+      if (ok && resc) {
         tc05_fence_after();
 #pragma unroll
         for (int c = 0; c < kPfD / 2; c += 32) {
@@ -475,11 +502,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
           tmem_st32(tmem_o + lane_base + c, v);
         }
-        tmem_wait_st();
       }
       if (ok) {
+        tmem_wait_st();
         tc05_fence_before();
-        mbar_arrive(bar(kPFull + g));
+        mbar_arrive(bar(kPFull + 2 * g + b));
       }
     }
     ok = __all_sync(0xffffffffu, ok && pf_wait(bar(kOFull + g), (nkt - 1) & 1, abort));
@@ -543,12 +570,14 @@ PFN_cuTensorMapEncodeTiled_v12000 pf_encode_fn() {
   return fn;
 }
 
-bool encode3d(CUtensorMap* map, const void* base, const cuuint64_t (&dims)[3], const cuuint64_t (&strides)[2],
-              const cuuint32_t (&box)[3]) {
+template <int R>
+bool encode(CUtensorMap* map, const void* base, const cuuint64_t (&dims)[R], const cuuint64_t (&strides)[R - 1],
+            const cuuint32_t (&box)[R]) {
   auto fn = pf_encode_fn();
   if (fn == nullptr) return false;
-  cuuint32_t es[3] = {1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(base), dims, strides, box, es,
+  cuuint32_t es[R];
+  for (int i = 0; i < R; ++i) es[i] = 1;
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, R, const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -557,7 +586,8 @@ bool encode3d(CUtensorMap* map, const void* base, const cuuint64_t (&dims)[3], c
 
 bool prefill_supported(int group, int head_dim, pa_dtype dtype, int block_size) {
   return head_dim == kPfD && (dtype == PA_F16 || dtype == PA_BF16) &&
-         (group == 1 || group == 2 || group == 4 || group == 8) && block_size >= 8 && block_size <= 64;
+         (group == 1 || group == 2 || group == 4 || group == 8) &&
+         (block_size == 8 || block_size == 16 || block_size == 32 || block_size == 64);
 }
 
 cudaError_t launch_prefill_tc(void* out, const void* q, const void* k_cache, const void* v_cache,
@@ -584,15 +614,19 @@ cudaError_t launch_prefill_tc(void* out, const void* q, const void* k_cache, con
   pp.scale_log2 = scale * 1.4426950408889634f;
   CUtensorMap mq, mk, mv;
   const cuuint64_t row = static_cast<cuuint64_t>(kPfD) * 2;
-  if (!encode3d(&mq, q, {static_cast<cuuint64_t>(kPfD), static_cast<cuuint64_t>(num_heads),
-                         static_cast<cuuint64_t>(num_tokens)},
-                {row, row * num_heads}, {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(kPfRows / G)}))
+  if (!encode<3>(&mq, q,
+                 {static_cast<cuuint64_t>(kPfD), static_cast<cuuint64_t>(num_heads),
+                  static_cast<cuuint64_t>(num_tokens)},
+                 {row, row * num_heads}, {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(kPfRows / G)}))
     return cudaErrorInvalidValue;
   const cuuint64_t bxh = static_cast<cuuint64_t>(num_blocks) * num_kv_heads;
-  const cuuint64_t kdims[3] = {static_cast<cuuint64_t>(kPfD), static_cast<cuuint64_t>(block_size), bxh};
-  const cuuint64_t kstr[2] = {row, row * block_size};
-  const cuuint32_t kbox[3] = {64, static_cast<cuuint32_t>(block_size), 1};
-  if (!encode3d(&mk, k_cache, kdims, kstr, kbox) || !encode3d(&mv, v_cache, kdims, kstr, kbox))
+  const cuuint64_t bsz = static_cast<cuuint64_t>(block_size);
+  const cuuint32_t bsb = static_cast<cuuint32_t>(block_size);
+  // K and V: (column, row, block x head), one 64-column half of a block per box
+  const cuuint64_t kdims[3] = {static_cast<cuuint64_t>(kPfD), bsz, bxh};
+  const cuuint64_t kstr[2] = {row, row * bsz};
+  const cuuint32_t kbox[3] = {64, bsb, 1};
+  if (!encode<3>(&mk, k_cache, kdims, kstr, kbox) || !encode<3>(&mv, v_cache, kdims, kstr, kbox))
     return cudaErrorInvalidValue;
   const int tiles = (max_query_len + pp.tokens_per_tile - 1) / pp.tokens_per_tile;
   dim3 grid((tiles + kGroups - 1) / kGroups, num_kv_heads, num_seqs);

@@ -9,7 +9,7 @@
 // (LLM 추론 확장, 품질·비용 절충 필수, the prefill / decode split), which makes
 // QK^T and PV dense tiles.
 //
-// One CTA of 20 warps per (pair of query tiles, KV head, sequence). A query
+// One CTA of 24 warps per (pair of query tiles, KV head, sequence). A query
 // tile is 128 MMA rows: 128/G query tokens x the G query heads of the KV
 // head, row r = token r/G, head r%G; the two tiles of a CTA share every K/V
 // tile, which halves the TMA boxes per FLOP. Per 64-key tile:
@@ -25,7 +25,8 @@
 //               K-major swizzled layout;
 //   O += P V    tcgen05.mma with V as an MN-major operand straight from its
 //               TMA tile, O in TMEM (128 columns per query tile).
-// Warp roles: one thread each loads K (and Q), loads V, issues S, issues PV.
+// Warp roles: K loaders (the first also loads Q), V loaders, one thread
+// each issues S and PV.
 // K and V tiles go through rings of 4 buffers, each refilled once the
 // products that read it have completed. CTAs take the heaviest work first
 // (see the work order below). Every wait is bounded: on a timeout the CTA
@@ -44,7 +45,24 @@ constexpr int kGroups = 2;                      // query tiles per CTA (they sha
 constexpr int kRowsPerGroup = 128;              // rows of a query tile
 constexpr int kGroupThreads = 2 * kRowsPerGroup;        // two softmax threads per row
 constexpr int kSoftThreads = kGroups * kGroupThreads;   // 16 softmax warps
-constexpr int kPfThreads = kSoftThreads + 128;  // + 4 role warps: K loads, V loads, S issue, PV issue
+// TMA issue: one thread issues only a few 2 KiB boxes per microsecond and
+// lanes of one warp add little, so each of K and V has kLoadWarps loader
+// warps with kLoadLanes issuing lanes each; box i (= 2 * block + half) of a
+// tile goes to loader q = i % (kLoadWarps * kLoadLanes), which is lane
+// q / kLoadWarps of loader warp q % kLoadWarps
+constexpr int kLoadWarps = 3;
+constexpr int kLoadLanes = 1;
+constexpr int kLoaders = kLoadWarps * kLoadLanes;
+// + role warps: K loaders (the first also loads Q), V loaders, S issue, PV issue
+constexpr int kPfThreads = kSoftThreads + 32 * (2 * kLoadWarps + 2);
+static_assert(kPfThreads % 128 == 0, "whole warpgroups");
+// Registers: 24 warps are 6 per scheduler, which caps a thread at 80 at
+// launch. The softmax warpgroups raise theirs to 96 and the role warpgroups
+// lower theirs to 48 (setmaxnreg); the split must not exceed what the launch
+// allocated, or the raise waits forever.
+constexpr int kLaunchRegs = 80, kSoftRegs = 96, kRoleRegs = 48;
+static_assert(kSoftThreads * kSoftRegs + (kPfThreads - kSoftThreads) * kRoleRegs <= kPfThreads * kLaunchRegs,
+              "register split within the launch allocation");
 constexpr int kPfRows = 128;                   // MMA M: rows of a query tile
 constexpr int kPfKeys = 64;                    // keys per K/V tile (MMA N of S, K of PV)
 constexpr int kPfD = 128;                      // head dim
@@ -61,10 +79,6 @@ static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLazyRescale = 8.f;            // log2 units
 constexpr int kRankMaxSeqs = 256;              // batches up to this size are ordered by work
-// lanes of each loader warp that issue a tile's TMA boxes: one thread issues
-// only a few 2 KiB boxes per microsecond, so a tile's boxes are spread over
-// several lanes (box i = 2 * block + half goes to lane i % kLoadLanes)
-constexpr int kLoadLanes = 2;
 
 struct PfParams {
   void* out;
@@ -218,8 +232,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const uint32_t sV0 = sK0 + kStages * kKVTile;
   unsigned char* const pV0 = sm + kGroups * kTile + kStages * kKVTile;
   constexpr int kTiles = kGroups * kTile + 2 * kStages * kKVTile;
-  // barrier counts: kLoadLanes for a K or V tile (one arrival per issuing
-  // lane), 1 for Q and the tensor-core completions, kGroupThreads for one
+  // barrier counts: kLoaders for a K or V tile (one arrival per issuing
+  // thread), 1 for Q and the tensor-core completions, kGroupThreads for one
   // softmax group's threads (P written)
   enum {
     kQ,
@@ -246,7 +260,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i) {
       const bool tile_full = (i >= kKFull && i < kKFree) || (i >= kVFull && i < kVFree);
-      mbar_init(bar(i), i >= kPFull ? static_cast<uint32_t>(kGroupThreads) : tile_full ? kLoadLanes : 1u);
+      mbar_init(bar(i), i >= kPFull ? static_cast<uint32_t>(kGroupThreads) : tile_full ? static_cast<uint32_t>(kLoaders) : 1u);
     }
     mbar_init_fence();
     s_abort = 0;
@@ -277,12 +291,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     return i < nblk ? __ldg(trow0 + i) : 0;
   };
 
-  // TMA of this lane's share of one K or V tile (lanes 0 .. kLoadLanes-1 of
-  // a loader warp): one 64-column box per block and half, box i = 2j + h
-  // issued by lane i % kLoadLanes; every such lane arrives on the full
-  // barrier once (its count), with the bytes of its own boxes
-  auto load_tile = [&](const CUtensorMap* map, uint32_t dst, uint32_t full, uint32_t freed, uint32_t free_par,
-                       bool wait_free, int kt, const int (&ent)[kPfKeys / 8]) -> bool {
+  // TMA of loader q's share of one K or V tile: one 64-column box per block
+  // and half, box i = 2j + h issued by loader i % kLoaders; every loader
+  // arrives on the full barrier once (its count), with the bytes of its own
+  // boxes
+  auto load_tile = [&](const CUtensorMap* map, int q, uint32_t dst, uint32_t full, uint32_t freed,
+                       uint32_t free_par, bool wait_free, int kt, const int (&ent)[kPfKeys / 8]) -> bool {
     const int lb0 = kt * blocks_per_tile;
     bool use[kPfKeys / 8];
     uint32_t nbox = 0;
@@ -294,7 +308,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         use[j] = false;
       }
 #pragma unroll
-      for (int h = 0; h < 2; ++h) nbox += (use[j] && (2 * j + h) % kLoadLanes == lane) ? 1u : 0u;
+      for (int h = 0; h < 2; ++h) nbox += (use[j] && (2 * j + h) % kLoaders == q) ? 1u : 0u;
     }
     if (wait_free && !pf_wait(freed, free_par, abort)) return false;
     mbar_arrive_expect_tx(full, nbox * bs * 128u);
@@ -304,21 +318,23 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const int z = ent[j] * p.num_kv_heads + kvh;
 #pragma unroll
       for (int h = 0; h < 2; ++h)
-        if ((2 * j + h) % kLoadLanes == lane) tma_load_3d(dst + h * kKVHalf + j * bs * 128, map, h * 64, 0, z, full);
+        if ((2 * j + h) % kLoaders == q) tma_load_3d(dst + h * kKVHalf + j * bs * 128, map, h * 64, 0, z, full);
     }
     return true;
   };
 
   constexpr uint32_t kAB = std::is_same<T, bf16>::value ? 1u : 0u;
   if (warp >= kSoftThreads / 32) {
-    // ====== one thread per role: K loads (+Q), V loads, S issue, PV issue ======
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRoleRegs));
+    // ====== roles: K loaders (+Q), V loaders, S issue, PV issue ======
     const int role = warp - kSoftThreads / 32;
-    if (role <= 1) {
-      // K (role 0, which also loads Q) or V (role 1) tiles into a ring of
-      // kStages buffers, each refilled once both products of the tile
-      // kStages back have read it
-      const bool is_k = role == 0;
-      if (is_k && lane == 0) {
+    if (role < 2 * kLoadWarps) {
+      // K (the first kLoadWarps role warps; the first also loads Q) or V
+      // tiles into a ring of kStages buffers, each refilled once both
+      // products of the tile kStages back have read it
+      const bool is_k = role < kLoadWarps;
+      const int lw = is_k ? role : role - kLoadWarps;
+      if (is_k && lw == 0 && lane == 0) {
         mbar_arrive_expect_tx(bar(kQ), 4u * kHalf);
         for (int g = 0; g < kGroups; ++g)
           for (int h = 0; h < 2; ++h)
@@ -339,11 +355,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         for (int j = 0; j < kPfKeys / 8; ++j) ent[j] = __shfl_sync(0xffffffffu, cur, (slot * blocks_per_tile + j) & 31);
         bool go = true;
         if (lane < kLoadLanes)
-          go = load_tile(map, dst0 + st * kKVTile, bar(full + st), bar(freed + st), ((kt / kStages) - 1) & 1,
+          go = load_tile(map, lw + kLoadWarps * lane, dst0 + st * kKVTile, bar(full + st), bar(freed + st), ((kt / kStages) - 1) & 1,
                          kt >= kStages, kt, ent);
         if (!__all_sync(0xffffffffu, go)) break;
       }
-    } else if (lane == 0 && role == 2) {
+    } else if (lane == 0 && role == 2 * kLoadWarps) {
       // S[g][kt % 2] = Q[g] K^T for both groups once K arrived and the PV
       // product that read the P in that S buffer two tiles back is done
       constexpr uint32_t idesc_s = mma_idesc_f16(kAB, 0, kPfRows, kPfKeys);
@@ -365,7 +381,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         if (go) tc05_commit(bar(kKFree + st));
       }
-    } else if (lane == 0 && role == 3) {
+    } else if (lane == 0 && role == 2 * kLoadWarps + 1) {
       // O[g] += P[g] V for both groups once V arrived and the group wrote P
       // (A = P from tensor memory, 16 keys = 8 columns per step)
       constexpr uint32_t idesc_o = mma_idesc_f16(kAB, 1, kPfRows, kPfD);
@@ -389,6 +405,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
     }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftRegs));
     // ====== softmax: group g = query tile g, two threads per row ======
     const int g = warp / 8;
     const int wg = warp % 8;

@@ -218,3 +218,13 @@ def test_fp8_kv_decode(q_dtype, bs):
         assert_close(out, ref, q_dtype, FP8_E4M3, f"fp8 part={part}")
     assert dc.debug_err.item() == 0
     assert np.array_equal(host_bits(dc.k_cache), kc)
+
+
+@pytest.mark.parametrize("group", [2, 4, 8])
+def test_merges_of_few_and_many_ranges_in_one_batch(group):
+    """One auto-schedule call whose pairs are merged from a few ranges (2000
+    tokens), from hundreds of static shares and chunks (a 32768-token
+    context), or not at all (a 100-token and a one-token pair)."""
+    lengths = [32768, 2000, 100, 1]
+    case = workloads.paged_case(700 + group, lengths, group * 4, 4, 128, 16, BF16, name=f"merges{group}")
+    _check(case)

@@ -21,12 +21,13 @@
 //   softmax     16 warps, two threads per row (32 keys each): read the row of
 //               S from TMEM, mask keys past the row's position, keep a running
 //               max in log2 units (O is rescaled only when the max grows by
-//               more than 2^8), and write P (16-bit) to shared memory in the
-//               K-major swizzled layout;
-//   O += P V    tcgen05.mma with V as an MN-major operand straight from its
-//               TMA tile, O in TMEM (128 columns per query tile).
-// Warp roles: K loaders (the first also loads Q), V loaders, one thread
-// each issues S and PV.
+//               more than 2^8), and store P (16-bit) in TMEM over the S it
+//               came from;
+//   O += P V    tcgen05.mma with A = P from TMEM and V an MN-major operand
+//               straight from its TMA tile, O in TMEM (128 columns per query
+//               tile).
+// Warp roles: three K loaders (the first also loads Q) and three V loaders
+// (a tile's boxes spread over them), one thread each issues S and PV.
 // K and V tiles go through rings of 4 buffers, each refilled once the
 // products that read it have completed. CTAs take the heaviest work first
 // (see the work order below). Every wait is bounded: on a timeout the CTA

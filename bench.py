@@ -81,6 +81,8 @@ def rank_seed(base, rank):
 
 
 def make_case(name, rank):
+    if name == "tiny":
+        return workloads.tiny()[0]
     if name == "llama8b":
         return workloads.llama8b(seed=rank_seed(1002, rank))
     if name == "shared_prefix":

@@ -62,3 +62,13 @@ def test_replica_workloads_share_shape():
     a = workloads.llama8b_lengths(bench.rank_seed(1002, 0), num_seqs=8)
     b = workloads.llama8b_lengths(bench.rank_seed(1002, 1), num_seqs=8)
     assert a.shape == b.shape and not (a == b).all()
+
+
+def test_oracle_timing_spreads_sequences_over_processes():
+    """The host oracle baseline runs one single-threaded process per worker,
+    never more workers than sequences, and reports one time per repetition."""
+    import bench
+    times, workers = bench.oracle_seconds("tiny", 4, 2, workers=2)
+    assert workers == 2 and len(times) == 2 and all(t > 0 for t in times)
+    times, workers = bench.oracle_seconds("tiny", 1, 1, workers=4)
+    assert workers == 1 and len(times) == 1

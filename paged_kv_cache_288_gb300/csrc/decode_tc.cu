@@ -1071,13 +1071,10 @@ cudaError_t launch_typed(const TcParams& tp, const void* k_cache, const void* v_
       !make_cache_map(&mv, v_cache, D, int(sizeof(KT)), p.block_size, TT, bxh))
     return cudaErrorInvalidValue;
   auto kernel = decode_tc_kernel<QT, KT, D, TT>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem_bytes<QT, KT, D, TT>(kTcMaxSeqs)));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> attr_set{0};
+  cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(kernel),
+                                      static_cast<int>(smem_bytes<QT, KT, D, TT>(kTcMaxSeqs)), attr_set);
+  if (e != cudaSuccess) return e;
   const int grid = (tp.num_warps + kWarps - 1) / kWarps;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

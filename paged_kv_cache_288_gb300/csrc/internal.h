@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "pa.h"
 
 namespace pa {
@@ -13,6 +15,20 @@ struct DecodeParams;
 
 // Adds n to the process-wide count of kernels launched by this library.
 void note_launches(int n);
+
+// Raises the dynamic shared memory limit of kernel `fn` to `bytes` on the
+// current device, once per device (a function attribute is per device);
+// `done` holds one bit per device already set.
+inline cudaError_t set_smem_limit_once(const void* fn, int bytes, std::atomic<unsigned long long>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit != 0 && (done.load(std::memory_order_relaxed) & bit) != 0) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_relaxed);
+  return e;
+}
 
 // Sets the message pa_last_error_message() returns on this thread.
 void set_last_error(const char* fmt, ...);

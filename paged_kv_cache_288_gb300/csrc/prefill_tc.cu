@@ -650,20 +650,14 @@ cudaError_t launch_prefill_tc(void* out, const void* q, const void* k_cache, con
   dim3 grid((tiles + kGroups - 1) / kGroups, num_kv_heads, num_seqs);
   cudaError_t err;
   if (dtype == PA_BF16) {
-    static bool set = false;
-    if (!set) {
-      err = cudaFuncSetAttribute(prefill_tc_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-      if (err != cudaSuccess) return err;
-      set = true;
-    }
+    static std::atomic<unsigned long long> set{0};
+    err = set_smem_limit_once(reinterpret_cast<const void*>(prefill_tc_kernel<bf16>), kSmemBytes, set);
+    if (err != cudaSuccess) return err;
     prefill_tc_kernel<bf16><<<grid, kPfThreads, kSmemBytes, stream>>>(mq, mk, mv, pp);
   } else {
-    static bool set = false;
-    if (!set) {
-      err = cudaFuncSetAttribute(prefill_tc_kernel<f16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-      if (err != cudaSuccess) return err;
-      set = true;
-    }
+    static std::atomic<unsigned long long> set{0};
+    err = set_smem_limit_once(reinterpret_cast<const void*>(prefill_tc_kernel<f16>), kSmemBytes, set);
+    if (err != cudaSuccess) return err;
     prefill_tc_kernel<f16><<<grid, kPfThreads, kSmemBytes, stream>>>(mq, mk, mv, pp);
   }
   err = cudaGetLastError();

@@ -145,3 +145,31 @@ def test_swap_blocks_argument_checks(L):
     assert swap(pairs=0) == 0             # nothing to move: no CUDA call
     assert swap(layers=0) == 0
     assert L.pa_swap_blocks(None, arr, arr, arr, 1, 16, 1, 4, 4, 4096, NULL, NULL) == 1
+
+
+def _prefill(L, **kw):
+    args = dict(out=16, q=16, k=16, v=16, tables=16, width=16, lens=16, qstart=16, B=2, T=64, maxq=32,
+                Hq=32, Hkv=8, d=128, bs=16, Nb=100, scale=0.1, dt=pa.BF16, err=NULL, stream=NULL)
+    args.update(kw)
+    return L.pa_prefill(args["out"], args["q"], args["k"], args["v"], args["tables"], args["width"],
+                        args["lens"], args["qstart"], args["B"], args["T"], args["maxq"], args["Hq"],
+                        args["Hkv"], args["d"], args["bs"], args["Nb"], args["scale"], args["dt"],
+                        args["err"], args["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(Hq=6, Hkv=4), 1),                # heads not a multiple
+    (dict(bs=12), 2),                      # unsupported block size
+    (dict(d=64), 2),                       # head_dim 128 only
+    (dict(Hq=24, Hkv=8), 2),               # group of 3
+    (dict(dt=pa.FP8_E4M3), 2),             # 16-bit only
+    (dict(Nb=0), 1),                       # empty pool
+    (dict(B=-1), 1),
+    (dict(out=NULL), 1),
+    (dict(q=24), 1),                       # misaligned
+    (dict(B=70000), 2),                    # more sequences than the grid takes
+    (dict(B=0), 0),                        # nothing to do
+    (dict(maxq=0), 0),
+])
+def test_prefill_argument_checks(L, kw, status):
+    assert _prefill(L, **kw) == status, pa.lib().pa_last_error_message()

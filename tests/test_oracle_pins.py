@@ -153,6 +153,48 @@ def test_e4m3_encoder_matches_exhaustive_nearest():
 
 
 # ----------------------------------------------------------------------------
+# widening of stored codes to float64, against torch's own conversions
+
+
+_TORCH_VIEW = {F16: torch.float16, BF16: torch.bfloat16, FP8_E4M3: torch.float8_e4m3fn}
+
+
+def _torch_widen(bits, dtype):
+    """Raw codes -> float64 through torch's reinterpretation of the bits, an
+    implementation of the formats that shares nothing with the oracle."""
+    a = np.ascontiguousarray(bits)
+    if dtype == FP8_E4M3:
+        t = torch.from_numpy(a.astype(np.uint8)).view(torch.float8_e4m3fn)
+    else:
+        t = torch.from_numpy(a.astype(np.uint16).view(np.int16)).view(_TORCH_VIEW[dtype])
+    return t.double().numpy()
+
+
+@pytest.mark.parametrize("dtype,ncodes", [(F16, 1 << 16), (BF16, 1 << 16), (FP8_E4M3, 256)])
+def test_bits_to_f64_matches_torch_on_every_code(dtype, ncodes):
+    """Every 16-bit (f16, bf16) and 8-bit (E4M3) code widens to the value torch
+    gives the same bits: same value, same sign of zero, NaN exactly where torch
+    has NaN. A wrong shift, a float16 view used for bf16 or a dropped sign
+    fails here."""
+    codes = np.arange(ncodes, dtype=np.uint16 if ncodes > 256 else np.uint8)
+    got = oracle.bits_to_f64(codes, dtype)
+    want = _torch_widen(codes, dtype)
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    fin = ~np.isnan(want)
+    assert np.array_equal(got[fin], want[fin])
+    assert np.array_equal(np.signbit(got[fin]), np.signbit(want[fin]))
+
+
+def test_bits_to_f64_known_codes():
+    """A few codes whose values the formats fix: 1.0, -2.0, the largest finite
+    value, the smallest subnormal."""
+    assert oracle.bits_to_f64(np.array([0x3F80, 0xC000, 0x7F7F, 0x0001]), BF16).tolist() == [
+        1.0, -2.0, (2 - 2.0 ** -7) * 2.0 ** 127, 2.0 ** -133]
+    assert oracle.bits_to_f64(np.array([0x3C00, 0xC000, 0x7BFF, 0x0001]), F16).tolist() == [
+        1.0, -2.0, 65504.0, 2.0 ** -24]
+
+
+# ----------------------------------------------------------------------------
 # scatter and copy
 
 
@@ -344,15 +386,16 @@ def test_decode_matches_torch_sdpa_float64():
     case = workloads.paged_case(31, [1, 16, 17, 100, 257], 8, 2, 32, 16, BF16)
     out = oracle.paged_decode(case.q, case.k_cache, case.v_cache, case.block_tables,
                               case.context_lens, case.scale, 16, BF16, BF16)
-    qf = _f(case.q, BF16)
+    qf = _torch_widen(case.q, BF16)
     G = 4
     for i, n in enumerate(case.context_lens):
         n = int(n)
         nb = -(-n // 16)
         ids = case.block_tables[i, :nb]
         # [Hkv, nb*bs, d] -> library attention with grouped heads
-        K = torch.from_numpy(_f(case.k_cache[ids], BF16)).permute(1, 0, 2, 3).reshape(2, -1, 32)[:, :n]
-        V = torch.from_numpy(_f(case.v_cache[ids], BF16)).permute(1, 0, 2, 3).reshape(2, -1, 32)[:, :n]
+        # inputs widened by torch itself, so this pin does not lean on bits_to_f64
+        K = torch.from_numpy(_torch_widen(case.k_cache[ids], BF16)).permute(1, 0, 2, 3).reshape(2, -1, 32)[:, :n]
+        V = torch.from_numpy(_torch_widen(case.v_cache[ids], BF16)).permute(1, 0, 2, 3).reshape(2, -1, 32)[:, :n]
         K = K.repeat_interleave(G, dim=0)
         V = V.repeat_interleave(G, dim=0)
         Q = torch.from_numpy(qf[i]).unsqueeze(1)  # [Hq, 1, d]

@@ -63,6 +63,8 @@ typedef enum {
 #define PA_DEVERR_CONTEXT_RANGE 0x4 /* context length above max_context_len or the table width */
 #define PA_DEVERR_TIMEOUT 0x8       /* a kernel gave up waiting for its own data copies (1 s) */
 #define PA_DEVERR_LAYOUT 0x10       /* a kernel found its shared memory misaligned; nothing computed */
+#define PA_DEVERR_QUERY_START 0x20  /* pa_prefill: query_start outside [0, num_tokens] or decreasing; clamped */
+#define PA_DEVERR_Q_RANGE 0x40      /* pa_decode, 8-bit KV: a q value beyond the f16 range (|q| > 65504) */
 
 /* Library version, major*10000 + minor*100 + patch. */
 int pa_version(void);
@@ -131,6 +133,19 @@ pa_status pa_reshape_and_cache(const void* key, const void* value, void* k_cache
  * 256-byte aligned; with partition_size = 0 and a smaller or NULL workspace
  * the library uses a schedule that needs none.
  *
+ * With an 8-bit cache the tensor-core path multiplies q, converted to f16,
+ * with the codes widened to f16: a q value beyond the f16 range (|q| > 65504)
+ * becomes infinite, which the kernel reports with PA_DEVERR_Q_RANGE.
+ *
+ * Calls that overlap on the GPU: with partition_size = 0 and a workspace,
+ * each call takes one of 256 work counters inside the library, in turn, and
+ * its last kernel sets it back to zero. Calls on one stream never overlap.
+ * Two calls that run at the same time on the GPU (on different streams or
+ * from several threads) share a counter when they were issued a multiple of
+ * 256 calls apart, and every replay of a captured graph uses the counter its
+ * capture took; calls sharing a counter must not overlap (the caller
+ * serialises them), or work is skipped or done twice with no error flagged.
+ *
  * Supported: num_heads / num_kv_heads in {1, 2, 4, 8}; head_dim in {64, 128,
  * 256}; block_size in {8, 16, 32, 64}.
  */
@@ -196,7 +211,10 @@ pa_status pa_copy_blocks(void* const* k_caches, void* const* v_caches,
  * q, out: DEVICE [num_tokens, num_heads, head_dim] of `dtype`, 16-byte
  * aligned; caches as for pa_decode, same dtype; block_tables, context_lens,
  * query_start (int32 [num_seqs + 1], non-decreasing, query_start[0] = 0,
- * query_start[num_seqs] = num_tokens): DEVICE. max_query_len bounds n_i (it
+ * query_start[num_seqs] = num_tokens): DEVICE. Entries outside [0,
+ * num_tokens], or smaller than the entry before, are clamped into that range
+ * (so no row outside q and out is read or written) and set
+ * PA_DEVERR_QUERY_START. max_query_len bounds n_i (it
  * sizes the grid; chunks beyond it are not computed). Sequences whose
  * context is shorter than their chunk, or longer than the table holds, set
  * PA_DEVERR_CONTEXT_RANGE; table entries outside [0, num_blocks) set

@@ -18,6 +18,8 @@ DEVERR_BLOCK_RANGE = 0x2
 DEVERR_CONTEXT_RANGE = 0x4
 DEVERR_TIMEOUT = 0x8
 DEVERR_LAYOUT = 0x10
+DEVERR_QUERY_START = 0x20
+DEVERR_Q_RANGE = 0x40
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libpa.so")
@@ -113,6 +115,24 @@ def _check(status, what):
         raise PaError(status, what)
 
 
+def _on_device(what, **tensors):
+    """Every given tensor (None is skipped) must be a dense, contiguous CUDA
+    tensor on one device: the C ABI takes raw pointers and assumes exactly
+    that layout, so a strided view or a host tensor would be misread."""
+    device = None
+    for name, t in tensors.items():
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError(f"{what}: {name} must be a CUDA tensor (got {t.device})")
+        if not t.is_contiguous():
+            raise ValueError(f"{what}: {name} must be contiguous")
+        if device is None:
+            device = t.device
+        elif t.device != device:
+            raise ValueError(f"{what}: {name} is on {t.device}, other tensors on {device}")
+
+
 def reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, k_scale=None, v_scale=None,
                       debug_err=None, stream=None):
     """Write new tokens' K/V ([T, Hkv, d]) into the caches ([Nb, Hkv, bs, d]) at their slots."""
@@ -122,6 +142,8 @@ def reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, k_scale=None, 
         raise ValueError("shape mismatch between new tokens and caches")
     if slot_mapping.dtype != torch.int64 or slot_mapping.numel() != T:
         raise ValueError("slot_mapping must be int64 [num_tokens]")
+    _on_device("reshape_and_cache", key=key, value=value, k_cache=k_cache, v_cache=v_cache,
+               slot_mapping=slot_mapping, k_scale=k_scale, v_scale=v_scale, debug_err=debug_err)
     _check(lib().pa_reshape_and_cache(
         _ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping), T, Hkv, d, bs,
         Nb, _dtype_code(key.dtype), _dtype_code(k_cache.dtype), _ptr(k_scale), _ptr(v_scale),
@@ -146,6 +168,9 @@ def decode(out, q, k_cache, v_cache, block_tables, context_lens, scale, max_cont
         raise ValueError("block_tables and context_lens must be int32")
     if block_tables.dim() != 2 or block_tables.shape[0] != B or context_lens.numel() != B:
         raise ValueError("block_tables must be [num_seqs, max_blocks]; context_lens [num_seqs]")
+    _on_device("decode", out=out, q=q, k_cache=k_cache, v_cache=v_cache, block_tables=block_tables,
+               context_lens=context_lens, k_scale=k_scale, v_scale=v_scale, workspace=workspace,
+               debug_err=debug_err)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().pa_decode(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
@@ -170,6 +195,8 @@ def prefill(out, q, k_cache, v_cache, block_tables, context_lens, query_start, s
     B = context_lens.numel()
     if query_start.numel() != B + 1 or block_tables.dim() != 2 or block_tables.shape[0] != B:
         raise ValueError("query_start must be [num_seqs + 1]; block_tables [num_seqs, width]")
+    _on_device("prefill", out=out, q=q, k_cache=k_cache, v_cache=v_cache, block_tables=block_tables,
+               context_lens=context_lens, query_start=query_start, debug_err=debug_err)
     _check(lib().pa_prefill(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
         _ptr(context_lens), _ptr(query_start), B, T, int(max_query_len), Hq, Hkv, d, bs, Nb,
@@ -190,6 +217,11 @@ def decode_split_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, s
         raise ValueError("shape mismatch")
     if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
         raise ValueError("block_tables and context_lens must be int32")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or context_lens.numel() != B:
+        raise ValueError("block_tables must be [num_seqs, max_blocks]; context_lens [num_seqs]")
+    _on_device("decode_split_noalloc", out=out, q=q, k_cache=k_cache, v_cache=v_cache,
+               block_tables=block_tables, context_lens=context_lens, k_scale=k_scale,
+               v_scale=v_scale, debug_err=debug_err)
     _check(lib().pa_decode_split_noalloc(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
         block_tables.shape[1], _ptr(context_lens), B, Hq, Hkv, d, bs, Nb, float(scale),
@@ -208,6 +240,10 @@ def copy_blocks(k_ptrs, v_ptrs, block_mapping, num_blocks, block_bytes, debug_er
     """Copy blocks (src, dst) = block_mapping[p] in every layer; *_ptrs from pointer_array."""
     if block_mapping.dtype != torch.int64 or block_mapping.dim() != 2 or block_mapping.shape[1] != 2:
         raise ValueError("block_mapping must be int64 [num_pairs, 2]")
+    if k_ptrs.dtype != torch.int64 or v_ptrs.dtype != torch.int64 or k_ptrs.numel() != v_ptrs.numel():
+        raise ValueError("k_ptrs and v_ptrs must be int64 pointer arrays of one entry per layer")
+    _on_device("copy_blocks", k_ptrs=k_ptrs, v_ptrs=v_ptrs, block_mapping=block_mapping,
+               debug_err=debug_err)
     _check(lib().pa_copy_blocks(
         _ptr(k_ptrs), _ptr(v_ptrs), k_ptrs.numel(), _ptr(block_mapping), block_mapping.shape[0],
         int(num_blocks), int(block_bytes), _ptr(debug_err), _stream(stream)), "pa_copy_blocks")

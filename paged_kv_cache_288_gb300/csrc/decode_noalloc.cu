@@ -70,7 +70,17 @@ pa_status pa_decode_split_noalloc(void* out, const void* q, const void* k_cache,
                                   const float* k_scale, const float* v_scale,
                                   int32_t max_context_len, int32_t partition_size,
                                   int32_t* debug_err, cudaStream_t stream) {
-  if (partition_size <= 0) partition_size = 512;
+  if (partition_size < 0) {
+    pa::set_last_error("partition_size < 0");
+    return PA_ERR_INVALID;
+  }
+  if (partition_size == 0) partition_size = 512;
+  // the arguments first, so a bad one is reported as such and not as a size
+  const pa_status v = pa::validate_decode_args(
+      out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+      num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, q_dtype, kv_dtype,
+      k_scale, v_scale, max_context_len, partition_size);
+  if (v != PA_OK || num_seqs == 0) return v;
   const size_t need = pa_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim,
                                                max_context_len, partition_size);
   if (need > kScratchBytes) {

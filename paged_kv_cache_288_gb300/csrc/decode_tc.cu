@@ -409,6 +409,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
         load_float<QT, 4>(qrow + 16 * k + 4 * tig, f);
         qb[k][0] = pack_f16(f[0], f[1]);
         qb[k][1] = pack_f16(f[2], f[3]);
+        // beyond the f16 range q turns infinite: report it
+        if (fmaxf(fmaxf(fabsf(f[0]), fabsf(f[1])), fmaxf(fabsf(f[2]), fabsf(f[3]))) > 65504.f)
+          flag_error(p.debug_err, PA_DEVERR_Q_RANGE);
       }
     }
   };

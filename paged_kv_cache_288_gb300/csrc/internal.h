@@ -33,6 +33,17 @@ inline cudaError_t set_smem_limit_once(const void* fn, int bytes, std::atomic<un
 // Sets the message pa_last_error_message() returns on this thread.
 void set_last_error(const char* fmt, ...);
 
+// Host-side checks of pa_decode's arguments other than the workspace:
+// PA_OK, or the status pa_decode returns for them (message set).
+pa_status validate_decode_args(const void* out, const void* q, const void* k_cache,
+                               const void* v_cache, const int32_t* block_tables,
+                               int32_t max_blocks_per_seq, const int32_t* context_lens,
+                               int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                               int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                               float scale, pa_dtype q_dtype, pa_dtype kv_dtype,
+                               const float* k_scale, const float* v_scale,
+                               int32_t max_context_len, int32_t partition_size);
+
 cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* k_cache,
                                      void* v_cache, const int64_t* slot_mapping, int num_tokens,
                                      int num_kv_heads, int head_dim, int block_size, int num_blocks,

@@ -146,14 +146,20 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t num
   return need;
 }
 
-pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
-                    const int32_t* block_tables, int32_t max_blocks_per_seq,
-                    const int32_t* context_lens, int32_t num_seqs, int32_t num_heads,
-                    int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
-                    int32_t num_blocks, float scale, pa_dtype q_dtype, pa_dtype kv_dtype,
-                    const float* k_scale, const float* v_scale, int32_t max_context_len,
-                    int32_t partition_size, void* workspace, size_t workspace_bytes,
-                    int32_t* debug_err, cudaStream_t stream) {
+}  // extern "C"
+
+namespace pa {
+
+// The host-side checks of pa_decode's arguments (everything but the
+// workspace), shared with pa_decode_split_noalloc.
+pa_status validate_decode_args(const void* out, const void* q, const void* k_cache,
+                               const void* v_cache, const int32_t* block_tables,
+                               int32_t max_blocks_per_seq, const int32_t* context_lens,
+                               int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                               int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                               float scale, pa_dtype q_dtype, pa_dtype kv_dtype,
+                               const float* k_scale, const float* v_scale,
+                               int32_t max_context_len, int32_t partition_size) {
   if (num_seqs < 0) return fail(PA_ERR_INVALID, "num_seqs < 0");
   if (num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
       num_blocks <= 0 || max_blocks_per_seq <= 0)
@@ -186,6 +192,26 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
     return fail(PA_ERR_INVALID, "null tensor pointer");
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
     return fail(PA_ERR_INVALID, "tensor pointers must be 16-byte aligned");
+  return PA_OK;
+}
+
+}  // namespace pa
+
+extern "C" {
+
+pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* block_tables, int32_t max_blocks_per_seq,
+                    const int32_t* context_lens, int32_t num_seqs, int32_t num_heads,
+                    int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                    int32_t num_blocks, float scale, pa_dtype q_dtype, pa_dtype kv_dtype,
+                    const float* k_scale, const float* v_scale, int32_t max_context_len,
+                    int32_t partition_size, void* workspace, size_t workspace_bytes,
+                    int32_t* debug_err, cudaStream_t stream) {
+  const pa_status v = pa::validate_decode_args(
+      out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+      num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, q_dtype, kv_dtype,
+      k_scale, v_scale, max_context_len, partition_size);
+  if (v != PA_OK || num_seqs == 0) return v;
   if (workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return fail(PA_ERR_INVALID, "workspace must be 256-byte aligned");
 

@@ -88,6 +88,7 @@ struct PfParams {
   const int32_t* query_start;
   int32_t* debug_err;
   int max_blocks_per_seq;
+  int num_tokens;
   int num_heads;
   int num_kv_heads;
   int block_size;
@@ -96,6 +97,19 @@ struct PfParams {
   int tokens_per_tile;
   float scale_log2;
 };
+
+// Rows [q0, q0 + n) of q and out that hold sequence i's queries, from
+// query_start clamped into [0, num_tokens] (an entry below the one before it
+// counts as that one), so no row outside q and out is ever addressed.
+// Returns true when query_start had to be clamped.
+__device__ __forceinline__ bool query_rows(const PfParams& p, int i, int& q0, int& n) {
+  const int a = p.query_start[i], b = p.query_start[i + 1];
+  const int lo = min(max(a, 0), p.num_tokens);
+  const int hi = min(max(b, lo), p.num_tokens);
+  q0 = lo;
+  n = hi - lo;
+  return a != lo || b != hi;
+}
 
 template <typename T>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi);
@@ -194,7 +208,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     int& s_seq = *reinterpret_cast<int*>(sm + kGroups * kTile + kRankMaxSeqs * 8);
     const int nseq = gridDim.z;
     for (int i = threadIdx.x; i < nseq; i += blockDim.x) {
-      const int ni = p.query_start[i + 1] - p.query_start[i], ci = p.context_lens[i];
+      int qi, ni;
+      query_rows(p, i, qi, ni);
+      const int ci = p.context_lens[i];
       w[i] = (ni > 0 && ci >= ni) ? static_cast<unsigned long long>(ni) * (2ull * ci - ni) : 0ull;
     }
     __syncthreads();
@@ -211,8 +227,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     __syncthreads();
     seq = s_seq;
   }
-  const int q0 = p.query_start[seq];
-  const int n = p.query_start[seq + 1] - q0;
+  int q0, n;
+  if (query_rows(p, seq, q0, n) && threadIdx.x == 0)
+    flag_error(p.debug_err, PA_DEVERR_QUERY_START);
   const int G = p.group, TQ = p.tokens_per_tile;
   const int t0 = pair * kGroups * TQ;  // first query of the CTA's two tiles
   if (t0 >= n) return;                 // CTA-uniform, before any TMEM is held
@@ -623,6 +640,7 @@ cudaError_t launch_prefill_tc(void* out, const void* q, const void* k_cache, con
   pp.query_start = query_start;
   pp.debug_err = debug_err;
   pp.max_blocks_per_seq = max_blocks_per_seq;
+  pp.num_tokens = num_tokens;
   pp.num_heads = num_heads;
   pp.num_kv_heads = num_kv_heads;
   pp.block_size = block_size;

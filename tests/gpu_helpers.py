@@ -1,9 +1,12 @@
 """Helpers for the GPU parity tests: move a seeded case to the device, run
 the library through its binding, and compare with the oracle.
 
-Tolerances (element-wise, allclose form |gpu - ref| <= atol + rtol * |ref|):
-16-bit KV: atol 2e-3, rtol 1e-2; 8-bit KV: atol 3e-2, rtol 1e-2, against the
-oracle run on the same stored E4M3 codes.
+Tolerances, element-wise:
+16-bit KV: the allclose form |gpu - ref| <= 2e-3 + 1e-2 * |ref| (the literal
+2e-3 alone fails for bf16 outputs of magnitude >= 0.5, whose half ulp is
+2^-9); 8-bit KV: the literal |gpu - ref| <= 3e-2, against the oracle run on
+the same stored E4M3 codes. For inputs drawn with a smaller spread than
+N(0, 1) the 8-bit bound scales with the largest |V| (``value_scale``).
 """
 
 import numpy as np
@@ -15,7 +18,6 @@ import workloads
 ATOL_16 = 2e-3
 RTOL_16 = 1e-2
 ATOL_FP8 = 3e-2
-RTOL_FP8 = 1e-2
 
 _TORCH = {workloads.F16: torch.float16, workloads.BF16: torch.bfloat16,
           workloads.FP8_E4M3: torch.uint8}
@@ -95,10 +97,10 @@ def oracle_decode(case, k_cache=None, v_cache=None, context_lens=None, q=None):
         case.scale, case.block_size, case.q_dtype, case.kv_dtype, case.k_scale, case.v_scale)
 
 
-def assert_close(got_t, ref, dtype_out, kv_dtype, what=""):
+def assert_close(got_t, ref, dtype_out, kv_dtype, what="", value_scale=1.0):
     got = to_f64(got_t, dtype_out)
     if kv_dtype == workloads.FP8_E4M3:
-        atol, rtol = ATOL_FP8, RTOL_FP8
+        atol, rtol = ATOL_FP8 * value_scale, 0.0
     else:
         atol, rtol = ATOL_16, RTOL_16
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"

@@ -173,3 +173,49 @@ def _prefill(L, **kw):
 ])
 def test_prefill_argument_checks(L, kw, status):
     assert _prefill(L, **kw) == status, pa.lib().pa_last_error_message()
+
+
+def _noalloc(L, **kw):
+    args = dict(out=16, q=16, k=16, v=16, tables=16, width=1024, lens=16, B=256, Hq=64, Hkv=8,
+                d=128, bs=16, Nb=100, scale=0.1, qt=pa.BF16, kvt=pa.BF16, maxctx=16384, part=512,
+                err=NULL, stream=NULL)
+    args.update(kw)
+    return L.pa_decode_split_noalloc(
+        args["out"], args["q"], args["k"], args["v"], args["tables"], args["width"], args["lens"],
+        args["B"], args["Hq"], args["Hkv"], args["d"], args["bs"], args["Nb"], args["scale"],
+        args["qt"], args["kvt"], NULL, NULL, args["maxctx"], args["part"], args["err"],
+        args["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(part=-16), 1),                   # negative partition size: invalid, not 512
+    (dict(Hq=6, Hkv=4), 1),                # a bad argument is reported before the size
+    (dict(d=100), 1),
+    (dict(bs=12, part=48, maxctx=12000), 2),
+    (dict(out=NULL), 1),
+    (dict(), 4),                           # valid, but the partials exceed the scratch
+    (dict(B=0), 0),                        # nothing to do
+])
+def test_noalloc_argument_checks(L, kw, status):
+    assert _noalloc(L, **kw) == status, pa.lib().pa_last_error_message()
+
+
+def test_binding_refuses_host_tensors():
+    """The binding hands raw pointers to the C ABI, so it refuses tensors the
+    kernels could not read as dense device memory (before loading anything)."""
+    import torch
+    q = torch.zeros(2, 8, 64, dtype=torch.float16)
+    kc = torch.zeros(4, 2, 16, 64, dtype=torch.float16)
+    tables = torch.zeros(2, 4, dtype=torch.int32)
+    lens = torch.ones(2, dtype=torch.int32)
+    with pytest.raises(ValueError, match="out must be a CUDA tensor"):
+        pa.decode(torch.empty_like(q), q, kc, kc, tables, lens, 0.1, 16)
+    key = torch.zeros(3, 2, 64, dtype=torch.float16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        pa.reshape_and_cache(key, key, kc, kc, torch.zeros(3, dtype=torch.int64))
+    qs = torch.tensor([0, 1, 2], dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        pa.prefill(torch.empty_like(q), q, kc, kc, tables, lens, qs, 0.1, 1)
+    ptrs = torch.zeros(1, dtype=torch.int64)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        pa.copy_blocks(ptrs, ptrs, torch.zeros(1, 2, dtype=torch.int64), 4, 4096)

@@ -86,5 +86,6 @@ def test_fp8_step_layer(layer):
     assert np.array_equal(host_bits(dc.k_cache), kc)
     assert np.array_equal(host_bits(dc.v_cache), vc)
     ref = oracle_decode(case, k_cache=kc, v_cache=vc)
-    assert_close(out, ref, BF16, FP8_E4M3, f"fp8 layer {layer}")
+    max_abs, _ = assert_close(out, ref, BF16, FP8_E4M3, f"fp8 layer {layer}")
+    assert max_abs <= 3e-2, max_abs  # the literal bound for the 8-bit KV workload
     assert dc.debug_err.item() == 0

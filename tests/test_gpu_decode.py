@@ -215,9 +215,58 @@ def test_fp8_kv_decode(q_dtype, bs):
         out = run_decode(pa, dc, partition_size=part)
         ref = oracle_decode(case, k_cache=kc, v_cache=vc)
         torch.cuda.synchronize()
-        assert_close(out, ref, q_dtype, FP8_E4M3, f"fp8 part={part}")
+        max_abs, _ = assert_close(out, ref, q_dtype, FP8_E4M3, f"fp8 part={part}")
+        assert max_abs <= 3e-2, max_abs
     assert dc.debug_err.item() == 0
     assert np.array_equal(host_bits(dc.k_cache), kc)
+
+
+def test_fp8_q_beyond_f16_range_is_flagged():
+    """With an 8-bit cache q is multiplied in f16: a bf16 q value above 65504
+    has no f16 counterpart, and the call reports it through debug_err."""
+    case = workloads.fp8_layer(860, [40, 70], num_heads=8, num_kv_heads=2, head_dim=128,
+                               block_size=16, src_dtype=BF16, name="fp8_big_q")
+    dc = DeviceCase(case)
+    pa.reshape_and_cache(dc.new_key, dc.new_value, dc.k_cache, dc.v_cache, dc.slot_mapping,
+                         k_scale=dc.k_scale, v_scale=dc.v_scale, debug_err=dc.debug_err)
+    run_decode(pa, dc)
+    torch.cuda.synchronize()
+    assert dc.debug_err.item() == 0
+    q = dc.q.clone()
+    q[1, 3, 17] = 1.0e5
+    run_decode(pa, dc, q=q)
+    torch.cuda.synchronize()
+    assert dc.debug_err.item() & pa.DEVERR_Q_RANGE
+
+
+@pytest.mark.parametrize("v_sigma,k_sigma", [(0.0125, 1.0), (0.0125, 0.0125), (1e-3, 1.0)])
+def test_fp8_kv_decode_small_value_scales(v_sigma, k_sigma):
+    """E4M3 caches of activations much smaller than N(0, 1): V drawn with
+    sigma 0.0125 (amax about 0.05, V scales about 1e-4) or 1e-3, and K either
+    N(0, 1) or as small as V (so the weights are nearly uniform). The kernel
+    folds each block's V scale into the softmax weights before they are
+    rounded to f16, where such small products are f16 subnormals; the error
+    that adds must stay within the 8-bit bound scaled to the size of V
+    (3e-2 * amax|V| / 4, i.e. the N(0, 1) bound times sigma)."""
+    lengths = [1, 16, 100, 777, 2048]
+    case = workloads.fp8_layer(850, lengths, num_heads=32, num_kv_heads=8, head_dim=128,
+                               block_size=16, src_dtype=BF16, name="fp8_small_v",
+                               k_sigma=k_sigma, v_sigma=v_sigma)
+    dc = DeviceCase(case)
+    pa.reshape_and_cache(dc.new_key, dc.new_value, dc.k_cache, dc.v_cache, dc.slot_mapping,
+                         k_scale=dc.k_scale, v_scale=dc.v_scale, debug_err=dc.debug_err)
+    kc, vc = case.k_cache.copy(), case.v_cache.copy()
+    oracle.reshape_and_cache(case.new_key, case.new_value, kc, vc, case.slot_mapping, 16, BF16,
+                             FP8_E4M3, case.k_scale, case.v_scale)
+    ref = oracle_decode(case, k_cache=kc, v_cache=vc)
+    for part in (0, 512):
+        out = run_decode(pa, dc, partition_size=part)
+        torch.cuda.synchronize()
+        max_abs, _ = assert_close(out, ref, BF16, FP8_E4M3, f"fp8 small v part={part}",
+                                  value_scale=v_sigma)
+        # relative to the output's own size the error stays small as well
+        assert max_abs <= 1e-2 * np.abs(ref).max() + 2.0 ** -8 * np.abs(ref).max(), max_abs
+    assert dc.debug_err.item() == 0
 
 
 @pytest.mark.parametrize("group", [2, 4, 8])
@@ -228,3 +277,18 @@ def test_merges_of_few_and_many_ranges_in_one_batch(group):
     lengths = [32768, 2000, 100, 1]
     case = workloads.paged_case(700 + group, lengths, group * 4, 4, 128, 16, BF16, name=f"merges{group}")
     _check(case)
+
+
+def test_binding_refuses_strided_views():
+    """A strided view passes a pointer whose rows are not where the kernels
+    look: the binding refuses it instead of letting the call misread memory."""
+    case = workloads.paged_case(870, [20, 33], 8, 2, 64, 16, F16)
+    dc = DeviceCase(case)
+    q2 = torch.cat([dc.q, dc.q], dim=2)[:, :, ::2]  # right shape, not contiguous
+    assert q2.shape == dc.q.shape and not q2.is_contiguous()
+    with pytest.raises(ValueError, match="contiguous"):
+        pa.decode(torch.empty_like(dc.q), q2, dc.k_cache, dc.v_cache, dc.block_tables,
+                  dc.context_lens, case.scale, case.max_context_len)
+    with pytest.raises(ValueError, match="contiguous"):
+        pa.decode(torch.empty_like(dc.q), dc.q, dc.k_cache, dc.v_cache, dc.block_tables.t().contiguous().t(),
+                  dc.context_lens, case.scale, case.max_context_len)

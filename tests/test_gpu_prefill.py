@@ -114,6 +114,29 @@ def test_prefill_flags_contexts_shorter_than_the_chunk():
     _check(out, ref, case, "the valid sequence", rows=slice(0, q1))
 
 
+def test_prefill_clamps_query_start_past_num_tokens():
+    """query_start entries beyond num_tokens are clamped by the kernel and
+    flagged: q and out are views of the first T rows of buffers with 8 guard
+    rows after them, the last sequence's query_start claims those 8 rows too,
+    and the guard rows of out must stay untouched (NaN) while the rows in
+    range still match the oracle. The guard rows exist, so even a missing
+    clamp would stay inside the allocation."""
+    case = workloads.prefill_case(73, [20, 5], [10, 12], 8, 2, 128, 16, BF16)
+    T = case.q.shape[0]
+    q_all = dev(np.concatenate([case.q, case.q[:8]]), BF16)
+    out_all = torch.full_like(q_all, float("nan"))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    qs = case.query_start.copy()
+    qs[-1] = T + 8  # past num_tokens = T
+    pa.prefill(out_all[:T], q_all[:T], dev(case.k_cache, BF16), dev(case.v_cache, BF16),
+               torch.from_numpy(case.block_tables).cuda(), torch.from_numpy(case.context_lens).cuda(),
+               torch.from_numpy(qs).cuda(), case.scale, int(np.diff(qs).max()), debug_err=err)
+    torch.cuda.synchronize()
+    assert err.item() & pa.DEVERR_QUERY_START
+    assert torch.isnan(out_all[T:].float()).all(), "a guard row past num_tokens was written"
+    _check(out_all[:T], _oracle(case), case, "clamped query_start")
+
+
 @pytest.mark.parametrize("num_seqs", [9, 260])
 def test_prefill_work_order_covers_every_sequence(num_seqs):
     """CTAs take the heaviest sequences first (by n (2 ctx - n)) when the batch

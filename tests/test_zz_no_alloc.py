@@ -6,9 +6,10 @@ memory is fixed at start-up), so they cannot provide the workspace that
 pa_decode's split path needs. pa_decode_split_noalloc keeps those partials in
 a scratch array built into the library instead. This test calls it through
 the C ABI twice in a row, on two different problems, and checks each result
-against pa_decode with a caller-allocated workspace, within the tolerance of
-the other decode tests. It also checks that sizes beyond the built-in
-scratch are refused.
+against the fp64 oracle and against pa_decode with a caller-allocated
+workspace, within the tolerance of the other decode tests (the output starts
+as NaN, so a row the call leaves unwritten fails). It also checks that sizes
+beyond the built-in scratch are refused.
 
 The file name sorts last so that a run stopping at the first failure has run
 every other test first; the test also passes on its own in a fresh process.
@@ -21,7 +22,7 @@ import torch
 
 import workloads
 from workloads import BF16, F16
-from gpu_helpers import DeviceCase, assert_close, to_f64
+from gpu_helpers import DeviceCase, assert_close, oracle_decode, to_f64
 import paged_kv_cache_288_gb300 as pa
 
 pytestmark = pytest.mark.gpu
@@ -69,6 +70,7 @@ def test_noalloc_matches_workspace_decode_on_two_calls_in_a_row():
         ref = _with_workspace(dc, part)
         torch.cuda.synchronize()
         assert dc.debug_err.item() == 0
+        assert_close(got, oracle_decode(case), case.q_dtype, case.kv_dtype, case.name + " vs oracle")
         assert_close(got, to_f64(ref, case.q_dtype), case.q_dtype, case.kv_dtype, case.name)
 
 

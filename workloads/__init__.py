@@ -55,13 +55,17 @@ def _gen(seed):
     return g
 
 
-def normal_bits(g, shape, dtype, chunk=1 << 24):
-    """N(0,1) values rounded to f16/bf16, returned as raw uint16 bits."""
+def normal_bits(g, shape, dtype, chunk=1 << 24, sigma=1.0):
+    """N(0, sigma^2) values rounded to f16/bf16, returned as raw uint16 bits
+    (sigma = 1 leaves the N(0,1) draws unchanged)."""
     n = int(np.prod(shape)) if len(shape) else 1
     out = np.empty(n, dtype=np.uint16)
     for start in range(0, n, chunk):
         m = min(chunk, n - start)
-        x = torch.randn(m, generator=g, dtype=torch.float32).to(_TORCH_16[dtype])
+        x = torch.randn(m, generator=g, dtype=torch.float32)
+        if sigma != 1.0:
+            x = x * float(sigma)
+        x = x.to(_TORCH_16[dtype])
         out[start:start + m] = x.view(torch.int16).numpy().view(np.uint16)
     return out.reshape(shape)
 
@@ -331,13 +335,15 @@ def fp8_lengths(seed=1005, num_seqs=256, mean=500.0, sigma=1.0, lo=16, hi=2048):
 
 
 def fp8_layer(seed, context_lens, num_heads=32, num_kv_heads=8, head_dim=128,
-              block_size=16, src_dtype=BF16, pool_factor=1.25, name="fp8_layer"):
+              block_size=16, src_dtype=BF16, pool_factor=1.25, name="fp8_layer",
+              k_sigma=1.0, v_sigma=1.0):
     """One layer of an E4M3 KV cache, to be filled by cache writes.
 
     Every token of every sequence is a new token (bf16 N(0,1) key and value
-    plus its slot); the pool starts as NaN poison. Each (block, KV head) gets
-    the scale amax/448 over the values that will be written into it (1.0 when
-    that amax is 0), fixed before any write, as a caller would choose it.
+    plus its slot, or N(0, k_sigma^2) / N(0, v_sigma^2) when given); the pool
+    starts as NaN poison. Each (block, KV head) gets the scale amax/448 over
+    the values that will be written into it (1.0 when that amax is 0), fixed
+    before any write, as a caller would choose it.
     """
     g = _gen(seed)
     bs = block_size
@@ -348,8 +354,8 @@ def fp8_layer(seed, context_lens, num_heads=32, num_kv_heads=8, head_dim=128,
     poison = int(torch.randint(num_blocks, (1,), generator=g).item())
     tables, _ = _assign_tables(g, nbs, num_blocks, max(max(nbs), 1), poison)
     T = int(ctx.sum())
-    key = normal_bits(g, (T, num_kv_heads, head_dim), src_dtype)
-    value = normal_bits(g, (T, num_kv_heads, head_dim), src_dtype)
+    key = normal_bits(g, (T, num_kv_heads, head_dim), src_dtype, sigma=k_sigma)
+    value = normal_bits(g, (T, num_kv_heads, head_dim), src_dtype, sigma=v_sigma)
     seq_of = np.repeat(np.arange(len(ctx)), ctx)
     pos = np.concatenate([np.arange(c) for c in ctx]) if T else np.zeros(0, np.int64)
     blk = tables[seq_of, pos // bs].astype(np.int64)

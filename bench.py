@@ -90,7 +90,7 @@ def make_case(name, rank):
     if name.startswith("long_context"):
         bs = int(name.split("bs")[-1]) if "bs" in name else 16
         return workloads.long_context(bs, seed=rank_seed(1004, rank))
-    if name == "fp8_layer":
+    if name in ("fp8_layer", "fp8_step"):
         return workloads.fp8_step_layer(0, seed=rank_seed(1005, rank))
     if name == "prefix_cache":
         return prefix_cache_case(rank_seed(1007, rank))
@@ -373,49 +373,109 @@ def max_over_ranks(x, world, device):
     return float(t.item())
 
 
-def run_ours(args, world, rank, local):
-    import paged_kv_cache_288_gb300 as pa
-    from paged_kv_cache_288_gb300 import build
+def peak_hbm():
+    """(GB/s, source) of the roofline denominator."""
+    peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(peaks_path):
+        return json.load(open(peaks_path))["hbm_gbs"], "measured"
+    return 6800.0, "fallback"
 
-    build.build_library()
-    device = torch.device("cuda", local)
-    torch.cuda.set_device(device)
-    case = make_case(args.workload, rank)
 
-    def to_dev(bits, dtype):
-        a = np.ascontiguousarray(bits)
-        if dtype == workloads.FP8_E4M3:
-            return torch.from_numpy(a.view(np.uint8)).to(device)
-        t = torch.from_numpy(a.view(np.int16)).to(device)
-        return t.view(torch.float16 if dtype == workloads.F16 else torch.bfloat16)
+def unique_decode_bytes(case):
+    """Algorithmic bytes of one pa_decode counting each physical block's KV
+    once: a block that several tables share (a common prefix) need come from
+    HBM only once, so this is the call's HBM floor. Table entries are still
+    counted per sequence."""
+    bs = case.block_size
+    used = {}
+    nb_total = 0
+    for i, c in enumerate(case.context_lens):
+        c = int(c)
+        nb = -(-c // bs) if c > 0 else 0
+        nb_total += nb
+        for j in range(nb):
+            b = int(case.block_tables[i, j])
+            used[b] = max(used.get(b, 0), min(bs, c - j * bs))
+    eb = elem(case.kv_dtype)
+    kv = sum(used.values()) * case.num_kv_heads * 2 * case.head_dim * eb
+    scales = len(used) * case.num_kv_heads * 2 * 4 if case.kv_dtype == workloads.FP8_E4M3 else 0
+    qo = 2 * case.num_seqs * case.num_heads * case.head_dim * elem(case.q_dtype)
+    return kv + scales + qo + nb_total * 4 + case.num_seqs * 4
 
-    q = to_dev(case.q, case.q_dtype)
-    kc = to_dev(case.k_cache, case.kv_dtype)
-    vc = to_dev(case.v_cache, case.kv_dtype)
-    tables = torch.from_numpy(case.block_tables).to(device)
-    lens = torch.from_numpy(case.context_lens).to(device)
-    ks = torch.from_numpy(case.k_scale).to(device) if case.k_scale is not None else None
-    vs = torch.from_numpy(case.v_scale).to(device) if case.v_scale is not None else None
-    nk = to_dev(case.new_key, case.src_dtype)
-    nv = to_dev(case.new_value, case.src_dtype)
-    slots = torch.from_numpy(case.slot_mapping).to(device)
-    if case.kv_dtype == workloads.FP8_E4M3:
-        # the fp8 pool starts empty: fill it once through the library (untimed)
-        pa.reshape_and_cache(nk, nv, kc, vc, slots, k_scale=ks, v_scale=vs)
-        T = min(case.num_seqs, nk.shape[0])
-        last = np.cumsum(case.context_lens.astype(np.int64)) - 1
-        nk, nv, slots = nk[last].contiguous(), nv[last].contiguous(), slots[last].contiguous()
-        case.new_key = case.new_key[last]
-        case.new_value = case.new_value[last]
-        del T
-    out = torch.empty_like(q)
-    max_ctx = int(case.context_lens.max())
-    part = args.partition_size
-    ws_bytes = pa.decode_workspace_size(case.num_seqs, case.num_heads, case.num_kv_heads,
-                                        case.head_dim, max_ctx, part)
-    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=device)
+
+class DeviceDecode:
+    """One decode workload on the device: pool, tables, q, the step's new
+    tokens (one per sequence, written before the decode) and a workspace for
+    the chosen schedule. Setup that the workload's flow needs before its
+    steps (copy-on-write copies, the suffix or history tokens) is done once
+    here, outside any timing."""
+
+    def __init__(self, pa, case, device, part):
+        self.pa, self.case, self.part = pa, case, part
+
+        def to_dev(bits, dtype):
+            a = np.ascontiguousarray(bits)
+            if dtype == workloads.FP8_E4M3:
+                return torch.from_numpy(a.view(np.uint8)).to(device)
+            t = torch.from_numpy(a.view(np.int16)).to(device)
+            return t.view(torch.float16 if dtype == workloads.F16 else torch.bfloat16)
+
+        self.to_dev = to_dev
+        self.q = to_dev(case.q, case.q_dtype)
+        self.kc = to_dev(case.k_cache, case.kv_dtype)
+        self.vc = to_dev(case.v_cache, case.kv_dtype)
+        self.tables = torch.from_numpy(case.block_tables).to(device)
+        self.lens = torch.from_numpy(case.context_lens).to(device)
+        self.ks = torch.from_numpy(case.k_scale).to(device) if case.k_scale is not None else None
+        self.vs = torch.from_numpy(case.v_scale).to(device) if case.v_scale is not None else None
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        nk = to_dev(case.new_key, case.src_dtype)
+        nv = to_dev(case.new_value, case.src_dtype)
+        slots = torch.from_numpy(case.slot_mapping).to(device)
+        if case.cow_pairs is not None:
+            # the copy-on-write of the shared, partly filled block, once
+            block_bytes = case.num_kv_heads * case.block_size * case.head_dim * elem(case.kv_dtype)
+            pa.copy_blocks(pa.pointer_array([self.kc], device), pa.pointer_array([self.vc], device),
+                           torch.from_numpy(case.cow_pairs).to(device), case.num_blocks, block_bytes,
+                           debug_err=self.err)
+        T = nk.shape[0]
+        if T > case.num_seqs:
+            # the history (fp8: the empty pool; shared prefix: the private
+            # suffixes) is written once; a step then writes each sequence's
+            # last token again
+            pa.reshape_and_cache(nk, nv, self.kc, self.vc, slots, k_scale=self.ks, v_scale=self.vs,
+                                 debug_err=self.err)
+            last = np.cumsum(case.context_lens.astype(np.int64)) - 1
+            if case.cow_pairs is not None:
+                start = np.concatenate([[0], np.cumsum(case.context_lens.astype(np.int64)
+                                                       - int(case.meta["prefix_len"]))])
+                last = start[1:] - 1
+            idx = torch.from_numpy(last).to(device)
+            nk, nv, slots = nk[idx].contiguous(), nv[idx].contiguous(), slots[idx].contiguous()
+            case.new_key, case.new_value = case.new_key[last], case.new_value[last]
+            case.slot_mapping = case.slot_mapping[last]
+        self.nk, self.nv, self.slots = nk, nv, slots
+        self.out = torch.empty_like(self.q)
+        self.max_ctx = int(case.context_lens.max())
+        ws_bytes = pa.decode_workspace_size(case.num_seqs, case.num_heads, case.num_kv_heads,
+                                            case.head_dim, self.max_ctx, part)
+        self.ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=device)
+
+    def write(self, nk=None, nv=None, slots=None):
+        self.pa.reshape_and_cache(self.nk if nk is None else nk, self.nv if nv is None else nv,
+                                  self.kc, self.vc, self.slots if slots is None else slots,
+                                  k_scale=self.ks, v_scale=self.vs, debug_err=self.err)
+
+    def decode(self, q=None, tables=None, lens=None):
+        c = self.case
+        self.pa.decode(self.out, self.q if q is None else q, self.kc, self.vc,
+                       self.tables if tables is None else tables, self.lens if lens is None else lens,
+                       c.scale, self.max_ctx, k_scale=self.ks, v_scale=self.vs,
+                       partition_size=self.part, workspace=self.ws, debug_err=self.err)
+
+
+def make_flush(device):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
-    stream = torch.cuda.current_stream(device)
 
     def flush_l2():
         # write a buffer twice the L2 size, then read it back: the lines left in
@@ -423,52 +483,225 @@ def run_ours(args, world, rank, local):
         flush.zero_()
         flush.sum()
 
-    launches_before = pa.lib().pa_kernel_launch_count()
+    return flush_l2
 
-    def step():
-        pa.reshape_and_cache(nk, nv, kc, vc, slots, k_scale=ks, v_scale=vs)
 
-    def dec():
-        pa.decode(out, q, kc, vc, tables, lens, case.scale, max_ctx, k_scale=ks, v_scale=vs,
-                  partition_size=part, workspace=ws)
-
-    for _ in range(args.warmup):
+def time_write_decode(dd, K, W, flush_l2, stream, world=1):
+    """K timed steps (cache write, then decode) after W untimed ones; CUDA
+    events on the launching stream around both parts. Returns per-step
+    (step ms, decode ms) lists and the launches of the timed steps."""
+    for _ in range(W):
         flush_l2()
-        step()
-        dec()
+        dd.write()
+        dd.decode()
     torch.cuda.synchronize()
-
-    K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
-    sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.3)
     barrier(world)
     torch.cuda.synchronize()
-    n0 = pa.lib().pa_kernel_launch_count()
-    t0 = time.time()
+    n0 = dd.pa.lib().pa_kernel_launch_count()
     for k in range(K):
         flush_l2()
         ev[k][0].record(stream)
-        step()
+        dd.write()
         ev[k][1].record(stream)
-        dec()
+        dd.decode()
         ev[k][2].record(stream)
     torch.cuda.synchronize()
-    t1 = time.time()
     barrier(world)
+    n1 = dd.pa.lib().pa_kernel_launch_count()
+    return ([ev[k][0].elapsed_time(ev[k][2]) for k in range(K)],
+            [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)], n1 - n0)
+
+
+def decode_result(case, step_ms, dec_ms, launches, part, peak, peak_src, workload, extra=None):
+    """A per-workload bench record: decode call and step throughput and the
+    HBM roofline fraction of the decode call."""
+    K = len(step_ms)
+    dbytes = decode_bytes(case)
+    sbytes = dbytes + write_bytes(case)
+    dec_mean = statistics.mean(dec_ms)
+    step_mean = statistics.mean(step_ms)
+    achieved = dbytes / (dec_mean / 1e3) / 1e9
+    rec = {
+        "workload": workload, "partition_size": part, "steps": K,
+        "num_seqs": case.num_seqs, "num_heads": case.num_heads, "num_kv_heads": case.num_kv_heads,
+        "head_dim": case.head_dim, "block_size": case.block_size,
+        "kv_dtype": case.kv_dtype, "context_tokens": int(case.context_lens.sum()),
+        "decode_us": round(dec_mean * 1e3, 2), "step_us": round(step_mean * 1e3, 2),
+        "decode_bytes": dbytes, "step_bytes": sbytes,
+        "decode_gbs": round(achieved, 1), "step_gbs": round(sbytes / (step_mean / 1e3) / 1e9, 1),
+        "tokens_per_s_per_layer": round(case.num_seqs / (step_mean / 1e3), 1),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": recorded_traffic(workload, part),
+                     "kernel": "pa_decode (every kernel of the call)"},
+        "gpu_launches": launches,
+    }
+    if extra:
+        rec.update(extra)
+    return rec
+
+
+def run_config_suite(pa, device, stream, flush_l2, K, W, peak, peak_src):
+    """The other workloads' decode numbers, timed in the same run as the
+    headline line: the shared-prefix serving batch (logical and unique-byte
+    rooflines), the long-context batch at every block size (512-token split
+    path and the library's schedule) and the 32-layer E4M3 decode step."""
+    out = {}
+
+    def one(name, case, parts, extra_fn=None):
+        for part in parts:
+            dd = DeviceDecode(pa, case, device, part)
+            step_ms, dec_ms, launches = time_write_decode(dd, K, W, flush_l2, stream)
+            torch.cuda.synchronize()
+            if dd.err.item() != 0:
+                raise RuntimeError(f"{name}: device error word {dd.err.item():#x}")
+            extra = extra_fn(case, statistics.mean(dec_ms)) if extra_fn else None
+            out[f"{name}/p{part}"] = decode_result(case, step_ms, dec_ms, launches, part, peak, peak_src,
+                                                   name, extra)
+            del dd
+            torch.cuda.empty_cache()
+
+    def shared_extra(case, dec_ms):
+        ub = unique_decode_bytes(case)
+        a = ub / (dec_ms / 1e3) / 1e9
+        return {"unique_decode_bytes": ub, "unique_gbs": round(a, 1),
+                "roofline_unique": {"bound": "hbm", "achieved": round(a, 1), "peak": peak,
+                                    "peak_source": peak_src, "unit": "GB/s", "frac": round(a / peak, 4),
+                                    "note": "each shared block's KV counted once"}}
+
+    one("shared_prefix", workloads.shared_prefix(), [0], shared_extra)
+    for bs in (8, 16, 32, 64):
+        one(f"long_context_bs{bs}", workloads.long_context(bs), [512, 0])
+    out["fp8_step"] = run_fp8_step(pa, device, stream, flush_l2, K, W, peak, peak_src)
+    return out
+
+
+FP8_STEP_LAYERS = 32
+
+
+def run_fp8_step(pa, device, stream, flush_l2, K, W, peak, peak_src, layers=FP8_STEP_LAYERS):
+    """The full 8-bit decode step: for each of 32 layers, one
+    pa_reshape_and_cache of the new token of each of 256 sequences, then one
+    pa_decode over that layer's pool (E4M3 K/V, one float32 scale per block
+    and KV head). Every layer owns its pool; the pools hold the same history
+    (filled once from layer 0's tokens through the library, then copied on
+    the device), the block tables are shared by all layers as a model's are,
+    and q is drawn per layer."""
+    base = workloads.fp8_step_layer(0)
+    dd = DeviceDecode(pa, base, device, 0)
+    case = dd.case
+    g = workloads._gen(4242)
+    pools = [(dd.kc, dd.vc)] + [(dd.kc.clone(), dd.vc.clone()) for _ in range(layers - 1)]
+    qs = [dd.q] + [dd.to_dev(workloads.normal_bits(g, case.q.shape, case.q_dtype), case.q_dtype)
+                   for _ in range(layers - 1)]
+
+    def step():
+        for l in range(layers):
+            dd.kc, dd.vc = pools[l]
+            dd.write()
+            dd.decode(q=qs[l])
+
+    for _ in range(W):
+        flush_l2()
+        step()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * layers + 1)] for _ in range(K)]
+    n0 = pa.lib().pa_kernel_launch_count()
+    for k in range(K):
+        flush_l2()
+        ev[k][0].record(stream)
+        for l in range(layers):
+            dd.kc, dd.vc = pools[l]
+            dd.write()
+            ev[k][2 * l + 1].record(stream)
+            dd.decode(q=qs[l])
+            ev[k][2 * l + 2].record(stream)
+    torch.cuda.synchronize()
     n1 = pa.lib().pa_kernel_launch_count()
+    if dd.err.item() != 0:
+        raise RuntimeError(f"fp8 step: device error word {dd.err.item():#x}")
+    step_ms = [ev[k][0].elapsed_time(ev[k][2 * layers]) for k in range(K)]
+    dec_ms = [sum(ev[k][2 * l + 1].elapsed_time(ev[k][2 * l + 2]) for l in range(layers)) for k in range(K)]
+    dbytes = layers * decode_bytes(case)
+    sbytes = layers * (decode_bytes(case) + write_bytes(case))
+    step_mean, dec_mean = statistics.mean(step_ms), statistics.mean(dec_ms)
+    achieved = dbytes / (dec_mean / 1e3) / 1e9
+    step_gbs = sbytes / (step_mean / 1e3) / 1e9
+    del pools, qs, dd
+    torch.cuda.empty_cache()
+    return {
+        "workload": "fp8_step", "layers": layers, "steps": K, "num_seqs": case.num_seqs,
+        "num_heads": case.num_heads, "num_kv_heads": case.num_kv_heads, "head_dim": case.head_dim,
+        "block_size": case.block_size, "kv_dtype": case.kv_dtype,
+        "context_tokens_per_layer": int(case.context_lens.sum()),
+        "step_ms": round(step_mean, 4), "decode_ms_per_step": round(dec_mean, 4),
+        "decode_us_per_layer": round(1e3 * dec_mean / layers, 2),
+        "step_bytes": sbytes, "decode_bytes_per_step": dbytes,
+        "step_gbs": round(step_gbs, 1), "decode_gbs": round(achieved, 1),
+        "tokens_per_s_per_layer": round(case.num_seqs * layers / (step_mean / 1e3), 1),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "peak_source": peak_src,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": recorded_traffic("fp8_layer", 0),
+                     "kernel": "pa_decode (every kernel of the call), summed over the 32 layers"},
+        "roofline_step": {"bound": "hbm", "achieved": round(step_gbs, 1), "peak": peak,
+                          "peak_source": peak_src, "unit": "GB/s", "frac": round(step_gbs / peak, 4),
+                          "kernel": "the whole step: 32 x (pa_reshape_and_cache + pa_decode)"},
+        "gpu_launches": n1 - n0,
+    }
+
+
+def run_ours(args, world, rank, local):
+    import paged_kv_cache_288_gb300 as pa
+    from paged_kv_cache_288_gb300 import build
+
+    build.build_library()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    stream = torch.cuda.current_stream(device)
+    flush_l2 = make_flush(device)
+    peak, peak_src = peak_hbm()
+    if args.workload == "fp8_step":
+        sampler = ClockSampler(local)
+        sampler.start()
+        time.sleep(0.3)
+        t0 = time.time()
+        rec = run_fp8_step(pa, device, stream, flush_l2, args.steps, args.warmup, peak, peak_src)
+        t1 = time.time()
+        sampler.stop()
+        if rank != 0:
+            return None
+        return {"metric": METRIC, "value": rec["step_gbs"], "unit": "GB/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": rec["step_ms"],
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "fp8_e4m3 KV, bf16 q, f32 accumulate", "data": "synthetic",
+                "config": {"workload": "fp8_step", "l2": "flushed between steps"},
+                "roofline": rec["roofline"], "fp8_step": rec, "clocks": sampler.summary(t0, t1),
+                "gpu_launches": rec["gpu_launches"]}
+    case = make_case(args.workload, rank)
+    part = args.partition_size
+    dd = DeviceDecode(pa, case, device, part)
+    case = dd.case
+
+    K = args.steps
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    t0 = time.time()
+    step_ms, dec_ms, launches = time_write_decode(dd, K, args.warmup, flush_l2, stream, world)
+    t1 = time.time()
     sampler.stop()
-    step_ms = [ev[k][0].elapsed_time(ev[k][2]) for k in range(K)]
-    dec_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)]
     total_ms = max_over_ranks(sum(step_ms), world, device)
     dec_mean_ms = statistics.mean(dec_ms)
+    if dd.err.item() != 0:
+        raise RuntimeError(f"device error word {dd.err.item():#x}")
 
     # end to end through the public API with host buffers: inputs H2D, output D2H
+    q, nk, nv, slots, tables, lens = dd.q, dd.nk, dd.nv, dd.slots, dd.tables, dd.lens
     pin = lambda t: t.cpu().pin_memory()  # noqa: E731
     h_q, h_nk, h_nv, h_slots = pin(q), pin(nk), pin(nv), pin(slots)
     h_tables, h_lens = pin(tables), pin(lens)
-    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_out = torch.empty(dd.out.shape, dtype=dd.out.dtype).pin_memory()
     d_q, d_nk, d_nv = torch.empty_like(q), torch.empty_like(nk), torch.empty_like(nv)
     d_slots, d_tables, d_lens = torch.empty_like(slots), torch.empty_like(tables), torch.empty_like(lens)
     h2d = sum(t.numel() * t.element_size() for t in (h_q, h_nk, h_nv, h_slots, h_tables, h_lens))
@@ -483,10 +716,9 @@ def run_ours(args, world, rank, local):
         for dst, src in ((d_q, h_q), (d_nk, h_nk), (d_nv, h_nv), (d_slots, h_slots),
                          (d_tables, h_tables), (d_lens, h_lens)):
             dst.copy_(src, non_blocking=True)
-        pa.reshape_and_cache(d_nk, d_nv, kc, vc, d_slots, k_scale=ks, v_scale=vs)
-        pa.decode(out, d_q, kc, vc, d_tables, d_lens, case.scale, max_ctx, k_scale=ks,
-                  v_scale=vs, partition_size=part, workspace=ws)
-        h_out.copy_(out, non_blocking=True)
+        dd.write(d_nk, d_nv, d_slots)
+        dd.decode(q=d_q, tables=d_tables, lens=d_lens)
+        h_out.copy_(dd.out, non_blocking=True)
         eev[k][1].record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -498,13 +730,11 @@ def run_ours(args, world, rank, local):
     e2e_value = job_throughput_gbs(bytes_step, Ke, world, e2e_ms)
     dbytes = decode_bytes(case)
     achieved = dbytes / (dec_mean_ms / 1e3) / 1e9
-    peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    if os.path.exists(peaks_path):
-        peak = json.load(open(peaks_path))["hbm_gbs"]
-        peak_src = "measured"
-    else:
-        peak, peak_src = 6800.0, "fallback"
-    launches = n1 - n0
+    del dd
+    torch.cuda.empty_cache()
+    configs = None
+    if args.workload == "llama8b" and not args.no_configs and world == 1:
+        configs = run_config_suite(pa, device, stream, flush_l2, K, args.warmup, peak, peak_src)
     if rank != 0:
         return None
     line = {
@@ -527,7 +757,7 @@ def run_ours(args, world, rank, local):
             "num_kv_heads": case.num_kv_heads, "head_dim": case.head_dim,
             "block_size": case.block_size, "num_blocks": case.num_blocks,
             "context_tokens": int(case.context_lens.sum()),
-            "max_context_len": max_ctx, "partition_size": part,
+            "max_context_len": dd_max_ctx(case), "partition_size": part,
             "l2": "flushed between steps: 256 MiB written then read back, outside the timed events",
             "parallelism": f"{world} independent replica(s), one per GPU",
         },
@@ -545,12 +775,23 @@ def run_ours(args, world, rank, local):
         "gpu_launches": launches,
         "launches_per_step": launches / K,
     }
+    if args.workload == "shared_prefix":
+        ub = unique_decode_bytes(case)
+        a = ub / (dec_mean_ms / 1e3) / 1e9
+        line["roofline_unique"] = {"bound": "hbm", "achieved": round(a, 1), "peak": peak,
+                                   "peak_source": peak_src, "unit": "GB/s", "frac": round(a / peak, 4),
+                                   "note": "each shared block's KV counted once"}
     if case.meta and "prefix_cache" in case.meta:
         line["prefix_cache"] = case.meta["prefix_cache"]
+    if configs is not None:
+        line["configs"] = configs
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(args.workload, case)
-    del launches_before
     return line
+
+
+def dd_max_ctx(case):
+    return int(case.context_lens.max()) if case.num_seqs else 0
 
 
 # ----------------------------------------------------------------------------
@@ -1142,7 +1383,9 @@ def run_reference(args, world, rank):
     if rank != 0:
         return None
     case = make_case(args.workload, 0)
-    seqs = max(1, min(case.num_seqs, args.reference_seqs))
+    # at least one sequence per host core, so every core works as in cpu_baseline
+    want = args.reference_seqs if args.reference_seqs > 0 else max(8, host_cores())
+    seqs = max(1, min(case.num_seqs, want))
     times, cores = oracle_seconds(args.workload, seqs, args.warmup + args.steps)
     timed = times[args.warmup:]
     sub = sample_case(case, seqs)
@@ -1206,8 +1449,11 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llama8b")
     ap.add_argument("--partition-size", type=int, default=0)
-    ap.add_argument("--reference-seqs", type=int, default=8)
+    ap.add_argument("--reference-seqs", type=int, default=0,
+                    help="sequences per reference step (0: one per host core, at least 8)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="time only --workload (the llama8b line otherwise adds the other workloads)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")

@@ -72,3 +72,20 @@ def test_oracle_timing_spreads_sequences_over_processes():
     assert workers == 2 and len(times) == 2 and all(t > 0 for t in times)
     times, workers = bench.oracle_seconds("tiny", 1, 1, workers=4)
     assert workers == 1 and len(times) == 1
+
+
+def test_unique_bytes_count_shared_blocks_once():
+    """Two sequences sharing their first block: the logical bytes count it
+    twice, the unique bytes once; a private tail block counts its used
+    tokens only."""
+    import numpy as np
+    import bench
+    import workloads
+
+    case = workloads.paged_case(5, [20, 20], 4, 2, 8, 16, workloads.F16)
+    per_tok = case.num_kv_heads * 2 * case.head_dim * 2
+    case.block_tables[1, 0] = case.block_tables[0, 0]
+    fixed = 2 * 2 * 4 * 8 * 2 + 4 * 4 + 2 * 4  # q + out, 4 table entries, 2 lengths
+    assert bench.decode_bytes(case) == 40 * per_tok + fixed
+    assert bench.unique_decode_bytes(case) == (16 + 4 + 4) * per_tok + fixed
+    del np

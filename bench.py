@@ -85,6 +85,16 @@ def make_case(name, rank):
         return workloads.tiny()[0]
     if name == "llama8b":
         return workloads.llama8b(seed=rank_seed(1002, rank))
+    if name == "llama8b_mha":
+        # the Llama-8B-shaped batch with one KV head per query head (MHA, group 1)
+        ctx = workloads.llama8b_lengths(rank_seed(1002, rank))
+        return workloads.paged_case(rank_seed(1102, rank), ctx, 32, 32, 128, 16, workloads.BF16,
+                                    table_width=256, name="llama8b_mha", append=True)
+    if name == "llama8b_mqa":
+        # the same batch with one KV head shared by all 32 query heads (MQA)
+        ctx = workloads.llama8b_lengths(rank_seed(1002, rank))
+        return workloads.paged_case(rank_seed(1202, rank), ctx, 32, 1, 128, 16, workloads.BF16,
+                                    table_width=256, name="llama8b_mqa", append=True)
     if name == "shared_prefix":
         return workloads.shared_prefix(seed=rank_seed(1003, rank))
     if name.startswith("long_context"):

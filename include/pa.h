@@ -146,8 +146,10 @@ pa_status pa_reshape_and_cache(const void* key, const void* value, void* k_cache
  * capture took; calls sharing a counter must not overlap (the caller
  * serialises them), or work is skipped or done twice with no error flagged.
  *
- * Supported: num_heads / num_kv_heads in {1, 2, 4, 8}; head_dim in {64, 128,
- * 256}; block_size in {8, 16, 32, 64}.
+ * Supported: num_heads / num_kv_heads (the group G) 1, 2, 4, or any multiple
+ * of 8, which covers MHA (G = 1), GQA and MQA (num_kv_heads = 1, G =
+ * num_heads; LLM 추론 확장, 품질·비용 절충 필수, the MHA/MQA/GQA passage);
+ * head_dim in {64, 128, 256}; block_size in {8, 16, 32, 64}.
  */
 pa_status pa_decode(void* out, const void* q, const void* k_cache,
                     const void* v_cache, const int32_t* block_tables,

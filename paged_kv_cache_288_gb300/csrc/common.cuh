@@ -91,7 +91,9 @@ struct DecodeParams {
   int32_t max_blocks_per_seq;
   int32_t num_seqs;
   int32_t num_heads;
-  int32_t num_kv_heads;
+  int32_t num_kv_heads;     // KV units per sequence: KV heads, or slices of 8 query heads of one
+  int32_t kv_heads_phys;    // KV heads in the cache layout
+  int32_t kv_div;           // units per KV head (1, or G / 8 for groups above 8)
   int32_t block_size;
   int32_t num_blocks;
   int32_t max_context_len;
@@ -99,6 +101,11 @@ struct DecodeParams {
   int32_t num_partitions;   // partitions per sequence in the grid
   float scale_log2;         // softmax scale * log2(e)
 };
+
+// KV head of the caches that KV unit u reads.
+__device__ __forceinline__ int kv_head_of(const DecodeParams& p, int u) {
+  return p.kv_div == 1 ? u : u / p.kv_div;
+}
 
 // Clamp a sequence's context length to what the table and the grid cover.
 __device__ __forceinline__ int clamp_context(const DecodeParams& p, int seq) {

@@ -68,11 +68,12 @@ decode_simt_kernel(const DecodeParams p) {
       continue;
     }
     const int valid = min(bs, tok_end - b * bs);
-    const int64_t row0 = (static_cast<int64_t>(phys) * p.num_kv_heads + kvh) * bs;
+    const int64_t hi = static_cast<int64_t>(phys) * p.kv_heads_phys + kv_head_of(p, kvh);
+    const int64_t row0 = hi * bs;
     float kscale = 1.f, vscale = 1.f;
     if constexpr (kFp8) {
-      kscale = p.k_scale[static_cast<int64_t>(phys) * p.num_kv_heads + kvh];
-      vscale = p.v_scale[static_cast<int64_t>(phys) * p.num_kv_heads + kvh];
+      kscale = p.k_scale[hi];
+      vscale = p.v_scale[hi];
     }
     for (int t0 = 0; t0 < valid; t0 += kChunk) {
       float kf[kChunk][EPL];
@@ -191,42 +192,124 @@ decode_simt_kernel(const DecodeParams p) {
 }
 
 // Merge the partitions of one (sequence, query head): with M = max_p m_p and
-// w_p = 2^(m_p - M) * l_p, out = sum_p w_p * o_p / sum_p w_p.
+// w_p = 2^(m_p - M) * l_p, out = sum_p w_p * o_p / sum_p w_p (the partials
+// o_p are normalised). Partitions are taken kReduceThreads at a time: one
+// thread per partition loads its (m_p, l_p), and the rows are float4
+// elements of o_p with the threads split into groups of partitions, so one
+// round issues the loads of many partitions at once (kBatch per thread, all
+// independent). A running maximum carries the merge across chunks, so any
+// number of partitions fits the kernel's fixed shared memory.
+constexpr int kReduceThreads = 256;
+
 template <typename QT, int D>
-__global__ void __launch_bounds__(128) reduce_partitions_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kReduceThreads) reduce_partitions_kernel(const DecodeParams p) {
+  constexpr int NT = kReduceThreads;
+  constexpr int NE4 = D / 4;      // float4 elements per row: 16, 32 or 64
+  constexpr int NGRP = NT / NE4;  // groups of partitions: 16, 8 or 4
+  constexpr int kBatch = 4;       // row loads a thread keeps in flight
+  constexpr int kWarpsR = NT / 32;
   griddep_wait();
   const int h = blockIdx.x;
   const int seq = blockIdx.y;
   const int ctx = clamp_context(p, seq);
-  const int nparts = (ctx + p.partition_size - 1) / p.partition_size;
+  const int nparts = min((ctx + p.partition_size - 1) / p.partition_size, p.num_partitions);
   const int64_t base = (static_cast<int64_t>(seq) * p.num_heads + h) * p.num_partitions;
-  extern __shared__ float sm_w[];  // [num_partitions]
-  __shared__ float sm_max, sm_sum;
-  if (threadIdx.x < 32) {
-    float mt = -INFINITY;
-    for (int q = threadIdx.x; q < nparts; q += 32) mt = fmaxf(mt, p.ws_ml[(base + q) * 2]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
-    float st = 0.f;
-    for (int q = threadIdx.x; q < nparts; q += 32) {
-      const float w = (mt == -INFINITY) ? 0.f : exp2f(p.ws_ml[(base + q) * 2] - mt) * p.ws_ml[(base + q) * 2 + 1];
-      sm_w[q] = w;
-      st += w;
+  const int e4 = threadIdx.x % NE4, grp = threadIdx.x / NE4;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __shared__ float s_w[NT];
+  __shared__ float s_red[kWarpsR];
+  __shared__ float4 s_part[NT];
+  const float4* rows = reinterpret_cast<const float4*>(p.ws_acc + base * D) + e4;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float run = -INFINITY, den = 0.f;  // running maximum and denominator (uniform over the CTA)
+  for (int c0 = 0; c0 < nparts; c0 += NT) {
+    const int nin = min(NT, nparts - c0);
+    float m = -INFINITY, l = 0.f;
+    if (static_cast<int>(threadIdx.x) < nin) {
+      const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.ws_ml) + base + c0 + threadIdx.x);
+      m = ml.x;
+      l = ml.y;
     }
+    float4 v[kBatch];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) st += __shfl_xor_sync(0xffffffffu, st, off);
-    if (threadIdx.x == 0) {
-      sm_max = mt;
-      sm_sum = st;
+    for (int u = 0; u < kBatch; ++u) {
+      const int j = grp + u * NGRP;
+      v[u] = j < nin ? __ldcg(rows + static_cast<int64_t>(c0 + j) * NE4) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    // the chunk's maximum
+    float cm = m;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, off));
+    if (lane == 0) s_red[warp] = cm;
+    __syncthreads();
+    cm = s_red[0];
+#pragma unroll
+    for (int w = 1; w < kWarpsR; ++w) cm = fmaxf(cm, s_red[w]);
+    const float nm = fmaxf(run, cm);
+    const float scale = run == -INFINITY ? 0.f : exp2f(run - nm);
+    const float w = m == -INFINITY ? 0.f : exp2f(m - nm) * l;
+    s_w[threadIdx.x] = w;
+    float sw = w;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sw += __shfl_xor_sync(0xffffffffu, sw, off);
+    __syncthreads();  // every thread has read s_red (maxima) and written s_w
+    if (lane == 0) s_red[warp] = sw;
+    __syncthreads();
+    float d = 0.f;
+#pragma unroll
+    for (int i = 0; i < kWarpsR; ++i) d += s_red[i];
+    den = den * scale + d;
+    run = nm;
+    acc.x *= scale;
+    acc.y *= scale;
+    acc.z *= scale;
+    acc.w *= scale;
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int j = grp + u * NGRP;
+      const float wt = j < nin ? s_w[j] : 0.f;
+      acc.x = fmaf(wt, v[u].x, acc.x);
+      acc.y = fmaf(wt, v[u].y, acc.y);
+      acc.z = fmaf(wt, v[u].z, acc.z);
+      acc.w = fmaf(wt, v[u].w, acc.w);
+    }
+    // partitions beyond the first batch of this thread
+    for (int j0 = grp + kBatch * NGRP; j0 < nin; j0 += kBatch * NGRP) {
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int j = j0 + u * NGRP;
+        v[u] = j < nin ? __ldcg(rows + static_cast<int64_t>(c0 + j) * NE4) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int j = j0 + u * NGRP;
+        const float wt = j < nin ? s_w[j] : 0.f;
+        acc.x = fmaf(wt, v[u].x, acc.x);
+        acc.y = fmaf(wt, v[u].y, acc.y);
+        acc.z = fmaf(wt, v[u].z, acc.z);
+        acc.w = fmaf(wt, v[u].w, acc.w);
+      }
+    }
+    __syncthreads();  // s_w and s_red are rewritten by the next chunk
   }
+  s_part[threadIdx.x] = acc;
   __syncthreads();
-  QT* out = static_cast<QT*>(p.out);
-  const float inv = sm_sum > 0.f ? 1.f / sm_sum : 0.f;
-  for (int e = threadIdx.x; e < D; e += blockDim.x) {
-    float a = 0.f;
-    for (int q = 0; q < nparts; ++q) a = fmaf(sm_w[q], p.ws_acc[(base + q) * D + e], a);
-    out[(static_cast<int64_t>(seq) * p.num_heads + h) * D + e] = from_float(a * inv, static_cast<QT*>(nullptr));
+  if (grp == 0) {
+    float4 t = acc;
+#pragma unroll
+    for (int gi = 1; gi < NGRP; ++gi) {
+      const float4 u = s_part[gi * NE4 + e4];
+      t.x += u.x;
+      t.y += u.y;
+      t.z += u.z;
+      t.w += u.w;
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    QT* out = static_cast<QT*>(p.out) + (static_cast<int64_t>(seq) * p.num_heads + h) * D + 4 * e4;
+    out[0] = from_float(t.x * inv, static_cast<QT*>(nullptr));
+    out[1] = from_float(t.y * inv, static_cast<QT*>(nullptr));
+    out[2] = from_float(t.z * inv, static_cast<QT*>(nullptr));
+    out[3] = from_float(t.w * inv, static_cast<QT*>(nullptr));
   }
 }
 
@@ -245,7 +328,7 @@ cudaError_t launch_d(const DecodeParams& p, int group, cudaStream_t stream) {
   note_launches(1);
   if (p.num_partitions == 1) return err;
   dim3 rgrid(p.num_heads, p.num_seqs);
-  reduce_partitions_kernel<QT, D><<<rgrid, 128, p.num_partitions * sizeof(float), stream>>>(p);
+  reduce_partitions_kernel<QT, D><<<rgrid, kReduceThreads, 0, stream>>>(p);
   err = cudaGetLastError();
   if (err == cudaSuccess) note_launches(1);
   return err;
@@ -258,8 +341,8 @@ cudaError_t launch_reduce_pdl(const DecodeParams& p, bool pdl, cudaStream_t stre
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.num_heads, p.num_seqs);
-  cfg.blockDim = dim3(128);
-  cfg.dynamicSmemBytes = p.num_partitions * sizeof(float);
+  cfg.blockDim = dim3(kReduceThreads);
+  cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;

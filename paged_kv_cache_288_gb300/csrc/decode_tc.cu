@@ -317,7 +317,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
       if (kvh != win_kvh) {
         win_kvh = kvh;
         const bool ok = win_val >= 0 && win_val < p.num_blocks;
-        const int64_t si = static_cast<int64_t>(ok ? win_val : 0) * Hkv + kvh;
+        const int64_t si = static_cast<int64_t>(ok ? win_val : 0) * p.kv_heads_phys + kv_head_of(p, kvh);
         win_ks = ok ? p.k_scale[si] : 1.f;
         win_vs = ok ? p.v_scale[si] : 1.f;
       }
@@ -380,7 +380,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
 #pragma unroll
       for (int h = 0; h < kMaxSub; ++h) {
         if (phys[h] < 0) continue;
-        const int z = phys[h] * Hkv + c.kvh;
+        const int z = phys[h] * p.kv_heads_phys + kv_head_of(p, c.kvh);
         const uint32_t rows_before = h * bh * 128;  // boxes of later blocks sit after earlier ones
 #pragma unroll
         for (int b = 0; b < Gm::kBoxes; ++b) {
@@ -1069,7 +1069,7 @@ cudaError_t launch_typed(const TcParams& tp, const void* k_cache, const void* v_
                          cudaStream_t stream) {
   const DecodeParams& p = tp.p;
   CUtensorMap mk, mv;
-  const int64_t bxh = static_cast<int64_t>(p.num_blocks) * p.num_kv_heads;
+  const int64_t bxh = static_cast<int64_t>(p.num_blocks) * p.kv_heads_phys;
   if (!make_cache_map(&mk, k_cache, D, int(sizeof(KT)), p.block_size, TT, bxh) ||
       !make_cache_map(&mv, v_cache, D, int(sizeof(KT)), p.block_size, TT, bxh))
     return cudaErrorInvalidValue;
@@ -1120,7 +1120,7 @@ cudaError_t launch_typed(const TcParams& tp, const void* k_cache, const void* v_
 int tc_tile_tokens(pa_dtype kv_dtype) { return kv_dtype == PA_FP8_E4M3 ? 32 : 16; }
 
 bool tc_supported(int group, int head_dim, pa_dtype kv_dtype, int num_seqs, int partition_size) {
-  if (group != 2 && group != 4 && group != 8) return false;
+  if (group < 1 || group > kMaxG) return false;
   if (num_seqs > kTcMaxSeqs) return false;
   if (partition_size % tc_tile_tokens(kv_dtype) != 0) return false;
   if (kv_dtype == PA_FP8_E4M3) return head_dim == 128;

@@ -33,7 +33,12 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool is_16bit(pa_dtype t) { return t == PA_F16 || t == PA_BF16; }
 bool valid_dtype(pa_dtype t) { return t == PA_F16 || t == PA_BF16 || t == PA_FP8_E4M3; }
 bool supported_block_size(int bs) { return bs == 8 || bs == 16 || bs == 32 || bs == 64; }
-bool supported_group(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
+// Query heads per KV head: 1, 2, 4, 8, or a multiple of 8 (up to MQA, where
+// every query head shares one KV head). Groups above 8 are run as KV units of
+// 8 query heads that read the same KV head.
+bool supported_group(int g) { return g == 1 || g == 2 || g == 4 || (g >= 8 && g % 8 == 0); }
+constexpr int kUnitHeads = 8;
+int unit_group(int g) { return g > kUnitHeads ? kUnitHeads : g; }
 bool supported_head_dim(int d) { return d == 64 || d == 128 || d == 256; }
 
 constexpr int kAutoPartition = 512;
@@ -136,7 +141,7 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t num
   size_t need = 0;
   const int sms = current_sm_count();
   if (sms > 0 && num_kv_heads > 0 && num_heads % num_kv_heads == 0)
-    need = pa::tc_auto_workspace_bytes(num_seqs, head_dim, num_heads / num_kv_heads, sms);
+    need = pa::tc_auto_workspace_bytes(num_seqs, head_dim, unit_group(num_heads / num_kv_heads), sms);
   const int part = auto_partition(max_context_len);
   if (part > 0) {
     const size_t simt = split_workspace_bytes(num_seqs, num_heads, head_dim,
@@ -183,10 +188,11 @@ pa_status validate_decode_args(const void* out, const void* q, const void* k_cac
   if (!supported_block_size(block_size))
     return fail(PA_ERR_UNSUPPORTED, "block_size %d not in {8,16,32,64}", block_size);
   if (!supported_group(num_heads / num_kv_heads))
-    return fail(PA_ERR_UNSUPPORTED, "num_heads/num_kv_heads %d not in {1,2,4,8}",
+    return fail(PA_ERR_UNSUPPORTED, "num_heads/num_kv_heads %d not 1, 2, 4 or a multiple of 8",
                 num_heads / num_kv_heads);
   if (!supported_head_dim(head_dim))
     return fail(PA_ERR_UNSUPPORTED, "head_dim %d not in {64,128,256}", head_dim);
+  if (num_seqs > 65535) return fail(PA_ERR_UNSUPPORTED, "more than 65535 sequences");
   if (num_seqs == 0) return PA_OK;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
     return fail(PA_ERR_INVALID, "null tensor pointer");
@@ -228,13 +234,16 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
   p.max_blocks_per_seq = max_blocks_per_seq;
   p.num_seqs = num_seqs;
   p.num_heads = num_heads;
-  p.num_kv_heads = num_kv_heads;
+  // groups above 8 query heads: KV units of 8 query heads each, several per KV head
+  const int group = unit_group(num_heads / num_kv_heads);
+  p.kv_div = (num_heads / num_kv_heads) / group;
+  p.kv_heads_phys = num_kv_heads;
+  p.num_kv_heads = num_kv_heads * p.kv_div;
   p.block_size = block_size;
   p.num_blocks = num_blocks;
   p.max_context_len = max_context_len;
   p.scale_log2 = scale * pa::kLog2e;
 
-  const int group = num_heads / num_kv_heads;
   const bool tc = pa::tc_supported(group, head_dim, kv_dtype, num_seqs, partition_size > 0 ? partition_size : 0);
   if (partition_size > 0) {
     const int nparts = num_partitions_for(max_context_len, partition_size);

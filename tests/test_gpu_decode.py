@@ -59,6 +59,49 @@ def test_random_shapes(group, Hkv, d, bs, dtype):
     _check(case)
 
 
+# MQA and groups above 8 (LLM 추론 확장, 품질·비용 절충 필수: MHA, MQA and
+# GQA): every query head of a group reads the same KV head
+WIDE_GROUPS = [
+    # (num_heads, num_kv_heads, d, bs, dtype)
+    (32, 1, 128, 16, BF16), (16, 1, 128, 16, F16), (64, 1, 64, 32, BF16), (16, 2, 128, 8, BF16),
+    (32, 4, 64, 16, F16), (24, 1, 128, 64, BF16),
+]
+
+
+@pytest.mark.parametrize("Hq,Hkv,d,bs,dtype", WIDE_GROUPS)
+def test_mqa_and_wide_groups(Hq, Hkv, d, bs, dtype):
+    lengths = [1, 17, 300, 1000, 2500, 64]
+    case = workloads.paged_case(Hq * 100 + Hkv * 10 + bs, lengths, Hq, Hkv, d, bs, dtype,
+                                name=f"mqa{Hq}/{Hkv}")
+    _, out, dc = _check(case)
+    ref = oracle_decode(case)
+    # the split path and the schedule without a workspace take the same groups
+    for part, ws in ((256 if 256 % bs == 0 else 512, True), (0, False)):
+        other = run_decode(pa, dc, partition_size=part, workspace=ws)
+        torch.cuda.synchronize()
+        assert_close(other, ref, dtype, dtype, f"mqa part={part} ws={ws}")
+    assert dc.debug_err.item() == 0
+
+
+def test_mqa_fp8():
+    """MQA over an 8-bit cache: 32 query heads, one KV head."""
+    case = workloads.fp8_layer(880, [1, 40, 500, 1500], num_heads=32, num_kv_heads=1,
+                               head_dim=128, block_size=16, src_dtype=BF16, name="mqa_fp8")
+    dc = DeviceCase(case)
+    pa.reshape_and_cache(dc.new_key, dc.new_value, dc.k_cache, dc.v_cache, dc.slot_mapping,
+                         k_scale=dc.k_scale, v_scale=dc.v_scale, debug_err=dc.debug_err)
+    kc, vc = case.k_cache.copy(), case.v_cache.copy()
+    oracle.reshape_and_cache(case.new_key, case.new_value, kc, vc, case.slot_mapping, 16, BF16,
+                             FP8_E4M3, case.k_scale, case.v_scale)
+    ref = oracle_decode(case, k_cache=kc, v_cache=vc)
+    for part in (0, 512):
+        out = run_decode(pa, dc, partition_size=part)
+        torch.cuda.synchronize()
+        max_abs, _ = assert_close(out, ref, BF16, FP8_E4M3, f"mqa fp8 part={part}")
+        assert max_abs <= 3e-2
+    assert dc.debug_err.item() == 0
+
+
 @pytest.mark.parametrize("bs", [8, 16, 32, 64])
 def test_lengths_around_block_boundaries(bs):
     lengths = [1, 2, bs - 1, bs, bs + 1, 2 * bs - 1, 2 * bs, 2 * bs + 1, 5 * bs + 3]

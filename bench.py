@@ -420,8 +420,9 @@ class DeviceDecode:
     steps (copy-on-write copies, the suffix or history tokens) is done once
     here, outside any timing."""
 
-    def __init__(self, pa, case, device, part):
+    def __init__(self, pa, case, device, part, groups=None):
         self.pa, self.case, self.part = pa, case, part
+        self.groups = groups
 
         def to_dev(bits, dtype):
             a = np.ascontiguousarray(bits)
@@ -469,6 +470,16 @@ class DeviceDecode:
         self.max_ctx = int(case.context_lens.max())
         ws_bytes = pa.decode_workspace_size(case.num_seqs, case.num_heads, case.num_kv_heads,
                                             case.head_dim, self.max_ctx, part)
+        if groups is not None:
+            # sequences sharing leading blocks, attended once per group
+            gs, gp = groups
+            self.gs = torch.from_numpy(np.asarray(gs, np.int32)).to(device)
+            self.gp = torch.from_numpy(np.asarray(gp, np.int32)).to(device)
+            self.mgs = int(np.diff(gs).max())
+            self.mpl = int(np.max(gp))
+            ws_bytes = pa.decode_shared_prefix_workspace_size(
+                case.num_seqs, case.num_heads, case.num_kv_heads, case.head_dim, case.block_size,
+                len(gp), self.mgs, self.mpl)
         self.ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=device)
 
     def write(self, nk=None, nv=None, slots=None):
@@ -478,6 +489,13 @@ class DeviceDecode:
 
     def decode(self, q=None, tables=None, lens=None):
         c = self.case
+        if self.groups is not None:
+            self.pa.decode_shared_prefix(
+                self.out, self.q if q is None else q, self.kc, self.vc,
+                self.tables if tables is None else tables, self.lens if lens is None else lens,
+                c.scale, self.max_ctx, self.gs, self.gp, self.mgs, self.mpl, self.ws,
+                debug_err=self.err)
+            return
         self.pa.decode(self.out, self.q if q is None else q, self.kc, self.vc,
                        self.tables if tables is None else tables, self.lens if lens is None else lens,
                        c.scale, self.max_ctx, k_scale=self.ks, v_scale=self.vs,
@@ -559,16 +577,16 @@ def run_config_suite(pa, device, stream, flush_l2, K, W, peak, peak_src):
     path and the library's schedule) and the 32-layer E4M3 decode step."""
     out = {}
 
-    def one(name, case, parts, extra_fn=None):
+    def one(name, case, parts, extra_fn=None, groups=None, key=None):
         for part in parts:
-            dd = DeviceDecode(pa, case, device, part)
+            dd = DeviceDecode(pa, case, device, part, groups)
             step_ms, dec_ms, launches = time_write_decode(dd, K, W, flush_l2, stream)
             torch.cuda.synchronize()
             if dd.err.item() != 0:
                 raise RuntimeError(f"{name}: device error word {dd.err.item():#x}")
             extra = extra_fn(case, statistics.mean(dec_ms)) if extra_fn else None
-            out[f"{name}/p{part}"] = decode_result(case, step_ms, dec_ms, launches, part, peak, peak_src,
-                                                   name, extra)
+            out[key or f"{name}/p{part}"] = decode_result(case, step_ms, dec_ms, launches, part, peak,
+                                                          peak_src, name, extra)
             del dd
             torch.cuda.empty_cache()
 
@@ -581,6 +599,10 @@ def run_config_suite(pa, device, stream, flush_l2, K, W, peak, peak_src):
                                     "note": "each shared block's KV counted once"}}
 
     one("shared_prefix", workloads.shared_prefix(), [0], shared_extra)
+    sp = workloads.shared_prefix()
+    shared_tokens = sp.meta["prefix_len"] // sp.block_size * sp.block_size
+    one("shared_prefix", sp, [0], shared_extra, groups=([0, sp.num_seqs], [shared_tokens]),
+        key="shared_prefix/grouped")
     for bs in (8, 16, 32, 64):
         one(f"long_context_bs{bs}", workloads.long_context(bs), [512, 0])
     out["fp8_step"] = run_fp8_step(pa, device, stream, flush_l2, K, W, peak, peak_src)
@@ -690,7 +712,12 @@ def run_ours(args, world, rank, local):
                 "gpu_launches": rec["gpu_launches"]}
     case = make_case(args.workload, rank)
     part = args.partition_size
-    dd = DeviceDecode(pa, case, device, part)
+    groups = None
+    if args.shared_groups and args.workload in ("shared_prefix", "prefix_cache"):
+        # one group: every sequence shares the prefix's whole blocks
+        plen = case.meta["prefix_len"] if "prefix_len" in case.meta else 1016
+        groups = ([0, case.num_seqs], [plen // case.block_size * case.block_size])
+    dd = DeviceDecode(pa, case, device, part, groups)
     case = dd.case
 
     K = args.steps
@@ -768,6 +795,7 @@ def run_ours(args, world, rank, local):
             "block_size": case.block_size, "num_blocks": case.num_blocks,
             "context_tokens": int(case.context_lens.sum()),
             "max_context_len": dd_max_ctx(case), "partition_size": part,
+            "shared_groups": groups is not None,
             "l2": "flushed between steps: 256 MiB written then read back, outside the timed events",
             "parallelism": f"{world} independent replica(s), one per GPU",
         },
@@ -1462,6 +1490,8 @@ def main():
     ap.add_argument("--reference-seqs", type=int, default=0,
                     help="sequences per reference step (0: one per host core, at least 8)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--shared-groups", action="store_true",
+                    help="shared_prefix / prefix_cache: decode with pa_decode_shared_prefix")
     ap.add_argument("--no-configs", action="store_true",
                     help="time only --workload (the llama8b line otherwise adds the other workloads)")
     args = ap.parse_args()

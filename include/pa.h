@@ -65,6 +65,8 @@ typedef enum {
 #define PA_DEVERR_LAYOUT 0x10       /* a kernel found its shared memory misaligned; nothing computed */
 #define PA_DEVERR_QUERY_START 0x20  /* pa_prefill: query_start outside [0, num_tokens] or decreasing; clamped */
 #define PA_DEVERR_Q_RANGE 0x40      /* pa_decode, 8-bit KV: a q value beyond the f16 range (|q| > 65504) */
+#define PA_DEVERR_PREFIX 0x80       /* pa_decode_shared_prefix: a group description was clamped, or a
+                                       member's table differs from its group's in the shared blocks */
 
 /* Library version, major*10000 + minor*100 + patch. */
 int pa_version(void);
@@ -169,6 +171,62 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache,
 size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_heads,
                                 int32_t num_kv_heads, int32_t head_dim,
                                 int32_t max_context_len, int32_t partition_size);
+
+/*
+ * pa_decode_shared_prefix - pa_decode for a batch whose sequences come in
+ * groups that share the leading blocks of their tables, reading each shared
+ * block once per group instead of once per sequence.
+ *
+ * When many requests open with one prompt, their tables point at the same
+ * physical blocks for it (serving-paged-attention, "공유는 표를 베끼는 일이
+ * 된다": a system prompt shared by 100 requests is stored once). The result
+ * is pa_decode's, out[i, h] = softmax(scale * K q[i, h]) V over each
+ * sequence's whole context; only the order of the work changes. The shared
+ * tokens of a group are attended for all its members at once (their query
+ * rows form a dense tile for the tensor cores) into partial softmax states,
+ * which are merged with the states of each member's own suffix.
+ *
+ * Groups: group g is sequences group_start[g] .. group_start[g+1]-1 (DEVICE
+ * int32 [num_groups + 1], non-decreasing, group_start[0] = 0,
+ * group_start[num_groups] = num_seqs; a sequence in no group may sit in a
+ * group of its own with prefix 0). Its members share their first
+ * group_prefix[g] tokens (DEVICE int32 [num_groups], a multiple of
+ * block_size, at most every member's context length): the first
+ * group_prefix[g] / block_size entries of their tables are equal. The shared
+ * blocks are read through the table of the group's first sequence.
+ * max_group_size and max_prefix_len are host-known bounds on every group's
+ * size and prefix (they size the grid). Descriptions that break these rules
+ * are clamped so that nothing outside the arrays is read or written, and set
+ * PA_DEVERR_PREFIX in *debug_err (the results are then undefined); so does a
+ * member whose table differs from its group's first in the shared blocks.
+ *
+ * Other arguments as for pa_decode with partition_size = 0: dtype is the
+ * type of q, out and both caches (PA_F16 or PA_BF16); head_dim 64 or 128;
+ * the group sizes of pa_decode; at most 2048 sequences. The workspace
+ * (caller-owned device memory, 256-byte aligned) must hold
+ * pa_decode_shared_prefix_workspace_size() bytes for the same sizes on the
+ * current device, else PA_ERR_WORKSPACE. The calls-that-overlap rule of
+ * pa_decode applies.
+ */
+pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k_cache,
+                                  const void* v_cache, const int32_t* block_tables,
+                                  int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                  int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                  float scale, pa_dtype dtype, int32_t max_context_len,
+                                  const int32_t* group_start, const int32_t* group_prefix,
+                                  int32_t num_groups, int32_t max_group_size,
+                                  int32_t max_prefix_len, void* workspace,
+                                  size_t workspace_bytes, int32_t* debug_err,
+                                  cudaStream_t stream);
+
+/* Bytes of workspace pa_decode_shared_prefix needs for these sizes on the
+ * current device (0 for invalid sizes or without a device). */
+size_t pa_decode_shared_prefix_workspace_size(int32_t num_seqs, int32_t num_heads,
+                                              int32_t num_kv_heads, int32_t head_dim,
+                                              int32_t block_size, int32_t num_groups,
+                                              int32_t max_group_size,
+                                              int32_t max_prefix_len);
 
 /*
  * pa_copy_blocks - copy whole physical blocks, K and V, in every layer.

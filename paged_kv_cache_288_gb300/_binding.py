@@ -20,6 +20,7 @@ DEVERR_TIMEOUT = 0x8
 DEVERR_LAYOUT = 0x10
 DEVERR_QUERY_START = 0x20
 DEVERR_Q_RANGE = 0x40
+DEVERR_PREFIX = 0x80
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libpa.so")
@@ -69,6 +70,13 @@ def lib():
             _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int32, _c_ptr, _c_int32, _c_int32,
             _c_int32, _c_int32, _c_int32, _c_int32, ctypes.c_float, ctypes.c_int, ctypes.c_int,
             _c_ptr, _c_ptr, _c_int32, _c_int32, _c_ptr, _c_ptr]
+        L.pa_decode_shared_prefix.restype = ctypes.c_int
+        L.pa_decode_shared_prefix.argtypes = [
+            _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int32, _c_ptr, _c_int32, _c_int32,
+            _c_int32, _c_int32, _c_int32, _c_int32, ctypes.c_float, ctypes.c_int, _c_int32,
+            _c_ptr, _c_ptr, _c_int32, _c_int32, _c_int32, _c_ptr, _c_size, _c_ptr, _c_ptr]
+        L.pa_decode_shared_prefix_workspace_size.restype = _c_size
+        L.pa_decode_shared_prefix_workspace_size.argtypes = [_c_int32] * 8
         L.pa_prefill.restype = ctypes.c_int
         L.pa_prefill.argtypes = [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int32, _c_ptr, _c_ptr,
                                  _c_int32, _c_int32, _c_int32, _c_int32, _c_int32, _c_int32,
@@ -178,6 +186,48 @@ def decode(out, q, k_cache, v_cache, block_tables, context_lens, scale, max_cont
         _dtype_code(q.dtype), _dtype_code(k_cache.dtype), _ptr(k_scale), _ptr(v_scale),
         int(max_context_len), int(partition_size), _ptr(workspace), ws_bytes, _ptr(debug_err),
         _stream(stream)), "pa_decode")
+
+
+def decode_shared_prefix_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                                        num_groups, max_group_size, max_prefix_len):
+    return int(lib().pa_decode_shared_prefix_workspace_size(
+        num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_groups, max_group_size,
+        max_prefix_len))
+
+
+def decode_shared_prefix(out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                         max_context_len, group_start, group_prefix, max_group_size,
+                         max_prefix_len, workspace, debug_err=None, stream=None):
+    """pa_decode for sequences grouped by a shared leading run of blocks.
+
+    group_start (int32 [num_groups + 1]) and group_prefix (int32 [num_groups])
+    are device tensors; group g is sequences group_start[g] ..
+    group_start[g+1]-1 sharing their first group_prefix[g] tokens. The
+    workspace holds decode_shared_prefix_workspace_size() bytes.
+    """
+    B, Hq, d = q.shape
+    Nb, Hkv, bs, d2 = k_cache.shape
+    if d2 != d or out.shape != q.shape or v_cache.shape != k_cache.shape or q.dtype != k_cache.dtype:
+        raise ValueError("shape or dtype mismatch")
+    for t, name in ((block_tables, "block_tables"), (context_lens, "context_lens"),
+                    (group_start, "group_start"), (group_prefix, "group_prefix")):
+        if t.dtype != torch.int32:
+            raise ValueError(f"{name} must be int32")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or context_lens.numel() != B:
+        raise ValueError("block_tables must be [num_seqs, max_blocks]; context_lens [num_seqs]")
+    G = group_prefix.numel()
+    if group_start.numel() != G + 1:
+        raise ValueError("group_start must be [num_groups + 1]")
+    _on_device("decode_shared_prefix", out=out, q=q, k_cache=k_cache, v_cache=v_cache,
+               block_tables=block_tables, context_lens=context_lens, group_start=group_start,
+               group_prefix=group_prefix, workspace=workspace, debug_err=debug_err)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().pa_decode_shared_prefix(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
+        _ptr(context_lens), B, Hq, Hkv, d, bs, Nb, float(scale), _dtype_code(q.dtype),
+        int(max_context_len), _ptr(group_start), _ptr(group_prefix), G, int(max_group_size),
+        int(max_prefix_len), _ptr(workspace), ws_bytes, _ptr(debug_err), _stream(stream)),
+        "pa_decode_shared_prefix")
 
 
 def prefill(out, q, k_cache, v_cache, block_tables, context_lens, query_start, scale,

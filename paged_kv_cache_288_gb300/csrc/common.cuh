@@ -102,6 +102,52 @@ struct DecodeParams {
   float scale_log2;         // softmax scale * log2(e)
 };
 
+// Groups of sequences that share the leading blocks of their tables (a common
+// prompt prefix). Group g is sequences group_start[g] .. group_start[g+1]-1;
+// every member's first group_prefix[g] tokens are the same physical blocks.
+// The shared tokens are attended once per group (prefix_attn_kernel) into
+// partial softmax states, which the merge combines with each member's own
+// suffix.
+struct PrefixGroups {
+  const int32_t* group_start;   // device [num_groups + 1]
+  const int32_t* group_prefix;  // device [num_groups], tokens (multiples of block_size)
+  float* ws_prefix;             // [num_seqs * units * num_chunks] states of group * (D + 2) floats
+  int32_t num_groups;
+  int32_t max_group_size;       // members per group the prefix grid covers
+  int32_t max_prefix_len;       // bound on every group's prefix; sizes the prefix grid
+  int32_t chunk_len;            // keys per prefix chunk, a multiple of 16 and of block_size
+  int32_t num_chunks;           // chunks of the longest prefix
+};
+
+// The member range [a, b) and the shared token count of group g, clamped so
+// that no index leaves its array: ranges into [0, num_seqs], at most
+// max_group_size members, the prefix into [0, min(max_prefix_len, table
+// width)] and down to whole blocks. Returns true when anything was clamped.
+__device__ __forceinline__ bool prefix_group(const PrefixGroups& pg, int g, int num_seqs,
+                                             int max_blocks_per_seq, int block_size, int& a,
+                                             int& b, int& len) {
+  const int a0 = pg.group_start[g], b0 = pg.group_start[g + 1], p0 = pg.group_prefix[g];
+  a = min(max(a0, 0), num_seqs);
+  b = min(max(b0, a), num_seqs);
+  bool clamped = a != a0 || b != b0;
+  if (b - a > pg.max_group_size) {
+    b = a + pg.max_group_size;
+    clamped = true;
+  }
+  const int cap = min(pg.max_prefix_len, max_blocks_per_seq * block_size);
+  len = min(max(p0, 0), cap);
+  len -= len % block_size;
+  return clamped || len != p0;
+}
+
+// Floats of one partial softmax state of a KV unit with `group` query heads:
+// the unnormalised accumulators [group][head_dim], then the group's maxima and
+// sums, padded to a multiple of 4 so that every state starts 16-byte aligned
+// (the merge reads the accumulators as float4).
+__host__ __device__ constexpr int state_floats(int group, int head_dim) {
+  return group * head_dim + ((2 * group + 3) & ~3);
+}
+
 // KV head of the caches that KV unit u reads.
 __device__ __forceinline__ int kv_head_of(const DecodeParams& p, int u) {
   return p.kv_div == 1 ? u : u / p.kv_div;

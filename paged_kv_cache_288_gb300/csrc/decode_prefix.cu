@@ -1,0 +1,386 @@
+// Decode attention over a prefix that many sequences share, read once per
+// group of sequences.
+//
+// When many requests open with the same prompt, their block tables point at
+// the same physical blocks for it (serving-paged-attention, "공유는 표를
+// 베끼는 일이 된다": the system prompt of 100 requests is stored once). A
+// per-sequence decode still streams those blocks once per sequence. Here the
+// shared keys are attended once per group instead: the rows of the product
+// are (member sequence, query head) pairs of one KV unit, so with 100 members
+// and 4 heads per KV head a 16-key tile meets 400 query rows, a real dense
+// tile for the tensor cores.
+//
+// Work. One CTA of four warps takes 64 rows (16 per warp: member r / G, query
+// head r % G of the unit) and one chunk of the group's shared keys; the grid
+// is (row tiles, KV units, group x chunk). Its K and V tiles (16 keys, one
+// 3-D TMA box per 128-byte column per block) go through a four-stage ring in
+// shared memory that all warps read. Per tile and warp: S = Q K^T as
+// mma.sync m16n8k16 with Q held as A fragments in registers and K^T as B
+// fragments (ldmatrix), the online softmax on the accumulators (running
+// maximum in log2 units, running sum, rescaled O), P packed straight from
+// the S accumulators into A fragments, and O += P V with V through
+// ldmatrix.trans. Each row ends as a partial state (unnormalised O, maximum,
+// sum) in the same layout as the decode kernel's partial states, one per
+// (sequence, KV unit, chunk); the merge kernel combines them with the states
+// of the member's own suffix.
+//
+// The grid runs before the decode grid of the same call (which then streams
+// only the members' own suffixes), on the whole GPU.
+#include "common.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace pa {
+namespace {
+
+constexpr int kPxWarps = 4;
+constexpr int kPxThreads = 32 * kPxWarps;
+constexpr int kPxRows = 16 * kPxWarps;  // rows of a CTA
+constexpr int kPxTile = 16;             // keys per ring stage
+constexpr int kPxStages = 4;
+constexpr int kPxMaxEntries = 256;      // block-table entries of one chunk held in shared memory
+constexpr uint32_t kFullMask = 0xffffffffu;
+
+template <int D>
+struct PxGeom {
+  static constexpr int kBoxes = D * 2 / 128;          // 128-byte columns of a row
+  static constexpr int kBoxBytes = kPxTile * 128;     // one column of a 16-key tile
+  static constexpr int kTileBytes = kPxTile * D * 2;  // K (or V) of one stage
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kSmemBytes = 1024 + kPxStages * kStageBytes + 2 * kPxStages * 8 + 16 +
+                                    kPxMaxEntries * 4;
+};
+
+struct PxParams {
+  DecodeParams p;
+  PrefixGroups pg;
+  int group;  // query heads per KV unit
+};
+
+// Address of 16-byte chunk `chunk` of key row `row` in a stage tile whose
+// 128-byte columns are kBoxBytes apart, chunks swizzled by row % 8 as the TMA
+// 128-byte swizzle stores them.
+template <int box_bytes>
+__device__ __forceinline__ uint32_t px_addr(uint32_t base, int row, int chunk) {
+  return base + (chunk >> 3) * box_bytes + row * 128 + (((chunk & 7) ^ (row & 7)) << 4);
+}
+
+__device__ __forceinline__ uint32_t px_pack(float lo, float hi, bf16*) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t px_pack(float lo, float hi, f16*) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+template <typename T>
+__device__ __forceinline__ void px_mma(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  if constexpr (std::is_same<T, bf16>::value) mma_bf16(d, a, b0, b1);
+  else mma_f16(d, a, b0, b1);
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kPxThreads)
+prefix_attn_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                   const PxParams xp) {
+  using Gm = PxGeom<D>;
+  constexpr int KS = D / 16;  // 16-column steps of d
+  const DecodeParams& p = xp.p;
+  const PrefixGroups& pg = xp.pg;
+  const int G = xp.group;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = lane >> 2, tig = lane & 3;
+
+  const int unit = blockIdx.y;
+  const int grp = blockIdx.z / pg.num_chunks;
+  const int chunk = blockIdx.z % pg.num_chunks;
+  const int bs = p.block_size;
+  int a, b, plen;
+  const bool clamped = prefix_group(pg, grp, p.num_seqs, p.max_blocks_per_seq, bs, a, b, plen);
+  if (clamped && threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0 && chunk == 0)
+    flag_error(p.debug_err, PA_DEVERR_PREFIX);
+  const int rows = (b - a) * G;
+  const int row0 = blockIdx.x * kPxRows;
+  const int k0 = chunk * pg.chunk_len;
+  const int k1 = min(plen, k0 + pg.chunk_len);
+  if (row0 >= rows || k0 >= k1) return;
+  const int ntiles = (k1 - k0 + kPxTile - 1) / kPxTile;
+
+  extern __shared__ unsigned char px_smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(px_smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t stage0 = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kPxStages * Gm::kStageBytes);
+  int* s_abort = reinterpret_cast<int*>(bars + 2 * kPxStages);
+  int* s_ent = s_abort + 4;
+  auto full_bar = [&](int s) { return smem_u32(&bars[s]); };
+  auto empty_bar = [&](int s) { return smem_u32(&bars[kPxStages + s]); };
+
+  // the chunk's blocks, from the group's first member's table
+  const int j0 = k0 / bs;
+  const int nent = (k1 - 1) / bs - j0 + 1;  // <= chunk_len / bs + 1 <= kPxMaxEntries
+  const int32_t* lead = p.block_tables + static_cast<int64_t>(a) * p.max_blocks_per_seq;
+  for (int i = threadIdx.x; i < nent; i += kPxThreads) {
+    int e = lead[j0 + i];
+    if (e < 0 || e >= p.num_blocks) {
+      flag_error(p.debug_err, PA_DEVERR_BLOCK_RANGE);
+      e = -1;
+    }
+    s_ent[i] = e;
+  }
+  if (threadIdx.x < kPxStages) {
+    mbar_init(full_bar(threadIdx.x), 1);
+    mbar_init(empty_bar(threadIdx.x), kPxWarps);
+  }
+  if (threadIdx.x == 0) *s_abort = 0;
+  mbar_init_fence();
+  __syncthreads();
+
+  // every member of this CTA's rows must hold the same blocks in the chunk
+  // (checked by the first KV unit's CTAs only)
+  if (unit == 0) {
+    const int m0 = row0 / G, m1 = min(b - a, (row0 + kPxRows + G - 1) / G);
+    for (int i = threadIdx.x; i < (m1 - m0) * nent; i += kPxThreads) {
+      const int m = m0 + i / nent, j = i % nent;
+      if (m == 0) continue;
+      const int e = p.block_tables[static_cast<int64_t>(a + m) * p.max_blocks_per_seq + j0 + j];
+      if (e != lead[j0 + j]) flag_error(p.debug_err, PA_DEVERR_PREFIX);
+    }
+  }
+
+  const int kvh = kv_head_of(p, unit);
+  const int hkv = p.kv_heads_phys;
+  // TMA of key tile i into stage s: one box per 128-byte column per block
+  // the tile touches; blocks flagged out of range are skipped (their keys
+  // are masked below)
+  auto issue = [&](int i, int s) {
+    const int t0 = k0 + i * kPxTile;
+    const int bh = bs < kPxTile ? bs : kPxTile;  // rows per box
+    const int nsub = kPxTile / bh;
+    uint32_t tx = 0;
+    for (int h = 0; h < nsub; ++h) {
+      const int tok = t0 + h * bh;
+      if (tok >= k1) break;
+      if (s_ent[tok / bs - j0] >= 0) tx += 2u * bh * D * 2;
+    }
+    mbar_arrive_expect_tx(full_bar(s), tx);
+    const uint32_t kdst = stage0 + s * Gm::kStageBytes;
+    const uint32_t vdst = kdst + Gm::kTileBytes;
+    for (int h = 0; h < nsub; ++h) {
+      const int tok = t0 + h * bh;
+      if (tok >= k1) break;
+      const int e = s_ent[tok / bs - j0];
+      if (e < 0) continue;
+      const int z = e * hkv + kvh;
+      const int off = tok & (bs - 1);
+#pragma unroll
+      for (int c = 0; c < Gm::kBoxes; ++c) {
+        tma_load_3d(kdst + c * Gm::kBoxBytes + h * bh * 128, &tmap_k, c * 64, off, z, full_bar(s));
+        tma_load_3d(vdst + c * Gm::kBoxBytes + h * bh * 128, &tmap_v, c * 64, off, z, full_bar(s));
+      }
+    }
+  };
+  if (threadIdx.x == 0)
+    for (int i = 0; i < kPxStages && i < ntiles; ++i) issue(i, i);
+
+  // this warp's rows: gid and gid + 8 of its 16
+  const int r_a = row0 + warp * 16 + gid, r_b = r_a + 8;
+  const bool ok_a = r_a < rows, ok_b = r_b < rows;
+  const int seq_a = a + (ok_a ? r_a / G : 0), seq_b = a + (ok_b ? r_b / G : 0);
+  const int h_a = ok_a ? r_a % G : 0, h_b = ok_b ? r_b % G : 0;
+  const T* qa = static_cast<const T*>(p.q) + (static_cast<int64_t>(seq_a) * p.num_heads + unit * G + h_a) * D;
+  const T* qb = static_cast<const T*>(p.q) + (static_cast<int64_t>(seq_b) * p.num_heads + unit * G + h_b) * D;
+  uint32_t qf[KS][4];
+#pragma unroll
+  for (int k = 0; k < KS; ++k) {
+    qf[k][0] = ok_a ? *reinterpret_cast<const uint32_t*>(qa + 16 * k + 2 * tig) : 0u;
+    qf[k][1] = ok_b ? *reinterpret_cast<const uint32_t*>(qb + 16 * k + 2 * tig) : 0u;
+    qf[k][2] = ok_a ? *reinterpret_cast<const uint32_t*>(qa + 16 * k + 8 + 2 * tig) : 0u;
+    qf[k][3] = ok_b ? *reinterpret_cast<const uint32_t*>(qb + 16 * k + 8 + 2 * tig) : 0u;
+  }
+
+  float o[2 * KS][4];
+#pragma unroll
+  for (int n = 0; n < 2 * KS; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
+
+  for (int i = 0; i < ntiles; ++i) {
+    const int s = i % kPxStages;
+    const uint32_t par = (i / kPxStages) & 1u;
+    const bool got = mbar_wait_bounded(full_bar(s), par);
+    if (!__all_sync(kFullMask, got)) {
+      if (lane == 0) {
+        flag_error(p.debug_err, PA_DEVERR_TIMEOUT);
+        atomicExch(s_abort, 1);
+      }
+      break;
+    }
+    const uint32_t kbase = stage0 + s * Gm::kStageBytes;
+    const uint32_t vbase = kbase + Gm::kTileBytes;
+    const int t0 = k0 + i * kPxTile;
+
+    // S = Q K^T: 16 rows x 16 keys, as two 8-key tiles
+    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int k = 0; k < KS; ++k) {
+      uint32_t r0, r1, r2, r3;
+      ldsm_x4(px_addr<Gm::kBoxBytes>(kbase, (lane >> 4) * 8 + (lane & 7), 2 * k + ((lane >> 3) & 1)),
+              r0, r1, r2, r3);
+      px_mma<T>(sc[0], qf[k], r0, r1);
+      px_mma<T>(sc[1], qf[k], r2, r3);
+    }
+    // keys past the chunk, or in a block flagged out of range, do not count
+    float x_a = -INFINITY, x_b = -INFINITY;
+#pragma unroll
+    for (int n = 0; n < 2; ++n) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int tok = t0 + 8 * n + 2 * tig + e;
+        const bool valid = tok < k1 && s_ent[tok / bs - j0] >= 0;
+        sc[n][e] = valid ? sc[n][e] * p.scale_log2 : -INFINITY;
+        sc[n][2 + e] = valid ? sc[n][2 + e] * p.scale_log2 : -INFINITY;
+        x_a = fmaxf(x_a, sc[n][e]);
+        x_b = fmaxf(x_b, sc[n][2 + e]);
+      }
+    }
+#pragma unroll
+    for (int off = 1; off < 4; off <<= 1) {
+      x_a = fmaxf(x_a, __shfl_xor_sync(kFullMask, x_a, off));
+      x_b = fmaxf(x_b, __shfl_xor_sync(kFullMask, x_b, off));
+    }
+    const float n_a = fmaxf(m_a, x_a), n_b = fmaxf(m_b, x_b);
+    const float al_a = n_a == -INFINITY ? 1.f : exp2f(m_a - n_a);  // 0 while m is -inf
+    const float al_b = n_b == -INFINITY ? 1.f : exp2f(m_b - n_b);
+    m_a = n_a;
+    m_b = n_b;
+    l_a *= al_a;
+    l_b *= al_b;
+#pragma unroll
+    for (int n = 0; n < 2 * KS; ++n) {
+      o[n][0] *= al_a;
+      o[n][1] *= al_a;
+      o[n][2] *= al_b;
+      o[n][3] *= al_b;
+    }
+    const float b_a = m_a == -INFINITY ? 0.f : m_a, b_b = m_b == -INFINITY ? 0.f : m_b;
+    float pr[2][4];
+#pragma unroll
+    for (int n = 0; n < 2; ++n) {
+      pr[n][0] = exp2f(sc[n][0] - b_a);
+      pr[n][1] = exp2f(sc[n][1] - b_a);
+      pr[n][2] = exp2f(sc[n][2] - b_b);
+      pr[n][3] = exp2f(sc[n][3] - b_b);
+      l_a += pr[n][0] + pr[n][1];
+      l_b += pr[n][2] + pr[n][3];
+    }
+    // P as the A operand: rows gid / gid + 8, keys 2tig.. and 8 + 2tig..
+    uint32_t pa4[4];
+    pa4[0] = px_pack(pr[0][0], pr[0][1], static_cast<T*>(nullptr));
+    pa4[1] = px_pack(pr[0][2], pr[0][3], static_cast<T*>(nullptr));
+    pa4[2] = px_pack(pr[1][0], pr[1][1], static_cast<T*>(nullptr));
+    pa4[3] = px_pack(pr[1][2], pr[1][3], static_cast<T*>(nullptr));
+    // O += P V, 16 columns of d per transposed load
+#pragma unroll
+    for (int j = 0; j < KS; ++j) {
+      uint32_t r0, r1, r2, r3;
+      ldsm_x4_trans(px_addr<Gm::kBoxBytes>(vbase, ((lane >> 3) & 1) * 8 + (lane & 7), 2 * j + (lane >> 4)),
+                    r0, r1, r2, r3);
+      px_mma<T>(o[2 * j], pa4, r0, r1);
+      px_mma<T>(o[2 * j + 1], pa4, r2, r3);
+    }
+
+    // stage s is free again: the first thread refills it once both warps are done
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty_bar(s));
+    if (threadIdx.x == 0 && i + kPxStages < ntiles) {
+      // (warp 0 waits here for the other warps to release the stage)
+      if (!mbar_wait_bounded(empty_bar(s), par)) {
+        flag_error(p.debug_err, PA_DEVERR_TIMEOUT);
+        atomicExch(s_abort, 1);
+      } else {
+        fence_proxy_async_smem();
+        issue(i + kPxStages, s);
+      }
+    }
+    __syncwarp();
+    if (*reinterpret_cast<volatile int*>(s_abort)) break;
+  }
+
+  if (*reinterpret_cast<volatile int*>(s_abort) == 0) {
+#pragma unroll
+    for (int off = 1; off < 4; off <<= 1) {
+      l_a += __shfl_xor_sync(kFullMask, l_a, off);
+      l_b += __shfl_xor_sync(kFullMask, l_b, off);
+    }
+    const int stride = state_floats(G, D);
+    const int64_t units = p.num_kv_heads;
+    auto store_row = [&](bool ok, int seq, int h, float m, float l, int upper) {
+      if (!ok) return;
+      float* st = pg.ws_prefix + ((static_cast<int64_t>(seq) * units + unit) * pg.num_chunks + chunk) * stride;
+#pragma unroll
+      for (int n = 0; n < 2 * KS; ++n)
+        *reinterpret_cast<float2*>(st + h * D + 8 * n + 2 * tig) =
+            make_float2(o[n][2 * upper], o[n][2 * upper + 1]);
+      if (tig == 0) {
+        st[G * D + h] = m;
+        st[G * D + G + h] = l;
+      }
+    };
+    store_row(ok_a, seq_a, h_a, m_a, l_a, 0);
+    store_row(ok_b, seq_b, h_b, m_b, l_b, 1);
+  } else if (threadIdx.x == 0) {
+    // give copies still in flight a short while to land before the CTA leaves
+    for (int s = 0; s < kPxStages; ++s) mbar_wait_bounded(full_bar(s), 0, 10000000ull);
+  }
+}
+
+template <typename T, int D>
+cudaError_t launch_px(const PxParams& xp, dim3 grid, cudaStream_t stream) {
+  const DecodeParams& p = xp.p;
+  CUtensorMap mk, mv;
+  const int64_t bxh = static_cast<int64_t>(p.num_blocks) * p.kv_heads_phys;
+  if (!make_cache_map(&mk, p.k_cache, D, 2, p.block_size, kPxTile, bxh) ||
+      !make_cache_map(&mv, p.v_cache, D, 2, p.block_size, kPxTile, bxh))
+    return cudaErrorInvalidValue;
+  auto kernel = prefix_attn_kernel<T, D>;
+  static std::atomic<unsigned long long> attr_set{0};
+  cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(kernel), PxGeom<D>::kSmemBytes, attr_set);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kPxThreads);
+  cfg.dynamicSmemBytes = PxGeom<D>::kSmemBytes;
+  cfg.stream = stream;
+  e = cudaLaunchKernelEx(&cfg, kernel, mk, mv, xp);
+  if (e == cudaSuccess) note_launches(1);
+  return e;
+}
+
+}  // namespace
+
+int prefix_row_tiles(int max_group_size, int group) {
+  return static_cast<int>((static_cast<int64_t>(max_group_size) * group + kPxRows - 1) / kPxRows);
+}
+
+int prefix_max_chunk_len(int block_size) {
+  // the chunk's table entries fit the CTA's shared array
+  return (kPxMaxEntries - 1) * block_size;
+}
+
+cudaError_t launch_prefix_attn(const DecodeParams& p, const PrefixGroups& pg, int head_dim,
+                               pa_dtype dtype, cudaStream_t stream) {
+  PxParams xp{};
+  xp.p = p;
+  xp.pg = pg;
+  xp.group = p.num_heads / p.num_kv_heads;
+  dim3 grid(prefix_row_tiles(pg.max_group_size, xp.group), p.num_kv_heads, pg.num_groups * pg.num_chunks);
+  if (dtype == PA_BF16) {
+    if (head_dim == 128) return launch_px<bf16, 128>(xp, grid, stream);
+    return launch_px<bf16, 64>(xp, grid, stream);
+  }
+  if (head_dim == 128) return launch_px<f16, 128>(xp, grid, stream);
+  return launch_px<f16, 64>(xp, grid, stream);
+}
+
+}  // namespace pa

@@ -75,6 +75,7 @@ struct SlotMeta {
 
 struct TcParams {
   DecodeParams p;
+  PrefixGroups pg;     // shared-prefix groups (group_start == nullptr: none)
   float* ws_slots;     // [6 * num_warps][group * (D + 2)] partial states (auto schedule)
   int32_t* claim;      // chunk counter of the auto schedule: 0 on entry, reset by the merge
   int32_t num_warps;   // warps that share the work
@@ -110,6 +111,35 @@ __device__ __forceinline__ Sched make_sched(int64_t U, int64_t W) {
 template <int box_bytes>
 __device__ __forceinline__ uint32_t tile_addr(uint32_t base, int row, int chunk) {
   return base + (chunk >> 3) * box_bytes + row * 128 + (((chunk & 7) ^ (row & 7)) << 4);
+}
+
+// Tiles of a sequence whose first `start` tokens are left to the shared-prefix
+// kernel: tokens [start - start % TT, ctx) in tiles of TT (the tokens below
+// `start` of the first tile are masked).
+template <int TT>
+__device__ __forceinline__ int seq_tiles(int ctx, int start) {
+  if (ctx <= start) return 0;
+  const int lo = start - start % TT;
+  return (ctx - lo + TT - 1) / TT;
+}
+
+// Shared-prefix tokens of sequence i: the prefix of the group whose range
+// holds it (binary search over group_start, which a valid description keeps
+// non-decreasing), 0 outside every group.
+__device__ __forceinline__ int seq_prefix_len(const PrefixGroups& pg, const DecodeParams& p, int i,
+                                              int& group_len) {
+  group_len = 0;
+  if (pg.group_start == nullptr || pg.num_groups <= 0) return 0;
+  int lo = 0, hi = pg.num_groups - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pg.group_start[mid] <= i) lo = mid; else hi = mid - 1;
+  }
+  int a, b, len;
+  prefix_group(pg, lo, p.num_seqs, p.max_blocks_per_seq, p.block_size, a, b, len);
+  if (i < a || i >= b) return 0;
+  group_len = len;
+  return len;
 }
 
 // Bits [first, first + n) set, n <= 32.
@@ -195,6 +225,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
   int* s_ctx = reinterpret_cast<int*>(bars + kWarps * NS);
   int* s_prefT = s_ctx + B;
   int* s_prefP = s_prefT + B + 1;
+  int* s_start = s_prefP + B + 1;  // tokens of each sequence left to the shared-prefix kernel
+  const bool prefix_mode = tp.pg.group_start != nullptr;
   __shared__ int s_warp_sum[kWarps][2];
 
   if (threadIdx.x < kWarps * NS) mbar_init(smem_u32(&bars[threadIdx.x]), 1);
@@ -207,9 +239,27 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
   const int i1 = min(B, i0 + per);
   int sum_t = 0, sum_p = 0;
   for (int i = i0; i < i1; ++i) {
-    const int ctx = clamp_context(p, i);
-    s_ctx[i] = ctx;
-    const int tl = (ctx + TT - 1) / TT;
+    s_ctx[i] = clamp_context(p, i);
+    s_start[i] = 0;
+  }
+  if (prefix_mode) {
+    // each group's members skip its shared tokens
+    __syncthreads();
+    for (int g = threadIdx.x; g < tp.pg.num_groups; g += kThreads) {
+      int a, b, len;
+      if (prefix_group(tp.pg, g, B, p.max_blocks_per_seq, p.block_size, a, b, len))
+        flag_error(p.debug_err, PA_DEVERR_PREFIX);
+      for (int i = a; i < b; ++i) s_start[i] = len;
+    }
+    __syncthreads();
+  }
+  for (int i = i0; i < i1; ++i) {
+    const int ctx = s_ctx[i];
+    if (s_start[i] > ctx) {
+      flag_error(p.debug_err, PA_DEVERR_PREFIX);  // a member shorter than its group's prefix
+      s_start[i] = ctx;
+    }
+    const int tl = seq_tiles<TT>(ctx, s_start[i]);
     sum_t += tl;
     if (tp.part_tiles) sum_p += (tl + tp.part_tiles - 1) / tp.part_tiles;
   }
@@ -236,7 +286,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
   for (int i = i0; i < i1; ++i) {
     s_prefT[i] = run_t;
     s_prefP[i] = run_p;
-    const int tl = (s_ctx[i] + TT - 1) / TT;
+    const int tl = seq_tiles<TT>(s_ctx[i], s_start[i]);
     run_t += tl;
     if (tp.part_tiles) run_p += (tl + tp.part_tiles - 1) / tp.part_tiles;
   }
@@ -334,8 +384,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
   constexpr int kMaxSub = TT / 8;
   auto issue = [&](const Cursor& c, int s) {
     const int ctx = s_ctx[c.seq];
-    const int tok0 = c.t * TT;
+    const int st = s_start[c.seq];
+    const int tok0 = st - st % TT + c.t * TT;
     const int valid = min(TT, ctx - tok0);
+    const int skip = st > tok0 ? st - tok0 : 0;  // leading tokens of the shared prefix
     const uint32_t kdst = slot_base0 + s * Gm::kSlotBytes;
     const uint32_t vdst = kdst + Gm::kTileBytes;
     const uint32_t bar = bar_base + s * 8;
@@ -350,7 +402,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
       phys[h] = -1;
       ks[h] = vs[h] = 1.f;
       const int first = h * bh;
-      if (h >= nsub || first >= valid) continue;
+      if (h >= nsub || first >= valid || first < skip) continue;  // skip is a multiple of bh
       phys[h] = table_entry(c.seq, c.kvh, (tok0 >> lbs) + h, ks[h], vs[h]);
       if (phys[h] < 0 || phys[h] >= p.num_blocks) {
         if (lane == 0) flag_error(p.debug_err, PA_DEVERR_BLOCK_RANGE);
@@ -442,7 +494,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
       l1 += __shfl_xor_sync(kFull, l1, off);
     }
     const int h0 = 2 * tig, h1 = 2 * tig + 1;
-    if (whole && tp.part_tiles == 0) {
+    if (whole && tp.part_tiles == 0 && s_start[seq] == 0) {
       QT* out = static_cast<QT*>(p.out);
       const float i0 = l0 > 0.f ? 1.f / l0 : 0.f;
       const float i1 = l1 > 0.f ? 1.f / l1 : 0.f;
@@ -508,7 +560,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
       }
     } else {
       // part of a (sequence, KV head) shared with other warps
-      float* base = tp.ws_slots + slot_index * (G * (D + 2));
+      float* base = tp.ws_slots + slot_index * state_floats(G, D);
 #pragma unroll
       for (int k = 0; k < Gm::kSteps; ++k) {
         const int da = d_of(k, 0), db = d_of(k, 1);
@@ -797,7 +849,9 @@ __global__ void __launch_bounds__(NT, 1024 / NT) tc_merge_kernel(const TcParams 
   __shared__ int s_sum[kMergeThreads / 32][2];
   int before = 0, total = 0;
   for (int i = threadIdx.x; i < B; i += kMergeThreads) {
-    const int tl = (clamp_context(p, i) + TT - 1) / TT;
+    int glen;
+    const int ctx = clamp_context(p, i);
+    const int tl = seq_tiles<TT>(ctx, min(seq_prefix_len(tp.pg, p, i, glen), ctx));
     total += tl;
     if (i < seq) before += tl;
   }
@@ -817,8 +871,13 @@ __global__ void __launch_bounds__(NT, 1024 / NT) tc_merge_kernel(const TcParams 
     before += s_sum[w][0];
     total += s_sum[w][1];
   }
-  const int tiles = (clamp_context(p, seq) + TT - 1) / TT;
-  if (tiles == 0) {
+  // the shared-prefix states of this sequence: one per chunk of its group's prefix
+  int plen = 0;
+  const int ctx_self = clamp_context(p, seq);
+  const int start = min(seq_prefix_len(tp.pg, p, seq, plen), ctx_self);
+  const int npre = plen > 0 ? (plen + tp.pg.chunk_len - 1) / tp.pg.chunk_len : 0;
+  const int tiles = seq_tiles<TT>(ctx_self, start);
+  if (tiles == 0 && npre == 0) {
     for (int i = threadIdx.x; i < G * D; i += kMergeThreads) out[i] = from_float(0.f, static_cast<QT*>(nullptr));
     return;
   }
@@ -831,25 +890,28 @@ __global__ void __launch_bounds__(NT, 1024 / NT) tc_merge_kernel(const TcParams 
   // static shares meeting [seg0, min(seg1, S)): warp w holds [w*S/W, (w+1)*S/W),
   // so the owner of tile x < S is ceil((x+1)W/S) - 1
   int64_t ws0 = 0, nstat = 0;
-  if (seg0 < S) {
+  if (tiles > 0 && seg0 < S) {
     const int64_t e = seg1 < S ? seg1 : S;
     ws0 = ((seg0 + 1) * W - 1) / S;
     nstat = (e * W - 1) / S - ws0 + 1;
   }
   // chunks meeting [max(seg0, S), seg1)
   int64_t k0 = 0, ndyn = 0;
-  if (seg1 > S) {
+  if (tiles > 0 && seg1 > S) {
     const int64_t a = seg0 > S ? seg0 : S;
     k0 = (a - S) / C;
     ndyn = (seg1 - 1 - S) / C - k0 + 1;
   }
-  const int nc = static_cast<int>(nstat + ndyn);
-  if (nc == 1) return;  // one range held the whole segment and wrote the rows
+  const int ndec = static_cast<int>(nstat + ndyn);
+  if (ndec == 1 && npre == 0) return;  // one range held the whole segment and wrote the rows
+  const int nc = ndec + npre;
 
   // slot of contributor c: static shares first, then chunks; a range that
   // starts before the segment left it in its second slot; -1 for a warp
   // whose static share is empty (it wrote nothing)
   auto slot_of = [&](int c) -> int {
+    if (c >= ndec)  // a shared-prefix state, stored after the 6W decode states
+      return static_cast<int>(6 * W + (static_cast<int64_t>(seq) * Hkv + kvh) * tp.pg.num_chunks + (c - ndec));
     if (c < nstat) {
       const int64_t w = ws0 + c;
       const int64_t st = w * S / W, en = (w + 1) * S / W;
@@ -866,7 +928,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) tc_merge_kernel(const TcParams 
   __shared__ float s_run[kMaxG], s_den[kMaxG], s_scale[kMaxG];
   __shared__ float4 s_part[kMergeThreads];
   const float* slots = tp.ws_slots;
-  const int stride = G * (D + 2);
+  const int stride = state_floats(G, D);
   const int ne4 = G * D / 4;                 // float4 elements in the block: 32..256
   const int ngrp = kMergeThreads / ne4;      // contributor groups
   const int e4 = threadIdx.x % ne4;
@@ -1022,6 +1084,8 @@ int32_t* next_claim_counter() {
   return g_claim_base[dev] + (g_claim_next.fetch_add(1, std::memory_order_relaxed) % kClaimSlots);
 }
 
+}  // namespace
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static bool tried = false;
@@ -1057,11 +1121,13 @@ bool make_cache_map(CUtensorMap* map, const void* base, int head_dim, int elem, 
   return r == CUDA_SUCCESS;
 }
 
+namespace {
+
 template <typename QT, typename KT, int D, int TT>
 size_t smem_bytes(int num_seqs) {
   using Gm = Geom<KT, D, TT>;
   return 1024 + static_cast<size_t>(kWarps) * Gm::kSlots * (Gm::kSlotBytes + sizeof(SlotMeta) + 8) +
-         (3 * static_cast<size_t>(num_seqs) + 2) * sizeof(int);
+         (4 * static_cast<size_t>(num_seqs) + 2) * sizeof(int);
 }
 
 template <typename QT, typename KT, int D, int TT>
@@ -1079,6 +1145,12 @@ cudaError_t launch_typed(const TcParams& tp, const void* k_cache, const void* v_
                                       static_cast<int>(smem_bytes<QT, KT, D, TT>(kTcMaxSeqs)), attr_set);
   if (e != cudaSuccess) return e;
   const int grid = (tp.num_warps + kWarps - 1) / kWarps;
+  if (tp.pg.group_start != nullptr) {
+    // the shared prefixes first, on the whole GPU; the decode grid that
+    // follows waits for them (griddep_wait) before it starts its work
+    e = launch_prefix_attn(p, tp.pg, D, std::is_same<QT, bf16>::value ? PA_BF16 : PA_F16, stream);
+    if (e != cudaSuccess) return e;
+  }
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -1137,13 +1209,13 @@ size_t tc_auto_workspace_bytes(int num_seqs, int head_dim, int group, int num_sm
   (void)num_seqs;
   // two partial states per static share and per chunk (at most 2W chunks)
   const size_t W = static_cast<size_t>(num_sms) * kWarps;
-  const size_t slots = 6 * W * static_cast<size_t>(group) * (head_dim + 2) * sizeof(float);
+  const size_t slots = 6 * W * static_cast<size_t>(state_floats(group, head_dim)) * sizeof(float);
   return slots;
 }
 
 cudaError_t launch_decode_tc(const DecodeParams& p, int head_dim, pa_dtype q_dtype,
                              pa_dtype kv_dtype, int partition_size, void* workspace, int num_sms,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, const PrefixGroups* groups) {
   const int tt = tc_tile_tokens(kv_dtype);
   const int part_tiles = partition_size / tt;
   TcParams tp{};
@@ -1156,6 +1228,11 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int head_dim, pa_dtype q_dty
     if (tp.claim == nullptr) return cudaErrorInvalidDevice;
     tp.num_warps = tc_num_warps(num_sms, static_cast<int64_t>(p.num_seqs) * p.num_kv_heads * tiles_max);
     tp.ws_slots = static_cast<float*>(workspace);
+    if (groups != nullptr) {
+      // the shared-prefix states follow the 6W decode states
+      tp.pg = *groups;
+      tp.pg.ws_prefix = tp.ws_slots + 6 * static_cast<int64_t>(tp.num_warps) * state_floats(tp.group, head_dim);
+    }
   } else {
     const int64_t parts_max = (tiles_max + part_tiles - 1) / part_tiles;
     tp.num_warps = tc_num_warps(num_sms, static_cast<int64_t>(p.num_seqs) * p.num_kv_heads * parts_max);

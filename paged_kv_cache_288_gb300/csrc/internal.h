@@ -2,6 +2,7 @@
 // C++ (namespace pa); the C-ABI lives in pa_api.cu.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -12,6 +13,7 @@
 namespace pa {
 
 struct DecodeParams;
+struct PrefixGroups;
 
 // Adds n to the process-wide count of kernels launched by this library.
 void note_launches(int n);
@@ -29,6 +31,12 @@ inline cudaError_t set_smem_limit_once(const void* fn, int bytes, std::atomic<un
   if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_relaxed);
   return e;
 }
+
+// 3-D TMA view of a cache [blocks, KV heads, block_size, head_dim] as (d, token
+// in block, block x KV head), boxes of 128 bytes x min(block_size,
+// tile_tokens) rows x 1, 128-byte swizzle (decode_tc.cu).
+bool make_cache_map(CUtensorMap* map, const void* base, int head_dim, int elem, int block_size,
+                    int tile_tokens, int64_t blocks_x_heads);
 
 // Sets the message pa_last_error_message() returns on this thread.
 void set_last_error(const char* fmt, ...);
@@ -91,6 +99,15 @@ bool tc_supported(int group, int head_dim, pa_dtype kv_dtype, int num_seqs, int 
 size_t tc_auto_workspace_bytes(int num_seqs, int head_dim, int group, int num_sms);
 cudaError_t launch_decode_tc(const DecodeParams& p, int head_dim, pa_dtype q_dtype,
                              pa_dtype kv_dtype, int partition_size, void* workspace, int num_sms,
-                             cudaStream_t stream);
+                             cudaStream_t stream, const PrefixGroups* groups = nullptr);
+
+// Shared-prefix attention (decode_prefix.cu): one CTA per (64 rows of a
+// group's members x query heads, KV unit, group x chunk of the prefix),
+// launched before the decode grid of the call; partial states go to
+// groups.ws_prefix.
+int prefix_row_tiles(int max_group_size, int group);
+int prefix_max_chunk_len(int block_size);
+cudaError_t launch_prefix_attn(const DecodeParams& p, const PrefixGroups& groups, int head_dim,
+                               pa_dtype dtype, cudaStream_t stream);
 
 }  // namespace pa

@@ -66,6 +66,35 @@ int current_sm_count() {
   return sms;
 }
 
+// How the shared prefixes are cut: chunks of chunk_len keys (a multiple of
+// 16 and of the block size), so that the prefix grid has about three CTAs
+// per SM (more chunks mean more partial states to write and merge);
+// num_chunks covers the longest prefix.
+struct PrefixPlan {
+  int chunk_len = 0;
+  int num_chunks = 0;
+};
+
+PrefixPlan prefix_plan(int num_groups, int max_group_size, int max_prefix_len, int units, int group,
+                       int block_size, int sms) {
+  PrefixPlan pl;
+  if (num_groups <= 0 || max_group_size <= 0 || max_prefix_len <= 0) return pl;
+  const int64_t per_set = static_cast<int64_t>(pa::prefix_row_tiles(max_group_size, group)) * units * num_groups;
+  const int64_t target = 3 * static_cast<int64_t>(sms > 0 ? sms : 1);
+  int64_t c = (target + per_set - 1) / per_set;
+  const int64_t cmax = (max_prefix_len + 15) / 16;
+  if (c > cmax) c = cmax;
+  if (c < 1) c = 1;
+  const int step = block_size > 16 ? block_size : 16;
+  int64_t len = (max_prefix_len + c - 1) / c;
+  len = (len + step - 1) / step * step;
+  const int64_t cap = pa::prefix_max_chunk_len(block_size) / step * step;
+  if (len > cap) len = cap;
+  pl.chunk_len = static_cast<int>(len);
+  pl.num_chunks = static_cast<int>((max_prefix_len + len - 1) / len);
+  return pl;
+}
+
 }  // namespace
 
 namespace pa {
@@ -300,6 +329,97 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
   }
   return from_cuda(pa::launch_decode_simt(p, head_dim, q_dtype, kv_dtype, stream),
                    "decode launch");
+}
+
+size_t pa_decode_shared_prefix_workspace_size(int32_t num_seqs, int32_t num_heads,
+                                              int32_t num_kv_heads, int32_t head_dim,
+                                              int32_t block_size, int32_t num_groups,
+                                              int32_t max_group_size, int32_t max_prefix_len) {
+  if (num_seqs <= 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+      num_heads % num_kv_heads != 0)
+    return 0;
+  const int sms = current_sm_count();
+  if (sms <= 0) return 0;
+  const int group = unit_group(num_heads / num_kv_heads);
+  const int units = num_heads / group;
+  const size_t dec = pa::tc_auto_workspace_bytes(num_seqs, head_dim, group, sms);
+  const PrefixPlan pl = prefix_plan(num_groups, max_group_size, max_prefix_len, units, group, block_size, sms);
+  const size_t pre = static_cast<size_t>(num_seqs) * units * pl.num_chunks *
+                     pa::state_floats(group, head_dim) * sizeof(float);
+  return dec + pre;
+}
+
+pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t* context_lens, int32_t num_seqs, int32_t num_heads,
+                                  int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                  int32_t num_blocks, float scale, pa_dtype dtype,
+                                  int32_t max_context_len, const int32_t* group_start,
+                                  const int32_t* group_prefix, int32_t num_groups,
+                                  int32_t max_group_size, int32_t max_prefix_len, void* workspace,
+                                  size_t workspace_bytes, int32_t* debug_err, cudaStream_t stream) {
+  const pa_status v = pa::validate_decode_args(
+      out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs, num_heads,
+      num_kv_heads, head_dim, block_size, num_blocks, scale, dtype, dtype, nullptr, nullptr,
+      max_context_len, 0);
+  if (v != PA_OK) return v;
+  if (!is_16bit(dtype)) return fail(PA_ERR_UNSUPPORTED, "shared-prefix decode takes f16 or bf16 caches");
+  if (num_groups < 0 || max_group_size < 0 || max_prefix_len < 0)
+    return fail(PA_ERR_INVALID, "negative group count or bound");
+  if (num_groups > 0 && (group_start == nullptr || group_prefix == nullptr))
+    return fail(PA_ERR_INVALID, "null group arrays");
+  const int group = unit_group(num_heads / num_kv_heads);
+  if (head_dim == 256 || num_seqs > pa::kTcMaxSeqs)
+    return fail(PA_ERR_UNSUPPORTED, "shared-prefix decode takes head_dim 64 or 128 and at most %d sequences",
+                pa::kTcMaxSeqs);
+  if (num_seqs == 0) return PA_OK;
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(PA_ERR_INVALID, "workspace must be a 256-byte aligned device buffer");
+  const size_t need = pa_decode_shared_prefix_workspace_size(
+      num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_groups, max_group_size, max_prefix_len);
+  if (need == 0) return fail(PA_ERR_CUDA, "no current CUDA device");
+  if (workspace_bytes < need)
+    return fail(PA_ERR_WORKSPACE, "shared-prefix decode needs %zu workspace bytes, got %zu", need,
+                workspace_bytes);
+  const int sms = current_sm_count();
+  pa::DecodeParams p{};
+  p.out = out;
+  p.q = q;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.debug_err = debug_err;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.num_seqs = num_seqs;
+  p.num_heads = num_heads;
+  p.kv_div = (num_heads / num_kv_heads) / group;
+  p.kv_heads_phys = num_kv_heads;
+  p.num_kv_heads = num_kv_heads * p.kv_div;
+  p.block_size = block_size;
+  p.num_blocks = num_blocks;
+  p.max_context_len = max_context_len;
+  p.scale_log2 = scale * pa::kLog2e;
+  p.partition_size = 0;
+  p.num_partitions = 1;
+  const PrefixPlan pl = prefix_plan(num_groups, max_group_size, max_prefix_len, p.num_kv_heads, group,
+                                    block_size, sms);
+  if (pl.num_chunks == 0)  // nothing shared: the library's own schedule
+    return from_cuda(pa::launch_decode_tc(p, head_dim, dtype, dtype, 0, workspace, sms, stream),
+                     "decode launch");
+  if (static_cast<int64_t>(num_groups) * pl.num_chunks > 65535 ||
+      pa::prefix_row_tiles(max_group_size, group) > 65535)
+    return fail(PA_ERR_UNSUPPORTED, "too many groups or members for one prefix grid");
+  pa::PrefixGroups pg{};
+  pg.group_start = group_start;
+  pg.group_prefix = group_prefix;
+  pg.num_groups = num_groups;
+  pg.max_group_size = max_group_size;
+  pg.max_prefix_len = max_prefix_len;
+  pg.chunk_len = pl.chunk_len;
+  pg.num_chunks = pl.num_chunks;
+  return from_cuda(pa::launch_decode_tc(p, head_dim, dtype, dtype, 0, workspace, sms, stream, &pg),
+                   "shared-prefix decode launch");
 }
 
 pa_status pa_copy_blocks(void* const* k_caches, void* const* v_caches, int32_t num_layers,

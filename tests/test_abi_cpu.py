@@ -219,3 +219,31 @@ def test_binding_refuses_host_tensors():
     ptrs = torch.zeros(1, dtype=torch.int64)
     with pytest.raises(ValueError, match="CUDA tensor"):
         pa.copy_blocks(ptrs, ptrs, torch.zeros(1, 2, dtype=torch.int64), 4, 4096)
+
+
+def _shared(L, **kw):
+    args = dict(out=16, q=16, k=16, v=16, tables=16, width=16, lens=16, B=4, Hq=8, Hkv=2, d=128,
+                bs=16, Nb=100, scale=0.1, dt=pa.BF16, maxctx=100, gs=16, gp=16, ng=1, mgs=4, mpl=64,
+                ws=256, wsb=1 << 20, err=NULL, stream=NULL)
+    args.update(kw)
+    return L.pa_decode_shared_prefix(
+        args["out"], args["q"], args["k"], args["v"], args["tables"], args["width"], args["lens"],
+        args["B"], args["Hq"], args["Hkv"], args["d"], args["bs"], args["Nb"], args["scale"],
+        args["dt"], args["maxctx"], args["gs"], args["gp"], args["ng"], args["mgs"], args["mpl"],
+        args["ws"], args["wsb"], args["err"], args["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dt=pa.FP8_E4M3), 1),             # 16-bit caches only (q must be 16-bit)
+    (dict(d=256), 2),
+    (dict(Hq=12, Hkv=1), 2),               # group of 12
+    (dict(ng=-1), 1),
+    (dict(mpl=-16), 1),
+    (dict(gs=NULL), 1),                    # groups without their arrays
+    (dict(ws=NULL), 1),
+    (dict(ws=128), 1),                     # workspace not 256-byte aligned
+    (dict(B=3000), 2),                     # more sequences than the tensor-core schedule takes
+    (dict(B=0), 0),
+])
+def test_shared_prefix_argument_checks(L, kw, status):
+    assert _shared(L, **kw) == status, pa.lib().pa_last_error_message()

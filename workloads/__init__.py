@@ -471,3 +471,54 @@ def prefill_llama8b(seed=1011, num_seqs=16, chunk=512, prefix_hi=2048):
     g = _gen(seed)
     pre = torch.randint(0, prefix_hi + 1, (num_seqs,), generator=g).numpy()
     return prefill_case(seed + 1, pre, [chunk] * num_seqs, 32, 8, 128, 16, BF16)
+
+def grouped_prefix_case(seed, group_sizes, prefix_blocks, suffix_lo, suffix_hi, num_heads,
+                        num_kv_heads, head_dim, block_size, dtype, pool_factor=1.25):
+    """Sequences in groups whose tables share their leading blocks.
+
+    Group g has group_sizes[g] consecutive sequences; all of them point their
+    first prefix_blocks[g] table entries at the same physical blocks (random
+    K/V, a seeded permutation of the pool), then own private blocks for a
+    suffix of suffix_lo..suffix_hi tokens. Returns the DecodeCase plus the
+    group description (group_start [G + 1], group_prefix [G] in tokens).
+    """
+    g = _gen(seed)
+    bs = block_size
+    B = int(sum(group_sizes))
+    suffix = torch.randint(suffix_lo, suffix_hi + 1, (B,), generator=g).numpy().astype(np.int64)
+    pre_tok = np.repeat(np.asarray(prefix_blocks, dtype=np.int64) * bs, group_sizes)
+    ctx = pre_tok + suffix
+    nbs = [int(-(-c // bs)) for c in ctx]
+    need = int(sum(prefix_blocks)) + sum(nb - int(p // bs) for nb, p in zip(nbs, pre_tok))
+    num_blocks = max(int(math.ceil(pool_factor * need)), need) + 1
+    perm = torch.randperm(num_blocks, generator=g).numpy().astype(np.int64)
+    poison = int(perm[-1])
+    width = max(max(nbs), 1)
+    tables = np.full((B, width), poison, dtype=np.int32)
+    cursor = 0
+    i = 0
+    for gsize, pb in zip(group_sizes, prefix_blocks):
+        shared = perm[cursor:cursor + pb]
+        cursor += pb
+        for _ in range(gsize):
+            tables[i, :pb] = shared
+            own = nbs[i] - pb
+            tables[i, pb:pb + own] = perm[cursor:cursor + own]
+            cursor += own
+            i += 1
+    shape = (num_blocks, num_kv_heads, bs, head_dim)
+    k_cache = normal_bits(g, shape, dtype)
+    v_cache = normal_bits(g, shape, dtype)
+    k_cache[poison] = NAN_BITS[dtype]
+    v_cache[poison] = NAN_BITS[dtype]
+    _poison_tails(k_cache, tables, ctx, bs, dtype)
+    _poison_tails(v_cache, tables, ctx, bs, dtype)
+    q = normal_bits(g, (B, num_heads, head_dim), dtype)
+    case = DecodeCase(
+        name="grouped_prefix", num_seqs=B, num_heads=num_heads, num_kv_heads=num_kv_heads,
+        head_dim=head_dim, block_size=bs, num_blocks=num_blocks, q_dtype=dtype, kv_dtype=dtype,
+        scale=1.0 / math.sqrt(head_dim), q=q, k_cache=k_cache, v_cache=v_cache,
+        block_tables=tables, context_lens=ctx.astype(np.int32), poison_block=poison)
+    group_start = np.concatenate([[0], np.cumsum(group_sizes)]).astype(np.int32)
+    group_prefix = (np.asarray(prefix_blocks, dtype=np.int64) * bs).astype(np.int32)
+    return case, group_start, group_prefix

@@ -231,13 +231,20 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_cons
       px_mma<T>(sc[1], qf[k], r2, r3);
     }
     // keys past the chunk, or in a block flagged out of range, do not count
+    // (their rows of the stage hold stale data: scores are replaced, values
+    // zeroed below, so no NaN or infinity there reaches O)
+    uint32_t vmask = 0;  // bit k: key t0 + k is valid
+#pragma unroll
+    for (int k = 0; k < kPxTile; k += 8) {
+      const int tok = t0 + k;
+      if (tok < k1 && s_ent[tok / bs - j0] >= 0) vmask |= (tok + 8 <= k1 ? 0xffu : ((1u << (k1 - tok)) - 1u)) << k;
+    }
     float x_a = -INFINITY, x_b = -INFINITY;
 #pragma unroll
     for (int n = 0; n < 2; ++n) {
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const int tok = t0 + 8 * n + 2 * tig + e;
-        const bool valid = tok < k1 && s_ent[tok / bs - j0] >= 0;
+        const bool valid = (vmask >> (8 * n + 2 * tig + e)) & 1u;
         sc[n][e] = valid ? sc[n][e] * p.scale_log2 : -INFINITY;
         sc[n][2 + e] = valid ? sc[n][2 + e] * p.scale_log2 : -INFINITY;
         x_a = fmaxf(x_a, sc[n][e]);
@@ -286,6 +293,17 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_cons
       uint32_t r0, r1, r2, r3;
       ldsm_x4_trans(px_addr<Gm::kBoxBytes>(vbase, ((lane >> 3) & 1) * 8 + (lane & 7), 2 * j + (lane >> 4)),
                     r0, r1, r2, r3);
+      if (vmask != 0xffffu) {
+        // r0, r2 hold keys 2tig, 2tig + 1; r1, r3 keys 8 + 2tig, 9 + 2tig
+        const uint32_t lo = ((vmask >> (2 * tig)) & 1u ? 0x0000ffffu : 0u) |
+                            ((vmask >> (2 * tig + 1)) & 1u ? 0xffff0000u : 0u);
+        const uint32_t hi = ((vmask >> (8 + 2 * tig)) & 1u ? 0x0000ffffu : 0u) |
+                            ((vmask >> (9 + 2 * tig)) & 1u ? 0xffff0000u : 0u);
+        r0 &= lo;
+        r2 &= lo;
+        r1 &= hi;
+        r3 &= hi;
+      }
       px_mma<T>(o[2 * j], pa4, r0, r1);
       px_mma<T>(o[2 * j + 1], pa4, r2, r3);
     }

@@ -225,8 +225,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
   int* s_ctx = reinterpret_cast<int*>(bars + kWarps * NS);
   int* s_prefT = s_ctx + B;
   int* s_prefP = s_prefT + B + 1;
-  int* s_start = s_prefP + B + 1;  // tokens of each sequence left to the shared-prefix kernel
+  // tokens of each sequence left to the shared-prefix kernel; only with groups,
+  // which never come with a forced partition size, so it reuses s_prefP
   const bool prefix_mode = tp.pg.group_start != nullptr;
+  int* s_start = s_prefP;
+  auto start_of = [&](int i) -> int { return prefix_mode ? s_start[i] : 0; };
   __shared__ int s_warp_sum[kWarps][2];
 
   if (threadIdx.x < kWarps * NS) mbar_init(smem_u32(&bars[threadIdx.x]), 1);
@@ -240,7 +243,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
   int sum_t = 0, sum_p = 0;
   for (int i = i0; i < i1; ++i) {
     s_ctx[i] = clamp_context(p, i);
-    s_start[i] = 0;
+    if (prefix_mode) s_start[i] = 0;
   }
   if (prefix_mode) {
     // each group's members skip its shared tokens
@@ -255,11 +258,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
   }
   for (int i = i0; i < i1; ++i) {
     const int ctx = s_ctx[i];
-    if (s_start[i] > ctx) {
+    if (prefix_mode && s_start[i] > ctx) {
       flag_error(p.debug_err, PA_DEVERR_PREFIX);  // a member shorter than its group's prefix
       s_start[i] = ctx;
     }
-    const int tl = seq_tiles<TT>(ctx, s_start[i]);
+    const int tl = seq_tiles<TT>(ctx, start_of(i));
     sum_t += tl;
     if (tp.part_tiles) sum_p += (tl + tp.part_tiles - 1) / tp.part_tiles;
   }
@@ -284,15 +287,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     run_p += s_warp_sum[w][1];
   }
   for (int i = i0; i < i1; ++i) {
+    const int tl = seq_tiles<TT>(s_ctx[i], start_of(i));
     s_prefT[i] = run_t;
-    s_prefP[i] = run_p;
-    const int tl = seq_tiles<TT>(s_ctx[i], s_start[i]);
+    if (tp.part_tiles) s_prefP[i] = run_p;
     run_t += tl;
     if (tp.part_tiles) run_p += (tl + tp.part_tiles - 1) / tp.part_tiles;
   }
   if (threadIdx.x == kThreads - 1) {
     s_prefT[B] = run_t;
-    s_prefP[B] = run_p;
+    if (tp.part_tiles) s_prefP[B] = run_p;
   }
   __syncthreads();
   griddep_launch_dependents();
@@ -384,7 +387,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
   constexpr int kMaxSub = TT / 8;
   auto issue = [&](const Cursor& c, int s) {
     const int ctx = s_ctx[c.seq];
-    const int st = s_start[c.seq];
+    const int st = start_of(c.seq);
     const int tok0 = st - st % TT + c.t * TT;
     const int valid = min(TT, ctx - tok0);
     const int skip = st > tok0 ? st - tok0 : 0;  // leading tokens of the shared prefix
@@ -494,7 +497,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
       l1 += __shfl_xor_sync(kFull, l1, off);
     }
     const int h0 = 2 * tig, h1 = 2 * tig + 1;
-    if (whole && tp.part_tiles == 0 && s_start[seq] == 0) {
+    const bool prefixed = start_of(seq) > 0;
+    if (whole && prefixed) {
+      // a whole segment of a sequence with a shared prefix: its own state
+      // slot, after the decode and shared-prefix states
+      slot_index = 6 * static_cast<int64_t>(tp.num_warps) +
+                   static_cast<int64_t>(B) * Hkv * tp.pg.num_chunks + static_cast<int64_t>(seq) * Hkv + kvh;
+    }
+    if (whole && tp.part_tiles == 0 && !prefixed) {
       QT* out = static_cast<QT*>(p.out);
       const float i0 = l0 > 0.f ? 1.f / l0 : 0.f;
       const float i1 = l1 > 0.f ? 1.f / l1 : 0.f;
@@ -905,6 +915,9 @@ __global__ void __launch_bounds__(NT, 1024 / NT) tc_merge_kernel(const TcParams 
   const int ndec = static_cast<int>(nstat + ndyn);
   if (ndec == 1 && npre == 0) return;  // one range held the whole segment and wrote the rows
   const int nc = ndec + npre;
+  // a whole segment of a sequence with a shared prefix left its state in the
+  // sequence's own slot, after the decode and shared-prefix states
+  const bool own_slot = ndec == 1 && start > 0;
 
   // slot of contributor c: static shares first, then chunks; a range that
   // starts before the segment left it in its second slot; -1 for a warp
@@ -912,6 +925,9 @@ __global__ void __launch_bounds__(NT, 1024 / NT) tc_merge_kernel(const TcParams 
   auto slot_of = [&](int c) -> int {
     if (c >= ndec)  // a shared-prefix state, stored after the 6W decode states
       return static_cast<int>(6 * W + (static_cast<int64_t>(seq) * Hkv + kvh) * tp.pg.num_chunks + (c - ndec));
+    if (own_slot)
+      return static_cast<int>(6 * W + static_cast<int64_t>(B) * Hkv * tp.pg.num_chunks +
+                              static_cast<int64_t>(seq) * Hkv + kvh);
     if (c < nstat) {
       const int64_t w = ws0 + c;
       const int64_t st = w * S / W, en = (w + 1) * S / W;
@@ -1127,7 +1143,7 @@ template <typename QT, typename KT, int D, int TT>
 size_t smem_bytes(int num_seqs) {
   using Gm = Geom<KT, D, TT>;
   return 1024 + static_cast<size_t>(kWarps) * Gm::kSlots * (Gm::kSlotBytes + sizeof(SlotMeta) + 8) +
-         (4 * static_cast<size_t>(num_seqs) + 2) * sizeof(int);
+         (3 * static_cast<size_t>(num_seqs) + 2) * sizeof(int);
 }
 
 template <typename QT, typename KT, int D, int TT>

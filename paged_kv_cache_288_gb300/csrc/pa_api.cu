@@ -344,7 +344,9 @@ size_t pa_decode_shared_prefix_workspace_size(int32_t num_seqs, int32_t num_head
   const int units = num_heads / group;
   const size_t dec = pa::tc_auto_workspace_bytes(num_seqs, head_dim, group, sms);
   const PrefixPlan pl = prefix_plan(num_groups, max_group_size, max_prefix_len, units, group, block_size, sms);
-  const size_t pre = static_cast<size_t>(num_seqs) * units * pl.num_chunks *
+  // a state per (sequence, unit, chunk) of the shared prefixes, and one per
+  // (sequence, unit) for suffixes that one warp holds whole
+  const size_t pre = static_cast<size_t>(num_seqs) * units * (pl.num_chunks + 1) *
                      pa::state_floats(group, head_dim) * sizeof(float);
   return dec + pre;
 }

@@ -139,9 +139,10 @@ pa_status pa_reshape_and_cache(const void* key, const void* value, void* k_cache
  * with the codes widened to f16: a q value beyond the f16 range (|q| > 65504)
  * becomes infinite, which the kernel reports with PA_DEVERR_Q_RANGE.
  *
- * Calls that overlap on the GPU: with partition_size = 0 and a workspace,
- * each call takes one of 256 work counters inside the library, in turn, and
- * its last kernel sets it back to zero. Calls on one stream never overlap.
+ * Calls that overlap on the GPU: a call on the tensor-core path (groups of
+ * up to 8 query heads per KV unit, head_dim 64 or 128, with a workspace)
+ * takes one of 256 work counters inside the library, in turn, and its last
+ * kernel sets it back to zero. Calls on one stream never overlap.
  * Two calls that run at the same time on the GPU (on different streams or
  * from several threads) share a counter when they were issued a multiple of
  * 256 calls apart, and every replay of a captured graph uses the counter its

@@ -88,6 +88,7 @@ struct DecodeParams {
   float* ws_acc;   // [num_seqs, num_heads, num_partitions, head_dim] normalised partial outputs
   float* ws_ml;    // [num_seqs, num_heads, num_partitions, 2] (max in log2 units, sum)
   int32_t* debug_err;
+  int32_t* claim;           // work counter the partition reduce rearms (tensor-core split path), or null
   int32_t max_blocks_per_seq;
   int32_t num_seqs;
   int32_t num_heads;

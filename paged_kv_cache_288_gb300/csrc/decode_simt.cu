@@ -209,6 +209,8 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_partitions_kernel(const
   constexpr int kBatch = 4;       // row loads a thread keeps in flight
   constexpr int kWarpsR = NT / 32;
   griddep_wait();
+  // the partition kernel is complete: rearm its work counter for the next call
+  if (p.claim != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *p.claim = 0;
   const int h = blockIdx.x;
   const int seq = blockIdx.y;
   const int ctx = clamp_context(p, seq);

@@ -307,6 +307,20 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
   const int64_t U = static_cast<int64_t>(s_prefT[B]) * Hkv;
   int64_t f0, f1;
   int64_t S = U, C = 1, K = 0;  // static tiles, chunk size, chunks
+  // split path: whole partitions; partition index -> its first tile
+  const int64_t US = tp.part_tiles ? static_cast<int64_t>(s_prefP[B]) * Hkv : 0;
+  auto part_to_tile = [&](int64_t s) -> int64_t {
+    if (s >= US) return U;
+    const int seq = find_seq(s_prefP, B, Hkv, s);
+    const int np = s_prefP[seq + 1] - s_prefP[seq];
+    const int64_t r = s - static_cast<int64_t>(s_prefP[seq]) * Hkv;
+    const int kvh = static_cast<int>(r / np);
+    const int pi = static_cast<int>(r % np);
+    const int tiles = s_prefT[seq + 1] - s_prefT[seq];
+    return static_cast<int64_t>(s_prefT[seq]) * Hkv + static_cast<int64_t>(kvh) * tiles +
+           static_cast<int64_t>(pi) * tp.part_tiles;
+  };
+  int64_t SP = 0;  // split path: partitions shared out statically
   if (tp.part_tiles == 0) {
     const Sched sc = make_sched(U, W);
     S = sc.S;
@@ -315,21 +329,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     f0 = wid * S / W;
     f1 = (wid + 1) * S / W;
   } else {
-    // whole partitions: convert partition indices to tile indices
-    const int64_t US = static_cast<int64_t>(s_prefP[B]) * Hkv;
-    auto part_to_tile = [&](int64_t s) -> int64_t {
-      if (s >= US) return U;
-      const int seq = find_seq(s_prefP, B, Hkv, s);
-      const int np = s_prefP[seq + 1] - s_prefP[seq];
-      const int64_t r = s - static_cast<int64_t>(s_prefP[seq]) * Hkv;
-      const int kvh = static_cast<int>(r / np);
-      const int pi = static_cast<int>(r % np);
-      const int tiles = s_prefT[seq + 1] - s_prefT[seq];
-      return static_cast<int64_t>(s_prefT[seq]) * Hkv + static_cast<int64_t>(kvh) * tiles +
-             static_cast<int64_t>(pi) * tp.part_tiles;
-    };
-    f0 = part_to_tile(wid * US / W);
-    f1 = part_to_tile((wid + 1) * US / W);
+    // the first kStatic256/256 of the partitions in equal shares, the rest
+    // claimed one partition at a time by warps whose share is done (SMs
+    // stream at different rates)
+    SP = tp.claim != nullptr ? US * kStatic256 / 256 : US;
+    K = US - SP;
+    f0 = part_to_tile(wid * SP / W);
+    f1 = part_to_tile((wid + 1) * SP / W);
   }
   // claim the next chunk of the shared tail: its tile range and first slot
   auto claim = [&](int64_t& r0, int64_t& r1, int64_t& slot0) -> bool {
@@ -338,6 +344,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     if (lane == 0) k = atomicAdd(tp.claim, 1);
     k = __shfl_sync(kFull, k, 0);
     if (k >= K) return false;
+    if (tp.part_tiles) {
+      r0 = part_to_tile(SP + k);
+      r1 = part_to_tile(SP + k + 1);
+      slot0 = 0;  // partitions write their own partials
+      return true;
+    }
     r0 = S + static_cast<int64_t>(k) * C;
     r1 = r0 + C < U ? r0 + C : U;
     slot0 = 2 * W + 2 * static_cast<int64_t>(k);
@@ -1180,9 +1192,12 @@ cudaError_t launch_typed(const TcParams& tp, const void* k_cache, const void* v_
   cudaError_t err = cudaLaunchKernelEx(&cfg, kernel, mk, mv, tp);
   if (err != cudaSuccess) return err;
   note_launches(1);
-  if (tp.part_tiles != 0)
-    return launch_reduce_partitions(p, D, std::is_same<QT, bf16>::value ? PA_BF16 : PA_F16,
-                                    /*pdl=*/true, stream);
+  if (tp.part_tiles != 0) {
+    err = launch_reduce_partitions(p, D, std::is_same<QT, bf16>::value ? PA_BF16 : PA_F16,
+                                   /*pdl=*/true, stream);
+    if (err != cudaSuccess) cudaMemsetAsync(tp.claim, 0, sizeof(int32_t), stream);  // rearm it ourselves
+    return err;
+  }
   cudaLaunchConfig_t mcfg = cfg;
   mcfg.gridDim = dim3(p.num_kv_heads, p.num_seqs);
   mcfg.dynamicSmemBytes = 0;
@@ -1252,6 +1267,10 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int head_dim, pa_dtype q_dty
   } else {
     const int64_t parts_max = (tiles_max + part_tiles - 1) / part_tiles;
     tp.num_warps = tc_num_warps(num_sms, static_cast<int64_t>(p.num_seqs) * p.num_kv_heads * parts_max);
+    // the tail of the partitions is claimed from a counter the reduce rearms
+    tp.claim = next_claim_counter();
+    if (tp.claim == nullptr) return cudaErrorInvalidDevice;
+    tp.p.claim = tp.claim;
   }
   const void* kc = p.k_cache;
   const void* vc = p.v_cache;

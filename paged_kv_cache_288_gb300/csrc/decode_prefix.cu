@@ -81,7 +81,7 @@ __device__ __forceinline__ void px_mma(float (&d)[4], const uint32_t (&a)[4], ui
 }
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kPxThreads)
+__global__ void __launch_bounds__(kPxThreads, 4)
 prefix_attn_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                    const PxParams xp) {
   using Gm = PxGeom<D>;
@@ -121,11 +121,13 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_cons
   const int j0 = k0 / bs;
   const int nent = (k1 - 1) / bs - j0 + 1;  // <= chunk_len / bs + 1 <= kPxMaxEntries
   const int32_t* lead = p.block_tables + static_cast<int64_t>(a) * p.max_blocks_per_seq;
+  bool bad = false;
   for (int i = threadIdx.x; i < nent; i += kPxThreads) {
     int e = lead[j0 + i];
     if (e < 0 || e >= p.num_blocks) {
       flag_error(p.debug_err, PA_DEVERR_BLOCK_RANGE);
       e = -1;
+      bad = true;
     }
     s_ent[i] = e;
   }
@@ -135,7 +137,9 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_cons
   }
   if (threadIdx.x == 0) *s_abort = 0;
   mbar_init_fence();
-  __syncthreads();
+  // every block of the chunk in range: tiles inside the chunk need no masks
+  const bool all_valid = __syncthreads_and(!bad);
+  const int lbs = 31 - __clz(bs);  // block sizes are powers of two
 
   // every member of this CTA's rows must hold the same blocks in the chunk
   // (checked by the first KV unit's CTAs only)
@@ -230,45 +234,54 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_cons
       px_mma<T>(sc[0], qf[k], r0, r1);
       px_mma<T>(sc[1], qf[k], r2, r3);
     }
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sc[n][e] *= p.scale_log2;
     // keys past the chunk, or in a block flagged out of range, do not count
     // (their rows of the stage hold stale data: scores are replaced, values
     // zeroed below, so no NaN or infinity there reaches O)
-    uint32_t vmask = 0;  // bit k: key t0 + k is valid
+    uint32_t vmask = 0xffffu;  // bit k: key t0 + k is valid
+    if (!all_valid || t0 + kPxTile > k1) {
+      vmask = 0;
 #pragma unroll
-    for (int k = 0; k < kPxTile; k += 8) {
-      const int tok = t0 + k;
-      if (tok < k1 && s_ent[tok / bs - j0] >= 0) vmask |= (tok + 8 <= k1 ? 0xffu : ((1u << (k1 - tok)) - 1u)) << k;
-    }
-    float x_a = -INFINITY, x_b = -INFINITY;
-#pragma unroll
-    for (int n = 0; n < 2; ++n) {
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const bool valid = (vmask >> (8 * n + 2 * tig + e)) & 1u;
-        sc[n][e] = valid ? sc[n][e] * p.scale_log2 : -INFINITY;
-        sc[n][2 + e] = valid ? sc[n][2 + e] * p.scale_log2 : -INFINITY;
-        x_a = fmaxf(x_a, sc[n][e]);
-        x_b = fmaxf(x_b, sc[n][2 + e]);
+      for (int k = 0; k < kPxTile; k += 8) {
+        const int tok = t0 + k;
+        if (tok < k1 && s_ent[(tok >> lbs) - j0] >= 0)
+          vmask |= (tok + 8 <= k1 ? 0xffu : ((1u << (k1 - tok)) - 1u)) << k;
       }
+#pragma unroll
+      for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const bool valid = (vmask >> (8 * n + 2 * tig + e)) & 1u;
+          sc[n][e] = valid ? sc[n][e] : -INFINITY;
+          sc[n][2 + e] = valid ? sc[n][2 + e] : -INFINITY;
+        }
     }
+    float x_a = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
+    float x_b = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
 #pragma unroll
     for (int off = 1; off < 4; off <<= 1) {
       x_a = fmaxf(x_a, __shfl_xor_sync(kFullMask, x_a, off));
       x_b = fmaxf(x_b, __shfl_xor_sync(kFullMask, x_b, off));
     }
-    const float n_a = fmaxf(m_a, x_a), n_b = fmaxf(m_b, x_b);
-    const float al_a = n_a == -INFINITY ? 1.f : exp2f(m_a - n_a);  // 0 while m is -inf
-    const float al_b = n_b == -INFINITY ? 1.f : exp2f(m_b - n_b);
-    m_a = n_a;
-    m_b = n_b;
-    l_a *= al_a;
-    l_b *= al_b;
+    // rescale O only when some row's maximum grew (rarely, once the maxima settle)
+    if (__any_sync(kFullMask, x_a > m_a || x_b > m_b)) {
+      const float n_a = fmaxf(m_a, x_a), n_b = fmaxf(m_b, x_b);
+      const float al_a = n_a == -INFINITY ? 1.f : exp2f(m_a - n_a);  // 0 while m is -inf
+      const float al_b = n_b == -INFINITY ? 1.f : exp2f(m_b - n_b);
+      m_a = n_a;
+      m_b = n_b;
+      l_a *= al_a;
+      l_b *= al_b;
 #pragma unroll
-    for (int n = 0; n < 2 * KS; ++n) {
-      o[n][0] *= al_a;
-      o[n][1] *= al_a;
-      o[n][2] *= al_b;
-      o[n][3] *= al_b;
+      for (int n = 0; n < 2 * KS; ++n) {
+        o[n][0] *= al_a;
+        o[n][1] *= al_a;
+        o[n][2] *= al_b;
+        o[n][3] *= al_b;
+      }
     }
     const float b_a = m_a == -INFINITY ? 0.f : m_a, b_b = m_b == -INFINITY ? 0.f : m_b;
     float pr[2][4];

@@ -67,8 +67,8 @@ int current_sm_count() {
 }
 
 // How the shared prefixes are cut: chunks of chunk_len keys (a multiple of
-// 16 and of the block size), so that the prefix grid has about three CTAs
-// per SM (more chunks mean more partial states to write and merge);
+// 16 and of the block size), so that the prefix grid has about two CTAs per
+// SM, one wave (more chunks mean more partial states to write and merge);
 // num_chunks covers the longest prefix.
 struct PrefixPlan {
   int chunk_len = 0;
@@ -80,7 +80,7 @@ PrefixPlan prefix_plan(int num_groups, int max_group_size, int max_prefix_len, i
   PrefixPlan pl;
   if (num_groups <= 0 || max_group_size <= 0 || max_prefix_len <= 0) return pl;
   const int64_t per_set = static_cast<int64_t>(pa::prefix_row_tiles(max_group_size, group)) * units * num_groups;
-  const int64_t target = 3 * static_cast<int64_t>(sms > 0 ? sms : 1);
+  const int64_t target = 2 * static_cast<int64_t>(sms > 0 ? sms : 1);
   int64_t c = (target + per_set - 1) / per_set;
   const int64_t cmax = (max_prefix_len + 15) / 16;
   if (c > cmax) c = cmax;

@@ -367,44 +367,22 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
   const uint32_t bar_base = smem_u32(bars + warp * NS);
 
   // block-table window: lane l holds entry win_base + l of sequence win_seq
-  // and, for E4M3 caches, that block's K and V scales for KV head win_kvh.
-  // The window of the producer's next segment is read ahead into pw_* (and
-  // its scales a tile later), so a segment switch does not wait for it.
+  // and, for E4M3 caches, that block's K and V scales for KV head win_kvh
   int win_seq = -1, win_base = 0, win_val = -1, win_kvh = -1;
   float win_ks = 1.f, win_vs = 1.f;
-  int pw_seq = -1, pw_base = 0, pw_val = -1, pw_kvh = -1;
-  float pw_ks = 1.f, pw_vs = 1.f;
-  auto window_load = [&](int seq, int j) -> int {
-    const int jj = j + lane;
-    return jj < width ? p.block_tables[static_cast<int64_t>(seq) * width + jj] : -1;
-  };
-  auto scale_index = [&](int val, int kvh) -> int64_t {
-    const bool ok = val >= 0 && val < p.num_blocks;
-    return static_cast<int64_t>(ok ? val : 0) * p.kv_heads_phys + kv_head_of(p, kvh);
-  };
   auto table_entry = [&](int seq, int kvh, int j, float& ksc, float& vsc) -> int {
     if (seq != win_seq || j < win_base || j >= win_base + 32) {
-      if (seq == pw_seq && j == pw_base) {
-        // the window read ahead
-        win_seq = pw_seq;
-        win_base = pw_base;
-        win_val = pw_val;
-        win_kvh = pw_kvh;
-        win_ks = pw_ks;
-        win_vs = pw_vs;
-        pw_seq = -1;
-      } else {
-        win_seq = seq;
-        win_base = j;
-        win_kvh = -1;
-        win_val = window_load(seq, j);
-      }
+      win_seq = seq;
+      win_base = j;
+      win_kvh = -1;
+      const int jj = j + lane;
+      win_val = jj < width ? p.block_tables[static_cast<int64_t>(seq) * width + jj] : -1;
     }
     if constexpr (kFp8) {
       if (kvh != win_kvh) {
         win_kvh = kvh;
         const bool ok = win_val >= 0 && win_val < p.num_blocks;
-        const int64_t si = scale_index(win_val, kvh);
+        const int64_t si = static_cast<int64_t>(ok ? win_val : 0) * p.kv_heads_phys + kv_head_of(p, kvh);
         win_ks = ok ? p.k_scale[si] : 1.f;
         win_vs = ok ? p.v_scale[si] : 1.f;
       }
@@ -412,18 +390,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
       vsc = __shfl_sync(kFull, win_vs, j - win_base);
     }
     return __shfl_sync(kFull, win_val, j - win_base);
-  };
-  // read ahead the window of the tile under cursor n (the producer's next
-  // one) unless the current window already holds its block
-  auto window_ahead = [&](const Cursor& n) {
-    const int st = start_of(n.seq);
-    const int j = (st - st % TT + n.t * TT) >> lbs;
-    if ((n.seq == win_seq && j >= win_base && j < win_base + 32) || (n.seq == pw_seq && j == pw_base))
-      return;
-    pw_seq = n.seq;
-    pw_base = j;
-    pw_kvh = -1;
-    pw_val = window_load(n.seq, j);
   };
 
   // Issue the TMA loads of the tile under `c` into slot `s` (whole warp):
@@ -495,45 +461,26 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
   // q of one (sequence, KV head) as MMA B fragments: column g = query head
   // kvh*G + g (zero for g >= G); 16-bit caches contract d in order, E4M3
   // caches in the permuted order their K fragments arrive in.
-  // The next piece's q is read into qn while the current piece's last tile
-  // is processed (raw 16-bit values), then moved into qb.
-  uint32_t qb[Gm::kSteps][2], qn[Gm::kSteps][2];
-  auto prefetch_q = [&](int seq, int kvh) {
+  uint32_t qb[Gm::kSteps][2];
+  auto load_q = [&](int seq, int kvh) {
     const QT* qrow = static_cast<const QT*>(p.q) + (static_cast<int64_t>(seq) * Hq + kvh * G + g) * D;
 #pragma unroll
     for (int k = 0; k < Gm::kSteps; ++k) {
       if (g >= G) {
-        qn[k][0] = qn[k][1] = 0u;
+        qb[k][0] = qb[k][1] = 0u;
       } else if constexpr (!kFp8) {
-        qn[k][0] = *reinterpret_cast<const uint32_t*>(qrow + 16 * k + 2 * tig);
-        qn[k][1] = *reinterpret_cast<const uint32_t*>(qrow + 16 * k + 8 + 2 * tig);
+        qb[k][0] = *reinterpret_cast<const uint32_t*>(qrow + 16 * k + 2 * tig);
+        qb[k][1] = *reinterpret_cast<const uint32_t*>(qrow + 16 * k + 8 + 2 * tig);
       } else {
-        const uint2 v = *reinterpret_cast<const uint2*>(qrow + 16 * k + 4 * tig);
-        qn[k][0] = v.x;
-        qn[k][1] = v.y;
-      }
-    }
-  };
-  auto commit_q = [&]() {
-#pragma unroll
-    for (int k = 0; k < Gm::kSteps; ++k) {
-      if constexpr (!kFp8) {
-        qb[k][0] = qn[k][0];
-        qb[k][1] = qn[k][1];
-      } else {
-        float2 a = pair_to_float2(qn[k][0], static_cast<QT*>(nullptr));
-        float2 b = pair_to_float2(qn[k][1], static_cast<QT*>(nullptr));
-        qb[k][0] = pack_f16(a.x, a.y);
-        qb[k][1] = pack_f16(b.x, b.y);
+        float f[4];
+        load_float<QT, 4>(qrow + 16 * k + 4 * tig, f);
+        qb[k][0] = pack_f16(f[0], f[1]);
+        qb[k][1] = pack_f16(f[2], f[3]);
         // beyond the f16 range q turns infinite: report it
-        if (fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(b.x), fabsf(b.y))) > 65504.f)
+        if (fmaxf(fmaxf(fabsf(f[0]), fabsf(f[1])), fmaxf(fabsf(f[2]), fabsf(f[3]))) > 65504.f)
           flag_error(p.debug_err, PA_DEVERR_Q_RANGE);
       }
     }
-  };
-  auto load_q = [&](int seq, int kvh) {
-    prefetch_q(seq, kvh);
-    commit_q();
   };
 
   // online-softmax state of the current piece: this lane's two heads
@@ -683,12 +630,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
         have_next = true;
         pr1 = b;
         cursor_at(pc, a, s_prefT, B, Hkv);
-        window_ahead(pc);
       } else {
         prod_done = true;
       }
-    } else if (pc.t == 0) {
-      window_ahead(pc);  // a new segment: its table row a slot ahead of its loads
     }
   };
   int pending = 0;
@@ -713,22 +657,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     }
     parity ^= 1u << s;
     --pending;
-    // this tile ends its piece's (sequence, KV head): read the next one's q now
-    bool q_ahead = false;
-    if (cc.t + 1 == cc.tiles || cc.f + 1 == cr1) {
-      Cursor nx = cc;
-      bool more = true;
-      if (cc.f + 1 == cr1) {
-        if (have_next) cursor_at(nx, nr0, s_prefT, B, Hkv);
-        else more = false;
-      } else {
-        cursor_next(nx, s_prefT, B, Hkv);
-      }
-      if (more && (nx.seq != cc.seq || nx.kvh != cc.kvh)) {
-        prefetch_q(nx.seq, nx.kvh);
-        q_ahead = true;
-      }
-    }
     const SlotMeta mt = my_meta[s];
     const uint32_t kbase = slot_base0 + s * Gm::kSlotBytes;
     const uint32_t vbase = kbase + Gm::kTileBytes;
@@ -901,10 +829,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
       }
       reset();
       piece_t0 = cc.t;
-      if (range_end || cc.seq != seq || cc.kvh != kvh) {
-        if (q_ahead) commit_q();
-        else load_q(cc.seq, cc.kvh);
-      }
+      if (range_end || cc.seq != seq || cc.kvh != kvh) load_q(cc.seq, cc.kvh);
     }
   }
   (void)pending;
@@ -920,9 +845,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
 // carries the online softmax across chunks of contributors.
 // Threads of a merge CTA: 256, or 1024 when there are few pairs (their
 // contributor lists are then long, and more threads keep more rows in flight),
-// or 128 when the G x D block has at most 128 float4s (G <= 4): a 128-thread
-// CTA fits on an SM beside the persistent decode CTA, so the first of them
-// are resident, past their prologue, when the decode grid completes.
+// or 128 when most pairs have at most two contributors (fewer warps than twice
+// the pairs) and the G x D block has at most 128 float4s: a 128-thread CTA
+// fits on an SM beside the persistent decode CTA, so the first of them are
+// resident, past their prologue, when the decode grid completes. (Measured:
+// 128 threads were faster on batches of short pairs, 256 on the Llama-8B-
+// shaped batch, about 2.4 contributors per pair.)
 constexpr int kMergeThreads = 256;
 constexpr int kMergeThreadsFew = 1024;
 constexpr int kMergeThreadsSmall = 128;
@@ -1283,7 +1211,8 @@ cudaError_t launch_typed(const TcParams& tp, const void* k_cache, const void* v_
   if (static_cast<int64_t>(p.num_seqs) * p.num_kv_heads <= num_sms) {
     mcfg.blockDim = dim3(kMergeThreadsFew);
     err = cudaLaunchKernelEx(&mcfg, tc_merge_kernel<QT, D, TT, kMergeThreadsFew>, tp);
-  } else if (tp.group <= 4 && tp.group * D <= 4 * kMergeThreadsSmall) {
+  } else if (tp.group <= 4 && tp.group * D <= 4 * kMergeThreadsSmall &&
+             tp.num_warps < 2 * static_cast<int64_t>(p.num_seqs) * p.num_kv_heads) {
     mcfg.blockDim = dim3(kMergeThreadsSmall);
     err = cudaLaunchKernelEx(&mcfg, tc_merge_kernel<QT, D, TT, kMergeThreadsSmall>, tp);
   } else {

@@ -43,8 +43,9 @@
 namespace pa {
 namespace {
 
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
+constexpr int kWarps16 = 8;     // warps of a CTA, 16-bit caches
+constexpr int kWarpsFp8 = 12;   // warps of a CTA, E4M3 caches
+constexpr int kMaxWarps = 12;   // the most of either (sizes the workspace)
 constexpr int kRowTile = 16;   // MMA M: tokens per row tile
 constexpr int kMaxG = 8;       // MMA N
 constexpr uint32_t kFull = 0xffffffffu;
@@ -62,7 +63,10 @@ struct Geom {
   static constexpr uint32_t kFullMask = TT == 32 ? 0xffffffffu : 0xffffu;
   static constexpr int kTileBytes = TT * kRowBytes;
   static constexpr int kSlotBytes = 2 * kTileBytes;
-  static constexpr int kSlots = kSlotBytes >= 8192 ? 3 : 6;
+  // E4M3 tiles carry more conversion work per byte, so an SM runs more of
+  // their warps (each with a shorter ring) to hide its latencies
+  static constexpr int kWarps = kElem == 1 ? kWarpsFp8 : kWarps16;
+  static constexpr int kSlots = kElem == 1 ? (kWarpsFp8 > 8 ? 2 : 3) : (kSlotBytes >= 8192 ? 3 : 6);
   static constexpr int kSteps = D / 16;            // 16-column steps of QK^T and PV
 };
 
@@ -200,10 +204,12 @@ __device__ __forceinline__ void cursor_next(Cursor& c, const int* prefT, int B, 
 }
 
 template <typename QT, typename KT, int D, int TT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Geom<KT, D, TT>::kWarps * 32, 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                  const __grid_constant__ CUtensorMap tmap_v, const TcParams tp) {
   using Gm = Geom<KT, D, TT>;
+  constexpr int kWarps = Gm::kWarps;
+  constexpr int kThreads = kWarps * 32;
   constexpr int RT = Gm::kRowTiles;
   constexpr bool kFp8 = is_fp8<KT>::value;
   constexpr int NS = Gm::kSlots;
@@ -1161,7 +1167,7 @@ namespace {
 template <typename QT, typename KT, int D, int TT>
 size_t smem_bytes(int num_seqs) {
   using Gm = Geom<KT, D, TT>;
-  return 1024 + static_cast<size_t>(kWarps) * Gm::kSlots * (Gm::kSlotBytes + sizeof(SlotMeta) + 8) +
+  return 1024 + static_cast<size_t>(Gm::kWarps) * Gm::kSlots * (Gm::kSlotBytes + sizeof(SlotMeta) + 8) +
          (3 * static_cast<size_t>(num_seqs) + 2) * sizeof(int);
 }
 
@@ -1179,19 +1185,14 @@ cudaError_t launch_typed(const TcParams& tp, const void* k_cache, const void* v_
   cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(kernel),
                                       static_cast<int>(smem_bytes<QT, KT, D, TT>(kTcMaxSeqs)), attr_set);
   if (e != cudaSuccess) return e;
+  constexpr int kWarps = Geom<KT, D, TT>::kWarps;
   const int grid = (tp.num_warps + kWarps - 1) / kWarps;
-  if (tp.pg.group_start != nullptr) {
-    // the shared prefixes first, on the whole GPU; the decode grid that
-    // follows waits for them (griddep_wait) before it starts its work
-    e = launch_prefix_attn(p, tp.pg, D, std::is_same<QT, bf16>::value ? PA_BF16 : PA_F16, stream);
-    if (e != cudaSuccess) return e;
-  }
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kWarps * 32);
   cfg.dynamicSmemBytes = smem_bytes<QT, KT, D, TT>(p.num_seqs);
   cfg.stream = stream;
   cfg.attrs = attr;
@@ -1199,6 +1200,15 @@ cudaError_t launch_typed(const TcParams& tp, const void* k_cache, const void* v_
   cudaError_t err = cudaLaunchKernelEx(&cfg, kernel, mk, mv, tp);
   if (err != cudaSuccess) return err;
   note_launches(1);
+  if (tp.pg.group_start != nullptr) {
+    // the shared prefixes, on the tensor cores beside the decode CTAs
+    err = launch_prefix_attn(p, tp.pg, D, std::is_same<QT, bf16>::value ? PA_BF16 : PA_F16, num_sms,
+                             stream);
+    if (err != cudaSuccess) {
+      cudaMemsetAsync(tp.claim, 0, sizeof(int32_t), stream);  // rearm the counter ourselves
+      return err;
+    }
+  }
   if (tp.part_tiles != 0) {
     err = launch_reduce_partitions(p, D, std::is_same<QT, bf16>::value ? PA_BF16 : PA_F16,
                                    /*pdl=*/true, stream);
@@ -1241,8 +1251,8 @@ bool tc_supported(int group, int head_dim, pa_dtype kv_dtype, int num_seqs, int 
   return head_dim == 64 || head_dim == 128;
 }
 
-int tc_num_warps(int num_sms, int64_t max_units) {
-  int64_t w = static_cast<int64_t>(num_sms) * kWarps;
+int tc_num_warps(int num_sms, int64_t max_units, pa_dtype kv_dtype) {
+  int64_t w = static_cast<int64_t>(num_sms) * (kv_dtype == PA_FP8_E4M3 ? kWarpsFp8 : kWarps16);
   if (max_units < w) w = max_units;
   return static_cast<int>(w < 1 ? 1 : w);
 }
@@ -1250,7 +1260,7 @@ int tc_num_warps(int num_sms, int64_t max_units) {
 size_t tc_auto_workspace_bytes(int num_seqs, int head_dim, int group, int num_sms) {
   (void)num_seqs;
   // two partial states per static share and per chunk (at most 2W chunks)
-  const size_t W = static_cast<size_t>(num_sms) * kWarps;
+  const size_t W = static_cast<size_t>(num_sms) * kMaxWarps;
   const size_t slots = 6 * W * static_cast<size_t>(state_floats(group, head_dim)) * sizeof(float);
   return slots;
 }
@@ -1268,7 +1278,7 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int head_dim, pa_dtype q_dty
   if (part_tiles == 0) {
     tp.claim = next_claim_counter();
     if (tp.claim == nullptr) return cudaErrorInvalidDevice;
-    tp.num_warps = tc_num_warps(num_sms, static_cast<int64_t>(p.num_seqs) * p.num_kv_heads * tiles_max);
+    tp.num_warps = tc_num_warps(num_sms, static_cast<int64_t>(p.num_seqs) * p.num_kv_heads * tiles_max, kv_dtype);
     tp.ws_slots = static_cast<float*>(workspace);
     if (groups != nullptr) {
       // the shared-prefix states follow the 6W decode states
@@ -1277,7 +1287,7 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int head_dim, pa_dtype q_dty
     }
   } else {
     const int64_t parts_max = (tiles_max + part_tiles - 1) / part_tiles;
-    tp.num_warps = tc_num_warps(num_sms, static_cast<int64_t>(p.num_seqs) * p.num_kv_heads * parts_max);
+    tp.num_warps = tc_num_warps(num_sms, static_cast<int64_t>(p.num_seqs) * p.num_kv_heads * parts_max, kv_dtype);
     // the tail of the partitions is claimed from a counter the reduce rearms
     tp.claim = next_claim_counter();
     if (tp.claim == nullptr) return cudaErrorInvalidDevice;

@@ -67,9 +67,9 @@ int current_sm_count() {
 }
 
 // How the shared prefixes are cut: chunks of chunk_len keys (a multiple of
-// 16 and of the block size), so that the prefix grid has about two CTAs per
-// SM, one wave (more chunks mean more partial states to write and merge);
-// num_chunks covers the longest prefix.
+// 16 and of the block size), so that there are about two work items per SM
+// for the prefix grid's one CTA per SM (more chunks mean more partial states
+// to write and merge); num_chunks covers the longest prefix.
 struct PrefixPlan {
   int chunk_len = 0;
   int num_chunks = 0;

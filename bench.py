@@ -45,6 +45,8 @@ L2_FLUSH_BYTES = 256 << 20
 # sources are unchanged (their hash is stored beside the numbers)
 TRAFFIC_PATH = os.path.join(ROOT, "profiles", "traffic.json")
 TRAFFIC_SOURCES = ("paged_kv_cache_288_gb300/csrc/decode_tc.cu",
+                   "paged_kv_cache_288_gb300/csrc/decode_prefix.cu",
+                   "paged_kv_cache_288_gb300/csrc/decode_simt.cu",
                    "paged_kv_cache_288_gb300/csrc/ptx.cuh",
                    "paged_kv_cache_288_gb300/csrc/common.cuh")
 
@@ -541,7 +543,8 @@ def time_write_decode(dd, K, W, flush_l2, stream, world=1):
             [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)], n1 - n0)
 
 
-def decode_result(case, step_ms, dec_ms, launches, part, peak, peak_src, workload, extra=None):
+def decode_result(case, step_ms, dec_ms, launches, part, peak, peak_src, workload, extra=None,
+                  traffic_key=None):
     """A per-workload bench record: decode call and step throughput and the
     HBM roofline fraction of the decode call."""
     K = len(step_ms)
@@ -561,7 +564,7 @@ def decode_result(case, step_ms, dec_ms, launches, part, peak, peak_src, workloa
         "tokens_per_s_per_layer": round(case.num_seqs / (step_mean / 1e3), 1),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": recorded_traffic(workload, part),
+                     "traffic": recorded_traffic(traffic_key or workload, part),
                      "kernel": "pa_decode (every kernel of the call)"},
         "gpu_launches": launches,
     }
@@ -585,8 +588,9 @@ def run_config_suite(pa, device, stream, flush_l2, K, W, peak, peak_src):
             if dd.err.item() != 0:
                 raise RuntimeError(f"{name}: device error word {dd.err.item():#x}")
             extra = extra_fn(case, statistics.mean(dec_ms)) if extra_fn else None
-            out[key or f"{name}/p{part}"] = decode_result(case, step_ms, dec_ms, launches, part, peak,
-                                                          peak_src, name, extra)
+            out[key or f"{name}/p{part}"] = decode_result(
+                case, step_ms, dec_ms, launches, part, peak, peak_src, name, extra,
+                traffic_key=name + ("_grouped" if groups is not None else ""))
             del dd
             torch.cuda.empty_cache()
 
@@ -805,7 +809,8 @@ def run_ours(args, world, rank, local):
         "step_bytes": bytes_step,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": recorded_traffic(args.workload, part),
+                     "traffic": recorded_traffic(args.workload + ("_grouped" if groups is not None else ""),
+                                                 part),
                      "kernel": "pa_decode (every kernel of the call)"},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": Ke},

@@ -7,30 +7,28 @@
 // per-sequence decode still streams those blocks once per sequence. Here the
 // shared keys are attended once per group instead: the rows of the product
 // are (member sequence, query head) pairs of one KV unit, so with 100 members
-// and 4 heads per KV head a 16-key tile meets 400 query rows, a real dense
-// tile for the tensor cores.
+// and 4 heads per KV head a key tile meets 400 query rows, a real dense tile
+// for the tensor cores.
 //
-// Work. An item is 32 rows (16 per warp: member r / G, query head r % G of
-// one KV unit) and one chunk of the group's shared keys; a CTA of two warps
-// takes items in turn. An item's K and V tiles (16 keys, one 3-D TMA box per
-// 128-byte column per block) go through a two-stage ring in shared memory
-// that both warps read. Per tile and warp: S = Q K^T as
+// Work. A CTA of four warps takes 64 rows (16 per warp: member r / G, query
+// head r % G of one KV unit) and one chunk of the group's shared keys; the
+// grid is (row tiles, KV units, group x chunk). Its K and V tiles (64 keys,
+// one 3-D TMA box per 128-byte column per block) go through a three-stage
+// ring in shared memory that all warps read. Per tile and warp: S = Q K^T as
 // mma.sync m16n8k16 with Q held as A fragments in registers and K^T as B
-// fragments (ldmatrix), the online softmax on the accumulators (running
-// maximum in log2 units, running sum, rescaled O), P packed straight from
-// the S accumulators into A fragments, and O += P V with V through
-// ldmatrix.trans. Each row ends as a partial state (unnormalised O, maximum,
-// sum) in the same layout as the decode kernel's partial states, one per
-// (sequence, KV unit, chunk); the merge kernel combines them with the states
-// of the member's own suffix.
+// fragments (ldmatrix), eight independent 8-key accumulators; the online
+// softmax on the accumulators (running maximum in log2 units, running sum, O
+// rescaled only when a maximum grows); P packed straight from the S
+// accumulators into A fragments; O += P V with V through ldmatrix.trans. A
+// 64-key tile gives each softmax step 128 tensor-core products, so the
+// softmax chain is not what bounds a warp. Each row ends as a partial state
+// (unnormalised O, maximum, sum) in the same layout as the decode kernel's
+// partial states, one per (sequence, KV unit, chunk); the merge kernel
+// combines them with the states of the member's own suffix.
 //
-// The grid is launched after the decode grid of the same call (which streams
-// only the members' own suffixes) as its programmatic dependent, with at most
-// one small CTA per SM (64 threads, 18 KiB of shared memory) so that it runs
-// beside the persistent decode CTAs: the shared keys are attended on the
-// tensor cores while the decode streams the suffixes from HBM. It finishes
-// only after the decode grid (griddepcontrol.wait at its end), so the merge
-// that waits for it sees both grids' states.
+// The grid runs before the decode grid of the same call, on the whole GPU;
+// the decode grid (which streams only the members' own suffixes) starts its
+// work once this grid is complete.
 #include "common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
@@ -38,11 +36,11 @@
 namespace pa {
 namespace {
 
-constexpr int kPxWarps = 2;
+constexpr int kPxWarps = 4;
 constexpr int kPxThreads = 32 * kPxWarps;
 constexpr int kPxRows = 16 * kPxWarps;  // rows of a CTA
-constexpr int kPxTile = 16;             // keys per ring stage
-constexpr int kPxStages = 2;
+constexpr int kPxTile = 64;             // keys per ring stage
+constexpr int kPxStages = 3;
 constexpr int kPxMaxEntries = 256;      // block-table entries of one chunk held in shared memory
 constexpr uint32_t kFullMask = 0xffffffffu;
 
@@ -59,8 +57,7 @@ struct PxGeom {
 struct PxParams {
   DecodeParams p;
   PrefixGroups pg;
-  int group;      // query heads per KV unit
-  int row_tiles;  // tiles of kPxRows rows per (group, unit): the largest group's
+  int group;  // query heads per KV unit
 };
 
 // Address of 16-byte chunk `chunk` of key row `row` in a stage tile whose
@@ -87,18 +84,33 @@ __device__ __forceinline__ void px_mma(float (&d)[4], const uint32_t (&a)[4], ui
 }
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kPxThreads, 6)  // at most 168 registers: fits beside a decode CTA
+__global__ void __launch_bounds__(kPxThreads, 2)
 prefix_attn_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                    const PxParams xp) {
   using Gm = PxGeom<D>;
-  constexpr int KS = D / 16;  // 16-column steps of d
+  constexpr int KS = D / 16;        // 16-column steps of d
+  constexpr int NT = kPxTile / 8;   // 8-key tiles of S
   const DecodeParams& p = xp.p;
   const PrefixGroups& pg = xp.pg;
   const int G = xp.group;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
-  // the merge after this grid may get resident now; it waits for this grid
-  griddep_launch_dependents();
+
+  const int unit = blockIdx.y;
+  const int grp = blockIdx.z / pg.num_chunks;
+  const int chunk = blockIdx.z % pg.num_chunks;
+  const int bs = p.block_size;
+  const int lbs = 31 - __clz(bs);  // block sizes are powers of two
+  int a, b, plen;
+  const bool clamped = prefix_group(pg, grp, p.num_seqs, p.max_blocks_per_seq, bs, a, b, plen);
+  if (clamped && threadIdx.x == 0 && blockIdx.x == 0 && unit == 0 && chunk == 0)
+    flag_error(p.debug_err, PA_DEVERR_PREFIX);
+  const int rows = (b - a) * G;
+  const int row0 = blockIdx.x * kPxRows;
+  const int k0 = chunk * pg.chunk_len;
+  const int k1 = min(plen, k0 + pg.chunk_len);
+  if (row0 >= rows || k0 >= k1) return;  // uniform over the CTA, before any barrier
+  const int ntiles = (k1 - k0 + kPxTile - 1) / kPxTile;
 
   extern __shared__ unsigned char px_smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -109,280 +121,248 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_cons
   int* s_ent = s_abort + 4;
   auto full_bar = [&](int s) { return smem_u32(&bars[s]); };
   auto empty_bar = [&](int s) { return smem_u32(&bars[kPxStages + s]); };
+
+  // the chunk's blocks, from the group's first member's table
+  const int j0 = k0 >> lbs;
+  const int nent = ((k1 - 1) >> lbs) - j0 + 1;  // <= chunk_len / bs <= kPxMaxEntries
+  const int32_t* lead = p.block_tables + static_cast<int64_t>(a) * p.max_blocks_per_seq;
+  bool bad = false;
+  for (int i = threadIdx.x; i < nent; i += kPxThreads) {
+    int e = lead[j0 + i];
+    if (e < 0 || e >= p.num_blocks) {
+      flag_error(p.debug_err, PA_DEVERR_BLOCK_RANGE);
+      e = -1;
+      bad = true;
+    }
+    s_ent[i] = e;
+  }
   if (threadIdx.x < kPxStages) {
     mbar_init(full_bar(threadIdx.x), 1);
     mbar_init(empty_bar(threadIdx.x), kPxWarps);
   }
   if (threadIdx.x == 0) *s_abort = 0;
   mbar_init_fence();
-  __syncthreads();
+  // every block of the chunk in range: tiles inside the chunk need no masks
+  const bool all_valid = __syncthreads_and(!bad);
 
-  const int bs = p.block_size;
-  const int lbs = 31 - __clz(bs);  // block sizes are powers of two
+  const int kvh = kv_head_of(p, unit);
   const int hkv = p.kv_heads_phys;
-  const int row_tiles = xp.row_tiles;
-  const int units = p.num_kv_heads;
-  const int64_t items = static_cast<int64_t>(row_tiles) * units * pg.num_groups * pg.num_chunks;
-  uint32_t g_tiles = 0;  // tiles this CTA has taken through its ring, over all items
-
-  // work items (row tile, KV unit, group, chunk) in turn, gridDim.x apart
-  for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
-    const int rt = static_cast<int>(it % row_tiles);
-    int64_t r = it / row_tiles;
-    const int unit = static_cast<int>(r % units);
-    r /= units;
-    const int chunk = static_cast<int>(r % pg.num_chunks);
-    const int grp = static_cast<int>(r / pg.num_chunks);
-    int a, b, plen;
-    const bool clamped = prefix_group(pg, grp, p.num_seqs, p.max_blocks_per_seq, bs, a, b, plen);
-    if (clamped && threadIdx.x == 0 && rt == 0 && unit == 0 && chunk == 0)
-      flag_error(p.debug_err, PA_DEVERR_PREFIX);
-    const int rows = (b - a) * G;
-    const int row0 = rt * kPxRows;
-    const int k0 = chunk * pg.chunk_len;
-    const int k1 = min(plen, k0 + pg.chunk_len);
-    if (row0 >= rows || k0 >= k1) continue;  // uniform over the CTA
-    const int ntiles = (k1 - k0 + kPxTile - 1) / kPxTile;
-
-    // the chunk's blocks, from the group's first member's table
-    const int j0 = k0 >> lbs;
-    const int nent = ((k1 - 1) >> lbs) - j0 + 1;  // <= chunk_len / bs <= kPxMaxEntries
-    const int32_t* lead = p.block_tables + static_cast<int64_t>(a) * p.max_blocks_per_seq;
-    __syncthreads();  // every warp is done with the previous item's entries
-    bool bad = false;
-    for (int i = threadIdx.x; i < nent; i += kPxThreads) {
-      int e = lead[j0 + i];
-      if (e < 0 || e >= p.num_blocks) {
-        flag_error(p.debug_err, PA_DEVERR_BLOCK_RANGE);
-        e = -1;
-        bad = true;
-      }
-      s_ent[i] = e;
+  // TMA of key tile i into stage s: one box per 128-byte column per block
+  // the tile touches; blocks flagged out of range are skipped (their keys
+  // are masked below)
+  auto issue = [&](int i, int s) {
+    const int t0 = k0 + i * kPxTile;
+    const int bh = bs < kPxTile ? bs : kPxTile;  // rows per box
+    const int nsub = kPxTile / bh;
+    uint32_t tx = 0;
+    for (int h = 0; h < nsub; ++h) {
+      const int tok = t0 + h * bh;
+      if (tok >= k1) break;
+      if (s_ent[(tok >> lbs) - j0] >= 0) tx += 2u * bh * D * 2;
     }
-    // every block of the chunk in range: tiles inside the chunk need no masks
-    const bool all_valid = __syncthreads_and(!bad);
-
-    // every member of this item's rows must hold the same blocks in the
-    // chunk (checked by the first KV unit's items only)
-    if (unit == 0) {
-      const int m0 = row0 / G, m1 = min(b - a, (row0 + kPxRows + G - 1) / G);
-      for (int i = threadIdx.x; i < (m1 - m0) * nent; i += kPxThreads) {
-        const int m = m0 + i / nent, j = i % nent;
-        if (m == 0) continue;
-        const int e = p.block_tables[static_cast<int64_t>(a + m) * p.max_blocks_per_seq + j0 + j];
-        if (e != lead[j0 + j]) flag_error(p.debug_err, PA_DEVERR_PREFIX);
-      }
-    }
-
-    const int kvh = kv_head_of(p, unit);
-    // TMA of key tile i of the item into stage s: one box per 128-byte
-    // column per block the tile touches; blocks flagged out of range are
-    // skipped (their keys are masked below)
-    auto issue = [&](int i, int s) {
-      const int t0 = k0 + i * kPxTile;
-      const int bh = bs < kPxTile ? bs : kPxTile;  // rows per box
-      const int nsub = kPxTile / bh;
-      uint32_t tx = 0;
-      for (int h = 0; h < nsub; ++h) {
-        const int tok = t0 + h * bh;
-        if (tok >= k1) break;
-        if (s_ent[(tok >> lbs) - j0] >= 0) tx += 2u * bh * D * 2;
-      }
-      mbar_arrive_expect_tx(full_bar(s), tx);
-      const uint32_t kdst = stage0 + s * Gm::kStageBytes;
-      const uint32_t vdst = kdst + Gm::kTileBytes;
-      for (int h = 0; h < nsub; ++h) {
-        const int tok = t0 + h * bh;
-        if (tok >= k1) break;
-        const int e = s_ent[(tok >> lbs) - j0];
-        if (e < 0) continue;
-        const int z = e * hkv + kvh;
-        const int off = tok & (bs - 1);
+    mbar_arrive_expect_tx(full_bar(s), tx);
+    const uint32_t kdst = stage0 + s * Gm::kStageBytes;
+    const uint32_t vdst = kdst + Gm::kTileBytes;
+    for (int h = 0; h < nsub; ++h) {
+      const int tok = t0 + h * bh;
+      if (tok >= k1) break;
+      const int e = s_ent[(tok >> lbs) - j0];
+      if (e < 0) continue;
+      const int z = e * hkv + kvh;
+      const int off = tok & (bs - 1);
 #pragma unroll
-        for (int c = 0; c < Gm::kBoxes; ++c) {
-          tma_load_3d(kdst + c * Gm::kBoxBytes + h * bh * 128, &tmap_k, c * 64, off, z, full_bar(s));
-          tma_load_3d(vdst + c * Gm::kBoxBytes + h * bh * 128, &tmap_v, c * 64, off, z, full_bar(s));
-        }
+      for (int c = 0; c < Gm::kBoxes; ++c) {
+        tma_load_3d(kdst + c * Gm::kBoxBytes + h * bh * 128, &tmap_k, c * 64, off, z, full_bar(s));
+        tma_load_3d(vdst + c * Gm::kBoxBytes + h * bh * 128, &tmap_v, c * 64, off, z, full_bar(s));
       }
-    };
-    if (threadIdx.x == 0)
-      for (int i = 0; i < kPxStages && i < ntiles; ++i) issue(i, (g_tiles + i) % kPxStages);
+    }
+  };
+  if (threadIdx.x == 0)
+    for (int i = 0; i < kPxStages && i < ntiles; ++i) issue(i, i);
 
-    // this warp's rows: gid and gid + 8 of its 16
-    const int r_a = row0 + warp * 16 + gid, r_b = r_a + 8;
-    const bool ok_a = r_a < rows, ok_b = r_b < rows;
-    const int seq_a = a + (ok_a ? r_a / G : 0), seq_b = a + (ok_b ? r_b / G : 0);
-    const int h_a = ok_a ? r_a % G : 0, h_b = ok_b ? r_b % G : 0;
-    const T* qa = static_cast<const T*>(p.q) + (static_cast<int64_t>(seq_a) * p.num_heads + unit * G + h_a) * D;
-    const T* qb = static_cast<const T*>(p.q) + (static_cast<int64_t>(seq_b) * p.num_heads + unit * G + h_b) * D;
-    uint32_t qf[KS][4];
+  // every member of this CTA's rows must hold the same blocks in the chunk
+  // (checked by the first KV unit's CTAs only, while the first tiles load)
+  if (unit == 0) {
+    const int m0 = row0 / G, m1 = min(b - a, (row0 + kPxRows + G - 1) / G);
+    for (int i = threadIdx.x; i < (m1 - m0) * nent; i += kPxThreads) {
+      const int m = m0 + i / nent, j = i % nent;
+      if (m == 0) continue;
+      const int e = p.block_tables[static_cast<int64_t>(a + m) * p.max_blocks_per_seq + j0 + j];
+      if (e != lead[j0 + j]) flag_error(p.debug_err, PA_DEVERR_PREFIX);
+    }
+  }
+
+  // this warp's rows: gid and gid + 8 of its 16
+  const int r_a = row0 + warp * 16 + gid, r_b = r_a + 8;
+  const bool ok_a = r_a < rows, ok_b = r_b < rows;
+  const int seq_a = a + (ok_a ? r_a / G : 0), seq_b = a + (ok_b ? r_b / G : 0);
+  const int h_a = ok_a ? r_a % G : 0, h_b = ok_b ? r_b % G : 0;
+  const T* qa = static_cast<const T*>(p.q) + (static_cast<int64_t>(seq_a) * p.num_heads + unit * G + h_a) * D;
+  const T* qb = static_cast<const T*>(p.q) + (static_cast<int64_t>(seq_b) * p.num_heads + unit * G + h_b) * D;
+  uint32_t qf[KS][4];
+#pragma unroll
+  for (int k = 0; k < KS; ++k) {
+    qf[k][0] = ok_a ? *reinterpret_cast<const uint32_t*>(qa + 16 * k + 2 * tig) : 0u;
+    qf[k][1] = ok_b ? *reinterpret_cast<const uint32_t*>(qb + 16 * k + 2 * tig) : 0u;
+    qf[k][2] = ok_a ? *reinterpret_cast<const uint32_t*>(qa + 16 * k + 8 + 2 * tig) : 0u;
+    qf[k][3] = ok_b ? *reinterpret_cast<const uint32_t*>(qb + 16 * k + 8 + 2 * tig) : 0u;
+  }
+
+  float o[2 * KS][4];
+#pragma unroll
+  for (int n = 0; n < 2 * KS; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
+
+  for (int i = 0; i < ntiles; ++i) {
+    const int s = i % kPxStages;
+    const uint32_t par = (i / kPxStages) & 1u;
+    const bool got = mbar_wait_bounded(full_bar(s), par);
+    if (!__all_sync(kFullMask, got)) {
+      if (lane == 0) {
+        flag_error(p.debug_err, PA_DEVERR_TIMEOUT);
+        atomicExch(s_abort, 1);
+      }
+      break;
+    }
+    const uint32_t kbase = stage0 + s * Gm::kStageBytes;
+    const uint32_t vbase = kbase + Gm::kTileBytes;
+    const int t0 = k0 + i * kPxTile;
+
+    // S = Q K^T: 16 rows x 64 keys, as eight independent 8-key tiles
+    float sc[NT][4];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
 #pragma unroll
     for (int k = 0; k < KS; ++k) {
-      qf[k][0] = ok_a ? *reinterpret_cast<const uint32_t*>(qa + 16 * k + 2 * tig) : 0u;
-      qf[k][1] = ok_b ? *reinterpret_cast<const uint32_t*>(qb + 16 * k + 2 * tig) : 0u;
-      qf[k][2] = ok_a ? *reinterpret_cast<const uint32_t*>(qa + 16 * k + 8 + 2 * tig) : 0u;
-      qf[k][3] = ok_b ? *reinterpret_cast<const uint32_t*>(qb + 16 * k + 8 + 2 * tig) : 0u;
-    }
-
-    float o[2 * KS][4];
 #pragma unroll
-    for (int n = 0; n < 2 * KS; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-    float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
-
-    for (int i = 0; i < ntiles; ++i) {
-      const uint32_t gi = g_tiles + i;
-      const int s = gi % kPxStages;
-      const uint32_t par = (gi / kPxStages) & 1u;
-      const bool got = mbar_wait_bounded(full_bar(s), par);
-      if (!__all_sync(kFullMask, got)) {
-        if (lane == 0) {
-          flag_error(p.debug_err, PA_DEVERR_TIMEOUT);
-          atomicExch(s_abort, 1);
-        }
-        break;
-      }
-      const uint32_t kbase = stage0 + s * Gm::kStageBytes;
-      const uint32_t vbase = kbase + Gm::kTileBytes;
-      const int t0 = k0 + i * kPxTile;
-
-      // S = Q K^T: 16 rows x 16 keys, as two 8-key tiles
-      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-      for (int k = 0; k < KS; ++k) {
+      for (int n = 0; n < NT; n += 2) {
         uint32_t r0, r1, r2, r3;
-        ldsm_x4(px_addr<Gm::kBoxBytes>(kbase, (lane >> 4) * 8 + (lane & 7), 2 * k + ((lane >> 3) & 1)),
+        ldsm_x4(px_addr<Gm::kBoxBytes>(kbase, 8 * n + (lane >> 4) * 8 + (lane & 7), 2 * k + ((lane >> 3) & 1)),
                 r0, r1, r2, r3);
-        px_mma<T>(sc[0], qf[k], r0, r1);
-        px_mma<T>(sc[1], qf[k], r2, r3);
+        px_mma<T>(sc[n], qf[k], r0, r1);
+        px_mma<T>(sc[n + 1], qf[k], r2, r3);
+      }
+    }
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sc[n][e] *= p.scale_log2;
+    // keys past the chunk, or in a block flagged out of range, do not count
+    // (their rows of the stage hold stale data: scores are replaced, values
+    // zeroed below, so no NaN or infinity reaches O)
+    uint64_t vmask = ~0ull;  // bit k: key t0 + k is valid
+    const bool full = all_valid && t0 + kPxTile <= k1;
+    if (!full) {
+      vmask = 0;
+#pragma unroll
+      for (int k = 0; k < kPxTile; k += 8) {
+        const int tok = t0 + k;
+        if (tok < k1 && s_ent[(tok >> lbs) - j0] >= 0)
+          vmask |= static_cast<uint64_t>(tok + 8 <= k1 ? 0xffu : ((1u << (k1 - tok)) - 1u)) << k;
       }
 #pragma unroll
-      for (int n = 0; n < 2; ++n)
+      for (int n = 0; n < NT; ++n)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) sc[n][e] *= p.scale_log2;
-      // keys past the chunk, or in a block flagged out of range, do not
-      // count (their rows of the stage hold stale data: scores are
-      // replaced, values zeroed below, so no NaN or infinity reaches O)
-      uint32_t vmask = 0xffffu;  // bit k: key t0 + k is valid
-      if (!all_valid || t0 + kPxTile > k1) {
-        vmask = 0;
-#pragma unroll
-        for (int k = 0; k < kPxTile; k += 8) {
-          const int tok = t0 + k;
-          if (tok < k1 && s_ent[(tok >> lbs) - j0] >= 0)
-            vmask |= (tok + 8 <= k1 ? 0xffu : ((1u << (k1 - tok)) - 1u)) << k;
+        for (int e = 0; e < 2; ++e) {
+          const bool valid = (vmask >> (8 * n + 2 * tig + e)) & 1ull;
+          sc[n][e] = valid ? sc[n][e] : -INFINITY;
+          sc[n][2 + e] = valid ? sc[n][2 + e] : -INFINITY;
         }
+    }
+    float x_a = -INFINITY, x_b = -INFINITY;
 #pragma unroll
-        for (int n = 0; n < 2; ++n)
+    for (int n = 0; n < NT; ++n) {
+      x_a = fmaxf(x_a, fmaxf(sc[n][0], sc[n][1]));
+      x_b = fmaxf(x_b, fmaxf(sc[n][2], sc[n][3]));
+    }
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const bool valid = (vmask >> (8 * n + 2 * tig + e)) & 1u;
-            sc[n][e] = valid ? sc[n][e] : -INFINITY;
-            sc[n][2 + e] = valid ? sc[n][2 + e] : -INFINITY;
-          }
+    for (int off = 1; off < 4; off <<= 1) {
+      x_a = fmaxf(x_a, __shfl_xor_sync(kFullMask, x_a, off));
+      x_b = fmaxf(x_b, __shfl_xor_sync(kFullMask, x_b, off));
+    }
+    // rescale O only when some row's maximum grew (rarely, once the maxima settle)
+    if (__any_sync(kFullMask, x_a > m_a || x_b > m_b)) {
+      const float n_a = fmaxf(m_a, x_a), n_b = fmaxf(m_b, x_b);
+      const float al_a = n_a == -INFINITY ? 1.f : exp2f(m_a - n_a);  // 0 while m is -inf
+      const float al_b = n_b == -INFINITY ? 1.f : exp2f(m_b - n_b);
+      m_a = n_a;
+      m_b = n_b;
+      l_a *= al_a;
+      l_b *= al_b;
+#pragma unroll
+      for (int n = 0; n < 2 * KS; ++n) {
+        o[n][0] *= al_a;
+        o[n][1] *= al_a;
+        o[n][2] *= al_b;
+        o[n][3] *= al_b;
       }
-      float x_a = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
-      float x_b = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
+    }
+    const float b_a = m_a == -INFINITY ? 0.f : m_a, b_b = m_b == -INFINITY ? 0.f : m_b;
+    // O += P V, one 16-key step at a time: P of keys 16j.. as the A operand
+    // (rows gid / gid + 8), V rows 16j.. through transposed loads
 #pragma unroll
-      for (int off = 1; off < 4; off <<= 1) {
-        x_a = fmaxf(x_a, __shfl_xor_sync(kFullMask, x_a, off));
-        x_b = fmaxf(x_b, __shfl_xor_sync(kFullMask, x_b, off));
-      }
-      // rescale O only when some row's maximum grew (rarely, once the maxima settle)
-      if (__any_sync(kFullMask, x_a > m_a || x_b > m_b)) {
-        const float n_a = fmaxf(m_a, x_a), n_b = fmaxf(m_b, x_b);
-        const float al_a = n_a == -INFINITY ? 1.f : exp2f(m_a - n_a);  // 0 while m is -inf
-        const float al_b = n_b == -INFINITY ? 1.f : exp2f(m_b - n_b);
-        m_a = n_a;
-        m_b = n_b;
-        l_a *= al_a;
-        l_b *= al_b;
-#pragma unroll
-        for (int n = 0; n < 2 * KS; ++n) {
-          o[n][0] *= al_a;
-          o[n][1] *= al_a;
-          o[n][2] *= al_b;
-          o[n][3] *= al_b;
-        }
-      }
-      const float b_a = m_a == -INFINITY ? 0.f : m_a, b_b = m_b == -INFINITY ? 0.f : m_b;
+    for (int j = 0; j < NT / 2; ++j) {
       float pr[2][4];
 #pragma unroll
-      for (int n = 0; n < 2; ++n) {
-        pr[n][0] = exp2f(sc[n][0] - b_a);
-        pr[n][1] = exp2f(sc[n][1] - b_a);
-        pr[n][2] = exp2f(sc[n][2] - b_b);
-        pr[n][3] = exp2f(sc[n][3] - b_b);
-        l_a += pr[n][0] + pr[n][1];
-        l_b += pr[n][2] + pr[n][3];
+      for (int h = 0; h < 2; ++h) {
+        pr[h][0] = exp2f(sc[2 * j + h][0] - b_a);
+        pr[h][1] = exp2f(sc[2 * j + h][1] - b_a);
+        pr[h][2] = exp2f(sc[2 * j + h][2] - b_b);
+        pr[h][3] = exp2f(sc[2 * j + h][3] - b_b);
+        l_a += pr[h][0] + pr[h][1];
+        l_b += pr[h][2] + pr[h][3];
       }
-      // P as the A operand: rows gid / gid + 8, keys 2tig.. and 8 + 2tig..
       uint32_t pa4[4];
       pa4[0] = px_pack(pr[0][0], pr[0][1], static_cast<T*>(nullptr));
       pa4[1] = px_pack(pr[0][2], pr[0][3], static_cast<T*>(nullptr));
       pa4[2] = px_pack(pr[1][0], pr[1][1], static_cast<T*>(nullptr));
       pa4[3] = px_pack(pr[1][2], pr[1][3], static_cast<T*>(nullptr));
-      // O += P V, 16 columns of d per transposed load
+      const uint32_t km = static_cast<uint32_t>(vmask >> (16 * j)) & 0xffffu;
+      const uint32_t lo = ((km >> (2 * tig)) & 1u ? 0x0000ffffu : 0u) | ((km >> (2 * tig + 1)) & 1u ? 0xffff0000u : 0u);
+      const uint32_t hi = ((km >> (8 + 2 * tig)) & 1u ? 0x0000ffffu : 0u) |
+                          ((km >> (9 + 2 * tig)) & 1u ? 0xffff0000u : 0u);
 #pragma unroll
-      for (int j = 0; j < KS; ++j) {
+      for (int c = 0; c < KS; ++c) {
         uint32_t r0, r1, r2, r3;
-        ldsm_x4_trans(px_addr<Gm::kBoxBytes>(vbase, ((lane >> 3) & 1) * 8 + (lane & 7), 2 * j + (lane >> 4)),
+        ldsm_x4_trans(px_addr<Gm::kBoxBytes>(vbase, 16 * j + ((lane >> 3) & 1) * 8 + (lane & 7), 2 * c + (lane >> 4)),
                       r0, r1, r2, r3);
-        if (vmask != 0xffffu) {
-          // r0, r2 hold keys 2tig, 2tig + 1; r1, r3 keys 8 + 2tig, 9 + 2tig
-          const uint32_t lo = ((vmask >> (2 * tig)) & 1u ? 0x0000ffffu : 0u) |
-                              ((vmask >> (2 * tig + 1)) & 1u ? 0xffff0000u : 0u);
-          const uint32_t hi = ((vmask >> (8 + 2 * tig)) & 1u ? 0x0000ffffu : 0u) |
-                              ((vmask >> (9 + 2 * tig)) & 1u ? 0xffff0000u : 0u);
+        if (!full) {
+          // r0, r2 hold keys 2tig, 2tig + 1 of the step; r1, r3 keys 8 + 2tig, 9 + 2tig
           r0 &= lo;
           r2 &= lo;
           r1 &= hi;
           r3 &= hi;
         }
-        px_mma<T>(o[2 * j], pa4, r0, r1);
-        px_mma<T>(o[2 * j + 1], pa4, r2, r3);
+        px_mma<T>(o[2 * c], pa4, r0, r1);
+        px_mma<T>(o[2 * c + 1], pa4, r2, r3);
       }
-
-      // stage s is free again: the first thread refills it with the item's
-      // tile kPxStages ahead once every warp is done with it
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty_bar(s));
-      if (threadIdx.x == 0 && i + kPxStages < ntiles) {
-        if (!mbar_wait_bounded(empty_bar(s), par)) {
-          flag_error(p.debug_err, PA_DEVERR_TIMEOUT);
-          atomicExch(s_abort, 1);
-        } else {
-          fence_proxy_async_smem();
-          issue(i + kPxStages, s);
-        }
-      }
-      __syncwarp();
-      if (*reinterpret_cast<volatile int*>(s_abort)) break;
-    }
-    if (threadIdx.x == 0) {
-      // the last stages' releases: wait for them, so the next item's first
-      // loads never overwrite a stage a warp still reads
-      for (int i = max(0, ntiles - kPxStages); i < ntiles; ++i) {
-        const uint32_t gi = g_tiles + i;
-        if (!mbar_wait_bounded(empty_bar(gi % kPxStages), (gi / kPxStages) & 1u)) {
-          flag_error(p.debug_err, PA_DEVERR_TIMEOUT);
-          atomicExch(s_abort, 1);
-          break;
-        }
-      }
-    }
-    g_tiles += ntiles;
-    if (*reinterpret_cast<volatile int*>(s_abort)) {
-      if (threadIdx.x == 0)  // give copies still in flight a short while to land
-        for (int s = 0; s < kPxStages; ++s) mbar_wait_bounded(full_bar(s), 0, 10000000ull);
-      break;
     }
 
+    // stage s is free again: the first thread refills it with the tile
+    // kPxStages ahead once every warp is done with it
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty_bar(s));
+    if (threadIdx.x == 0 && i + kPxStages < ntiles) {
+      if (!mbar_wait_bounded(empty_bar(s), par)) {
+        flag_error(p.debug_err, PA_DEVERR_TIMEOUT);
+        atomicExch(s_abort, 1);
+      } else {
+        fence_proxy_async_smem();
+        issue(i + kPxStages, s);
+      }
+    }
+    __syncwarp();
+    if (*reinterpret_cast<volatile int*>(s_abort)) break;
+  }
+
+  if (*reinterpret_cast<volatile int*>(s_abort) == 0) {
 #pragma unroll
     for (int off = 1; off < 4; off <<= 1) {
       l_a += __shfl_xor_sync(kFullMask, l_a, off);
       l_b += __shfl_xor_sync(kFullMask, l_b, off);
     }
     const int stride = state_floats(G, D);
+    const int64_t units = p.num_kv_heads;
     auto store_row = [&](bool ok, int seq, int h, float m, float l, int upper) {
       if (!ok) return;
       float* st = pg.ws_prefix + ((static_cast<int64_t>(seq) * units + unit) * pg.num_chunks + chunk) * stride;
@@ -397,10 +377,10 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_cons
     };
     store_row(ok_a, seq_a, h_a, m_a, l_a, 0);
     store_row(ok_b, seq_b, h_b, m_b, l_b, 1);
+  } else if (threadIdx.x == 0) {
+    // give copies still in flight a short while to land before the CTA leaves
+    for (int s = 0; s < kPxStages; ++s) mbar_wait_bounded(full_bar(s), 0, 10000000ull);
   }
-  // complete only after the decode grid launched before this one: whoever
-  // waits for this grid then sees the decode grid's partial states as well
-  griddep_wait();
 }
 
 template <typename T, int D>
@@ -415,19 +395,11 @@ cudaError_t launch_px(const PxParams& xp, dim3 grid, cudaStream_t stream) {
   static std::atomic<unsigned long long> attr_set{0};
   cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(kernel), PxGeom<D>::kSmemBytes, attr_set);
   if (e != cudaSuccess) return e;
-  // a programmatic dependent of the decode grid: it starts once every decode
-  // CTA is resident and past its prologue (the decode grid waited for the
-  // kernels before it, so q, caches and tables are complete)
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kPxThreads);
   cfg.dynamicSmemBytes = PxGeom<D>::kSmemBytes;
   cfg.stream = stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, kernel, mk, mv, xp);
   if (e == cudaSuccess) note_launches(1);
   return e;
@@ -439,22 +411,23 @@ int prefix_row_tiles(int max_group_size, int group) {
   return static_cast<int>((static_cast<int64_t>(max_group_size) * group + kPxRows - 1) / kPxRows);
 }
 
+int prefix_chunk_step(int block_size) {
+  // chunks are whole key tiles (and whole blocks)
+  return block_size > kPxTile ? block_size : kPxTile;
+}
+
 int prefix_max_chunk_len(int block_size) {
   // the chunk's table entries fit the CTA's shared array
   return (kPxMaxEntries - 1) * block_size;
 }
 
 cudaError_t launch_prefix_attn(const DecodeParams& p, const PrefixGroups& pg, int head_dim,
-                               pa_dtype dtype, int num_sms, cudaStream_t stream) {
+                               pa_dtype dtype, cudaStream_t stream) {
   PxParams xp{};
   xp.p = p;
   xp.pg = pg;
   xp.group = p.num_heads / p.num_kv_heads;
-  xp.row_tiles = prefix_row_tiles(pg.max_group_size, xp.group);
-  // one CTA per SM at most, beside that SM's decode CTA, taking the work
-  // items in turn
-  const int64_t items = static_cast<int64_t>(xp.row_tiles) * p.num_kv_heads * pg.num_groups * pg.num_chunks;
-  dim3 grid(static_cast<unsigned>(items < num_sms ? (items < 1 ? 1 : items) : num_sms));
+  dim3 grid(prefix_row_tiles(pg.max_group_size, xp.group), p.num_kv_heads, pg.num_groups * pg.num_chunks);
   if (dtype == PA_BF16) {
     if (head_dim == 128) return launch_px<bf16, 128>(xp, grid, stream);
     return launch_px<bf16, 64>(xp, grid, stream);

@@ -1187,6 +1187,12 @@ cudaError_t launch_typed(const TcParams& tp, const void* k_cache, const void* v_
   if (e != cudaSuccess) return e;
   constexpr int kWarps = Geom<KT, D, TT>::kWarps;
   const int grid = (tp.num_warps + kWarps - 1) / kWarps;
+  if (tp.pg.group_start != nullptr) {
+    // the shared prefixes first, on the whole GPU; the decode grid that
+    // follows starts its work (griddepcontrol.wait) once they are complete
+    e = launch_prefix_attn(p, tp.pg, D, std::is_same<QT, bf16>::value ? PA_BF16 : PA_F16, stream);
+    if (e != cudaSuccess) return e;
+  }
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -1200,15 +1206,6 @@ cudaError_t launch_typed(const TcParams& tp, const void* k_cache, const void* v_
   cudaError_t err = cudaLaunchKernelEx(&cfg, kernel, mk, mv, tp);
   if (err != cudaSuccess) return err;
   note_launches(1);
-  if (tp.pg.group_start != nullptr) {
-    // the shared prefixes, on the tensor cores beside the decode CTAs
-    err = launch_prefix_attn(p, tp.pg, D, std::is_same<QT, bf16>::value ? PA_BF16 : PA_F16, num_sms,
-                             stream);
-    if (err != cudaSuccess) {
-      cudaMemsetAsync(tp.claim, 0, sizeof(int32_t), stream);  // rearm the counter ourselves
-      return err;
-    }
-  }
   if (tp.part_tiles != 0) {
     err = launch_reduce_partitions(p, D, std::is_same<QT, bf16>::value ? PA_BF16 : PA_F16,
                                    /*pdl=*/true, stream);

@@ -101,13 +101,14 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int head_dim, pa_dtype q_dty
                              pa_dtype kv_dtype, int partition_size, void* workspace, int num_sms,
                              cudaStream_t stream, const PrefixGroups* groups = nullptr);
 
-// Shared-prefix attention (decode_prefix.cu): items of (32 rows of a group's
-// members x query heads, KV unit, group x chunk of the prefix) taken in turn
-// by at most one CTA per SM, launched as a programmatic dependent of the
-// decode grid; partial states go to groups.ws_prefix.
+// Shared-prefix attention (decode_prefix.cu): one CTA per (64 rows of a
+// group's members x query heads, KV unit, group x chunk of the prefix),
+// launched before the decode grid of the call; partial states go to
+// groups.ws_prefix.
 int prefix_row_tiles(int max_group_size, int group);
 int prefix_max_chunk_len(int block_size);
+int prefix_chunk_step(int block_size);
 cudaError_t launch_prefix_attn(const DecodeParams& p, const PrefixGroups& groups, int head_dim,
-                               pa_dtype dtype, int num_sms, cudaStream_t stream);
+                               pa_dtype dtype, cudaStream_t stream);
 
 }  // namespace pa

@@ -66,10 +66,10 @@ int current_sm_count() {
   return sms;
 }
 
-// How the shared prefixes are cut: chunks of chunk_len keys (a multiple of
-// 16 and of the block size), so that there are about two work items per SM
-// for the prefix grid's one CTA per SM (more chunks mean more partial states
-// to write and merge); num_chunks covers the longest prefix.
+// How the shared prefixes are cut: chunks of chunk_len keys (whole key tiles
+// and whole blocks), so that the prefix grid has about two CTAs per SM (more
+// chunks mean more partial states to write and merge); num_chunks covers the
+// longest prefix.
 struct PrefixPlan {
   int chunk_len = 0;
   int num_chunks = 0;
@@ -82,10 +82,10 @@ PrefixPlan prefix_plan(int num_groups, int max_group_size, int max_prefix_len, i
   const int64_t per_set = static_cast<int64_t>(pa::prefix_row_tiles(max_group_size, group)) * units * num_groups;
   const int64_t target = 2 * static_cast<int64_t>(sms > 0 ? sms : 1);
   int64_t c = (target + per_set - 1) / per_set;
-  const int64_t cmax = (max_prefix_len + 15) / 16;
+  const int64_t cmax = (max_prefix_len + pa::prefix_chunk_step(block_size) - 1) / pa::prefix_chunk_step(block_size);
   if (c > cmax) c = cmax;
   if (c < 1) c = 1;
-  const int step = block_size > 16 ? block_size : 16;
+  const int step = pa::prefix_chunk_step(block_size);
   int64_t len = (max_prefix_len + c - 1) / c;
   len = (len + step - 1) / step * step;
   const int64_t cap = pa::prefix_max_chunk_len(block_size) / step * step;

@@ -254,11 +254,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
   if (prefix_mode) {
     // each group's members skip its shared tokens
     __syncthreads();
-    for (int g = threadIdx.x; g < tp.pg.num_groups; g += kThreads) {
+    for (int g = warp; g < tp.pg.num_groups; g += kWarps) {  // a warp per group, a lane per member
       int a, b, len;
-      if (prefix_group(tp.pg, g, B, p.max_blocks_per_seq, p.block_size, a, b, len))
+      if (prefix_group(tp.pg, g, B, p.max_blocks_per_seq, p.block_size, a, b, len) && lane == 0)
         flag_error(p.debug_err, PA_DEVERR_PREFIX);
-      for (int i = a; i < b; ++i) s_start[i] = len;
+      for (int i = a + lane; i < b; i += 32) s_start[i] = len;
     }
     __syncthreads();
   }

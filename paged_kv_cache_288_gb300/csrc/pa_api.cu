@@ -67,9 +67,9 @@ int current_sm_count() {
 }
 
 // How the shared prefixes are cut: chunks of chunk_len keys (whole key tiles
-// and whole blocks), so that the prefix grid has about two CTAs per SM (more
-// chunks mean more partial states to write and merge); num_chunks covers the
-// longest prefix.
+// and whole blocks), as many as fit the prefix grid into one wave of two
+// CTAs per SM (more chunks mean more partial states to write and merge, and
+// a second wave); num_chunks covers the longest prefix.
 struct PrefixPlan {
   int chunk_len = 0;
   int num_chunks = 0;
@@ -80,8 +80,8 @@ PrefixPlan prefix_plan(int num_groups, int max_group_size, int max_prefix_len, i
   PrefixPlan pl;
   if (num_groups <= 0 || max_group_size <= 0 || max_prefix_len <= 0) return pl;
   const int64_t per_set = static_cast<int64_t>(pa::prefix_row_tiles(max_group_size, group)) * units * num_groups;
-  const int64_t target = 2 * static_cast<int64_t>(sms > 0 ? sms : 1);
-  int64_t c = (target + per_set - 1) / per_set;
+  const int64_t target = 2 * static_cast<int64_t>(sms > 0 ? sms : 1);  // CTAs resident at once
+  int64_t c = target / per_set;  // one wave when the rows allow it
   const int64_t cmax = (max_prefix_len + pa::prefix_chunk_step(block_size) - 1) / pa::prefix_chunk_step(block_size);
   if (c > cmax) c = cmax;
   if (c < 1) c = 1;

@@ -13,8 +13,9 @@
 // Work. A CTA of four warps takes 64 rows (16 per warp: member r / G, query
 // head r % G of one KV unit) and one chunk of the group's shared keys; the
 // grid is (row tiles, KV units, group x chunk). Its K and V tiles (64 keys,
-// one 3-D TMA box per 128-byte column per block) go through a three-stage
-// ring in shared memory that all warps read. Per tile and warp: S = Q K^T as
+// one 3-D TMA box per 128-byte column per block, issued by the first lanes
+// of all four warps) go through a three-stage ring in shared memory that all
+// warps read. Per tile and warp: S = Q K^T as
 // mma.sync m16n8k16 with Q held as A fragments in registers and K^T as B
 // fragments (ldmatrix), eight independent 8-key accumulators; the online
 // softmax on the accumulators (running maximum in log2 units, running sum, O
@@ -137,7 +138,7 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_cons
     s_ent[i] = e;
   }
   if (threadIdx.x < kPxStages) {
-    mbar_init(full_bar(threadIdx.x), 1);
+    mbar_init(full_bar(threadIdx.x), kPxWarps);  // each warp's first lane issues a share of a tile
     mbar_init(empty_bar(threadIdx.x), kPxWarps);
   }
   if (threadIdx.x == 0) *s_abort = 0;
@@ -148,36 +149,41 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_cons
   const int kvh = kv_head_of(p, unit);
   const int hkv = p.kv_heads_phys;
   // TMA of key tile i into stage s: one box per 128-byte column per block
-  // the tile touches; blocks flagged out of range are skipped (their keys
-  // are masked below)
+  // the tile touches, K and V; blocks flagged out of range are skipped
+  // (their keys are masked below). A single issuing thread manages only a
+  // few boxes per microsecond, so the first lane of every warp issues its
+  // share (box b goes to warp b % kPxWarps) and arrives on the stage's
+  // barrier with the bytes of its own boxes.
   auto issue = [&](int i, int s) {
     const int t0 = k0 + i * kPxTile;
     const int bh = bs < kPxTile ? bs : kPxTile;  // rows per box
     const int nsub = kPxTile / bh;
-    uint32_t tx = 0;
-    for (int h = 0; h < nsub; ++h) {
-      const int tok = t0 + h * bh;
-      if (tok >= k1) break;
-      if (s_ent[(tok >> lbs) - j0] >= 0) tx += 2u * bh * D * 2;
-    }
-    mbar_arrive_expect_tx(full_bar(s), tx);
     const uint32_t kdst = stage0 + s * Gm::kStageBytes;
     const uint32_t vdst = kdst + Gm::kTileBytes;
-    for (int h = 0; h < nsub; ++h) {
+    constexpr int kBoxesPerSub = 2 * Gm::kBoxes;  // K and V columns of one block
+    uint32_t tx = 0;
+    for (int bx = warp; bx < nsub * kBoxesPerSub; bx += kPxWarps) {
+      const int h = bx / kBoxesPerSub;
       const int tok = t0 + h * bh;
-      if (tok >= k1) break;
+      if (tok < k1 && s_ent[(tok >> lbs) - j0] >= 0) tx += bh * 128;
+    }
+    mbar_arrive_expect_tx(full_bar(s), tx);
+    for (int bx = warp; bx < nsub * kBoxesPerSub; bx += kPxWarps) {
+      const int h = bx / kBoxesPerSub, r = bx % kBoxesPerSub;
+      const int tok = t0 + h * bh;
+      if (tok >= k1) continue;
       const int e = s_ent[(tok >> lbs) - j0];
       if (e < 0) continue;
       const int z = e * hkv + kvh;
       const int off = tok & (bs - 1);
-#pragma unroll
-      for (int c = 0; c < Gm::kBoxes; ++c) {
+      const int c = r >> 1;
+      if ((r & 1) == 0)
         tma_load_3d(kdst + c * Gm::kBoxBytes + h * bh * 128, &tmap_k, c * 64, off, z, full_bar(s));
+      else
         tma_load_3d(vdst + c * Gm::kBoxBytes + h * bh * 128, &tmap_v, c * 64, off, z, full_bar(s));
-      }
     }
   };
-  if (threadIdx.x == 0)
+  if (lane == 0)
     for (int i = 0; i < kPxStages && i < ntiles; ++i) issue(i, i);
 
   // every member of this CTA's rows must hold the same blocks in the chunk
@@ -338,11 +344,11 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_cons
       }
     }
 
-    // stage s is free again: the first thread refills it with the tile
-    // kPxStages ahead once every warp is done with it
+    // stage s is free again: once every warp is done with it, each warp's
+    // first lane issues its share of the tile kPxStages ahead
     __syncwarp();
     if (lane == 0) mbar_arrive(empty_bar(s));
-    if (threadIdx.x == 0 && i + kPxStages < ntiles) {
+    if (lane == 0 && i + kPxStages < ntiles) {
       if (!mbar_wait_bounded(empty_bar(s), par)) {
         flag_error(p.debug_err, PA_DEVERR_TIMEOUT);
         atomicExch(s_abort, 1);

@@ -84,7 +84,11 @@ def rank_seed(base, rank):
 
 def make_case(name, rank):
     if name == "tiny":
-        return workloads.tiny()[0]
+        # the pool before the append, with the appended token of each
+        # sequence as the step's cache write and the lengths after it
+        before, step = workloads.tiny()
+        return workloads.DecodeCase(**{**step.__dict__, "k_cache": before.k_cache,
+                                       "v_cache": before.v_cache})
     if name == "llama8b":
         return workloads.llama8b(seed=rank_seed(1002, rank))
     if name == "llama8b_mha":
@@ -393,6 +397,14 @@ def peak_hbm():
     return 6800.0, "fallback"
 
 
+def shared_groups_of(case):
+    """Groups of sequences sharing leading whole blocks, from the tables the
+    decode reads (the shared-prefix workload's tables after its copy-on-write
+    of the partly filled last prefix block)."""
+    from paged_kv_cache_288_gb300.block_pool import shared_prefix_groups
+    return shared_prefix_groups(case.block_tables, case.context_lens, case.block_size)
+
+
 def unique_decode_bytes(case):
     """Algorithmic bytes of one pa_decode counting each physical block's KV
     once: a block that several tables share (a common prefix) need come from
@@ -575,9 +587,11 @@ def decode_result(case, step_ms, dec_ms, launches, part, peak, peak_src, workloa
 
 def run_config_suite(pa, device, stream, flush_l2, K, W, peak, peak_src):
     """The other workloads' decode numbers, timed in the same run as the
-    headline line: the shared-prefix serving batch (logical and unique-byte
-    rooflines), the long-context batch at every block size (512-token split
-    path and the library's schedule) and the 32-layer E4M3 decode step."""
+    headline line: the tiny case (latency), the shared-prefix serving batch
+    (logical and unique-byte rooflines; per-sequence decode and the shared
+    blocks read once per group), the long-context batch at every block size
+    (512-token split path and the library's schedule) and the 32-layer E4M3
+    decode step."""
     out = {}
 
     def one(name, case, parts, extra_fn=None, groups=None, key=None):
@@ -602,11 +616,10 @@ def run_config_suite(pa, device, stream, flush_l2, K, W, peak, peak_src):
                                     "peak_source": peak_src, "unit": "GB/s", "frac": round(a / peak, 4),
                                     "note": "each shared block's KV counted once"}}
 
+    one("tiny", make_case("tiny", 0), [0])
     one("shared_prefix", workloads.shared_prefix(), [0], shared_extra)
     sp = workloads.shared_prefix()
-    shared_tokens = sp.meta["prefix_len"] // sp.block_size * sp.block_size
-    one("shared_prefix", sp, [0], shared_extra, groups=([0, sp.num_seqs], [shared_tokens]),
-        key="shared_prefix/grouped")
+    one("shared_prefix", sp, [0], shared_extra, groups=shared_groups_of(sp), key="shared_prefix/grouped")
     for bs in (8, 16, 32, 64):
         one(f"long_context_bs{bs}", workloads.long_context(bs), [512, 0])
     out["fp8_step"] = run_fp8_step(pa, device, stream, flush_l2, K, W, peak, peak_src)
@@ -717,10 +730,9 @@ def run_ours(args, world, rank, local):
     case = make_case(args.workload, rank)
     part = args.partition_size
     groups = None
-    if args.shared_groups and args.workload in ("shared_prefix", "prefix_cache"):
-        # one group: every sequence shares the prefix's whole blocks
-        plen = case.meta["prefix_len"] if "prefix_len" in case.meta else 1016
-        groups = ([0, case.num_seqs], [plen // case.block_size * case.block_size])
+    if args.shared_groups:
+        # the sharing in the tables (after any copy-on-write), found on the host
+        groups = shared_groups_of(case)
     dd = DeviceDecode(pa, case, device, part, groups)
     case = dd.case
 

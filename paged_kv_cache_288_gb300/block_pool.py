@@ -257,3 +257,43 @@ class PrefixCache:
         for b in blocks:
             if b in self.key_of:
                 self._touch(b)
+
+
+def shared_prefix_groups(block_tables, context_lens, block_size, min_shared_blocks=1):
+    """Groups of consecutive sequences that share the leading blocks of their
+    tables, in the form pa_decode_shared_prefix takes.
+
+    Sharing a prompt prefix stores its blocks once and points every table at
+    them (serving-paged-attention, "공유는 표를 베끼는 일이 된다"); this finds
+    that sharing again from the tables themselves, so the decode can read the
+    shared blocks once per group. Walking the batch in order, a sequence
+    joins the current group while its first k table entries equal the group
+    leader's for some k >= min_shared_blocks (k is the group's common run,
+    shrunk as members join), and only blocks that lie wholly inside every
+    member's context count. Returns (group_start int32 [G + 1], group_prefix
+    int32 [G] in tokens); a sequence that shares nothing is a group of its
+    own with prefix 0.
+    """
+    tables = np.asarray(block_tables)
+    lens = np.asarray(context_lens, dtype=np.int64)
+    B = len(lens)
+    starts, prefixes = [0], []
+    i = 0
+    while i < B:
+        full_i = int(lens[i]) // block_size  # whole blocks of the leader
+        run = full_i
+        j = i + 1
+        while j < B:
+            full_j = int(lens[j]) // block_size
+            k = min(run, full_j)
+            eq = tables[i, :k] == tables[j, :k]
+            common = k if eq.all() else int(np.argmin(eq))
+            if common < min_shared_blocks:
+                break
+            run = common
+            j += 1
+        shared = run if j - i > 1 else 0
+        prefixes.append(shared * block_size)
+        starts.append(j)
+        i = j
+    return np.asarray(starts, dtype=np.int32), np.asarray(prefixes, dtype=np.int32)

@@ -190,3 +190,40 @@ def test_prefix_cache_one_hundred_requests_over_one_system_prompt():
     assert all(pool.refcount[b] == 101 for b in shared)
     # blocks in use: 63 shared + per request ceil((1056 - 1008) / 16) = 3 own
     assert pool.used_blocks() == 63 + 100 * 3
+
+
+def test_shared_prefix_groups_from_tables():
+    """Groups found from the tables: consecutive sequences whose leading
+    whole blocks agree, the common run shrinking as members join; a lone
+    sequence has prefix 0; a partly filled last block is never shared."""
+    from paged_kv_cache_288_gb300.block_pool import shared_prefix_groups
+    t = np.array([
+        [5, 6, 7, 9],     # 0: group A
+        [5, 6, 7, 10],    # 1: group A (3 common blocks)
+        [5, 6, 11, 12],   # 2: group A, common run shrinks to 2
+        [20, 21, 0, 0],   # 3: alone
+        [30, 31, 32, 0],  # 4: group B
+        [30, 31, 33, 0],  # 5: group B (2 common blocks)
+    ], dtype=np.int32)
+    lens = np.array([64, 60, 50, 30, 40, 40])  # block size 16
+    gs, gp = shared_prefix_groups(t, lens, 16)
+    assert gs.tolist() == [0, 3, 4, 6]
+    assert gp.tolist() == [32, 0, 32]
+    # a shared block only partly inside a member's context does not count
+    gs, gp = shared_prefix_groups(t[:2], np.array([64, 40]), 16)
+    assert gs.tolist() == [0, 2] and gp.tolist() == [32]
+
+
+def test_shared_prefix_groups_of_a_prefix_cache_batch():
+    """100 requests with one 1016-token system prompt admitted through the
+    prefix cache form one group sharing its 63 whole blocks."""
+    from paged_kv_cache_288_gb300.block_pool import shared_prefix_groups
+    rng = np.random.default_rng(3)
+    pool = BlockPool(4000, 16)
+    cache = PrefixCache(pool)
+    system = rng.integers(0, 32000, 1016)
+    for i in range(100):
+        cache.add_sequence(i, np.concatenate([system, rng.integers(0, 32000, int(rng.integers(32, 513)))]))
+    ids = list(range(100))
+    gs, gp = shared_prefix_groups(pool.block_table_array(ids), pool.context_lens(ids), 16)
+    assert gs.tolist() == [0, 100] and gp.tolist() == [1008]

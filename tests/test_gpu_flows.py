@@ -163,4 +163,18 @@ def test_prefix_cache_sharing_matches_private_copies():
         assert np.allclose(own[0], ref[i], rtol=0, atol=1e-12)
     torch.cuda.synchronize()
     assert_close(out, ref, dtype, dtype, "prefix-cache decode")
+    # the sharing the prefix cache set up, found from the tables, read once:
+    # one group of the four requests over the 4 whole blocks of the prompt
+    from paged_kv_cache_288_gb300.block_pool import shared_prefix_groups
+    gs, gp = shared_prefix_groups(tables, lens, bs)
+    assert gs.tolist() == [0, 4] and gp.tolist() == [64]
+    B, mx = len(ids), int(lens.max())
+    n = pa.decode_shared_prefix_workspace_size(B, Hq, Hkv, d, bs, len(gp), 4, int(gp.max()))
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    grouped = torch.full((B, Hq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    pa.decode_shared_prefix(grouped, dev(q, dtype), P.kd, P.vd, torch.from_numpy(tables).cuda(),
+                            torch.from_numpy(lens).cuda(), 0.125, mx, torch.from_numpy(gs).cuda(),
+                            torch.from_numpy(gp).cuda(), 4, int(gp.max()), ws, debug_err=P.err)
+    torch.cuda.synchronize()
+    assert_close(grouped, ref, dtype, dtype, "prefix-cache decode, shared blocks read once")
     P.check_pools()

@@ -237,6 +237,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
   int* s_start = s_prefP;
   auto start_of = [&](int i) -> int { return prefix_mode ? s_start[i] : 0; };
   __shared__ int s_warp_sum[kWarps][2];
+  __shared__ int64_t s_queue[kWarps][NS + 1][3];  // claimed ranges waiting: start, end, first slot
 
   if (threadIdx.x < kWarps * NS) mbar_init(smem_u32(&bars[threadIdx.x]), 1);
   mbar_init_fence();
@@ -616,24 +617,31 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
 
   // ---- the warp's pipeline ----------------------------------------------
   // The producer side runs up to NS tiles ahead of the consumer side; when it
-  // reaches the end of its range it claims the next chunk, which the consumer
-  // takes over when it reaches the same point (chunks are longer than NS
-  // tiles, so at most one claimed range waits).
+  // reaches the end of its range it claims the next one, which the consumer
+  // takes over when it reaches the same point. Claimed ranges wait in a small
+  // queue in shared memory (lane 0 writes, the warp reads): every waiting
+  // range but the newest has a tile in the ring, so NS + 1 entries suffice
+  // even when ranges are a single tile (a split-path partition of one tile).
   Cursor pc, cc;
   cursor_at(pc, cr0, s_prefT, B, Hkv);
   cc = pc;
   int64_t pr1 = cr1;
-  int64_t nr0 = 0, nr1 = 0, nslot = 0;
-  bool have_next = false, prod_done = false;
+  int q_head = 0, q_count = 0;  // warp-uniform
+  bool prod_done = false;
   auto advance_producer = [&]() {
     cursor_next(pc, s_prefT, B, Hkv);
     if (pc.f == pr1) {
       int64_t a, b, sl;
       if (claim(a, b, sl)) {
-        nr0 = a;
-        nr1 = b;
-        nslot = sl;
-        have_next = true;
+        int i = q_head + q_count;
+        if (i > NS) i -= NS + 1;
+        if (lane == 0) {
+          s_queue[warp][i][0] = a;
+          s_queue[warp][i][1] = b;
+          s_queue[warp][i][2] = sl;
+        }
+        __syncwarp();
+        ++q_count;
         pr1 = b;
         cursor_at(pc, a, s_prefT, B, Hkv);
       } else {
@@ -825,11 +833,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
       flush(seq, kvh, tp.part_tiles ? t / tp.part_tiles : 0, whole, first_piece ? cslot : cslot + 1);
       first_piece = false;
       if (range_end) {
-        if (!have_next) break;
-        cr0 = nr0;
-        cr1 = nr1;
-        cslot = nslot;
-        have_next = false;
+        if (q_count == 0) break;
+        cr0 = s_queue[warp][q_head][0];
+        cr1 = s_queue[warp][q_head][1];
+        cslot = s_queue[warp][q_head][2];
+        q_head = q_head == NS ? 0 : q_head + 1;
+        --q_count;
         first_piece = true;
         cursor_at(cc, cr0, s_prefT, B, Hkv);
       }

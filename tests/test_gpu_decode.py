@@ -128,6 +128,38 @@ def test_split_path_matches_oracle_and_other_schedules(partition_size, bs):
     assert np.all(np.abs(a - b) <= 2e-3 + 1e-2 * np.abs(b))
 
 
+@pytest.mark.parametrize("partition_size", [16, 32])
+def test_split_path_partitions_shorter_than_the_ring(partition_size):
+    """Partitions of one or two 16-token tiles and many more partitions than
+    warps: in the claimed quarter a warp's loads run up to three tiles ahead,
+    so it claims several partitions before it computes the first of them;
+    they must be taken in the order they were claimed."""
+    lengths = [12000, 9000, 7001, 5003, 3]
+    case = workloads.paged_case(960 + partition_size, lengths, 16, 4, 128, 16, BF16, name=f"ring{partition_size}")
+    _check(case, partition_size=partition_size)
+
+
+def test_fp8_split_path_single_tile_partitions():
+    """The E4M3 kernel (32-token tiles, two ring slots per warp) with 32-token
+    partitions: every claimed partition is a single tile."""
+    lengths = [9000, 7000, 5001, 33]
+    case = workloads.fp8_layer(970, lengths, num_heads=16, num_kv_heads=4, head_dim=128,
+                               block_size=16, src_dtype=BF16, name="fp8_ring")
+    dc = DeviceCase(case)
+    pa.reshape_and_cache(dc.new_key, dc.new_value, dc.k_cache, dc.v_cache, dc.slot_mapping,
+                         k_scale=dc.k_scale, v_scale=dc.v_scale, debug_err=dc.debug_err)
+    kc, vc = case.k_cache.copy(), case.v_cache.copy()
+    oracle.reshape_and_cache(case.new_key, case.new_value, kc, vc, case.slot_mapping, 16, BF16,
+                             FP8_E4M3, case.k_scale, case.v_scale)
+    ref = oracle_decode(case, k_cache=kc, v_cache=vc)
+    for part in (32, 0):
+        out = run_decode(pa, dc, partition_size=part)
+        torch.cuda.synchronize()
+        max_abs, _ = assert_close(out, ref, BF16, FP8_E4M3, f"fp8 part={part}")
+        assert max_abs <= 3e-2, max_abs
+    assert dc.debug_err.item() == 0
+
+
 def test_empty_and_single_token_sequences():
     lengths = [0, 1, 0, 3, 1]
     case = workloads.paged_case(700, lengths, 4, 2, 64, 16, F16, name="empty")

@@ -71,9 +71,9 @@ struct Geom {
 };
 
 struct SlotMeta {
-  uint32_t mask;  // bit t: token t of the tile holds data
   float ks[4];    // E4M3 K scale of tokens 8i .. 8i+7
   float vs[4];    // E4M3 V scale
+  uint32_t mask;  // bit t: token t of the tile holds data
   uint32_t pad[3];
 };
 
@@ -434,33 +434,48 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
       mask |= bit_range(first, min(bh, valid - first));
       tx += 2u * bh * Gm::kRowBytes;
     }
+    // lane 0: the slot's token mask and, for E4M3 caches, the scales of its
+    // 8-token groups (vector stores), then the expected bytes
     if (lane == 0) {
       SlotMeta& m = my_meta[s];
-      m.mask = mask;
+      if constexpr (kFp8) {
+        float k4[4], v4[4];
 #pragma unroll
-      for (int i = 0; i < TT / 8; ++i) {
-        const int h = (8 * i) / bh;  // the block holding tokens 8i .. 8i+7
-        float k = ks[0], v = vs[0];
+        for (int i = 0; i < 4; ++i) {
+          const int h = (8 * i) / bh;  // the block holding tokens 8i .. 8i+7
+          k4[i] = ks[0];
+          v4[i] = vs[0];
 #pragma unroll
-        for (int q = 1; q < kMaxSub; ++q)
-          if (h == q) {
-            k = ks[q];
-            v = vs[q];
-          }
-        m.ks[i] = k;
-        m.vs[i] = v;
-      }
-      mbar_arrive_expect_tx(bar, tx);
-#pragma unroll
-      for (int h = 0; h < kMaxSub; ++h) {
-        if (phys[h] < 0) continue;
-        const int z = phys[h] * p.kv_heads_phys + kv_head_of(p, c.kvh);
-        const uint32_t rows_before = h * bh * 128;  // boxes of later blocks sit after earlier ones
-#pragma unroll
-        for (int b = 0; b < Gm::kBoxes; ++b) {
-          tma_load_3d(kdst + b * Gm::kBoxBytes + rows_before, &tmap_k, b * Gm::kBoxW, off, z, bar);
-          tma_load_3d(vdst + b * Gm::kBoxBytes + rows_before, &tmap_v, b * Gm::kBoxW, off, z, bar);
+          for (int q = 1; q < kMaxSub; ++q)
+            if (h == q) {
+              k4[i] = ks[q];
+              v4[i] = vs[q];
+            }
         }
+        *reinterpret_cast<float4*>(m.ks) = make_float4(k4[0], k4[1], k4[2], k4[3]);
+        *reinterpret_cast<float4*>(m.vs) = make_float4(v4[0], v4[1], v4[2], v4[3]);
+      }
+      m.mask = mask;
+      mbar_arrive_expect_tx(bar, tx);
+    }
+    __syncwarp();
+    // the boxes, one per lane: box i is column (i / 2) % kBoxes of block
+    // i / (2 kBoxes), of K (i even) or V (i odd); a single thread issues
+    // only a few boxes per microsecond
+    constexpr int kPerSub = 2 * Gm::kBoxes;
+    if (lane < kMaxSub * kPerSub) {
+      const int h = lane / kPerSub, r = lane % kPerSub, b = r >> 1;
+      int ph = phys[0];
+#pragma unroll
+      for (int q = 1; q < kMaxSub; ++q)
+        if (h == q) ph = phys[q];
+      if (ph >= 0) {
+        const int z = ph * p.kv_heads_phys + kv_head_of(p, c.kvh);
+        const uint32_t at = b * Gm::kBoxBytes + h * bh * 128;  // boxes of later blocks sit after earlier ones
+        if (r & 1)
+          tma_load_3d(vdst + at, &tmap_v, b * Gm::kBoxW, off, z, bar);
+        else
+          tma_load_3d(kdst + at, &tmap_k, b * Gm::kBoxW, off, z, bar);
       }
     }
   };
@@ -705,7 +720,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
           mma_f16(sb, a1, qb[k + 1][0], qb[k + 1][1]);
         }
       }
-      const float sc0 = p.scale_log2 * mt.ks[2 * rt], sc1 = p.scale_log2 * mt.ks[2 * rt + 1];
+      // the block's K scale for E4M3 caches (the slot's scales are only
+      // written for them)
+      const float sc0 = kFp8 ? p.scale_log2 * mt.ks[2 * rt] : p.scale_log2;
+      const float sc1 = kFp8 ? p.scale_log2 * mt.ks[2 * rt + 1] : p.scale_log2;
       sv[rt][0] = (sa[0] + sb[0]) * sc0;
       sv[rt][1] = (sa[1] + sb[1]) * sc0;
       sv[rt][2] = (sa[2] + sb[2]) * sc1;
@@ -929,24 +947,37 @@ __global__ void __launch_bounds__(NT, 1024 / NT) tc_merge_kernel(const TcParams 
   const int64_t W = tp.num_warps;
   const int64_t seg0 = static_cast<int64_t>(before) * Hkv + static_cast<int64_t>(kvh) * tiles;
   const int64_t seg1 = seg0 + tiles;
-  const Sched sc = make_sched(U, W);
-  const int64_t S = sc.S, C = sc.C;
-  // static shares meeting [seg0, min(seg1, S)): warp w holds [w*S/W, (w+1)*S/W),
-  // so the owner of tile x < S is ceil((x+1)W/S) - 1
-  int64_t ws0 = 0, nstat = 0;
-  if (tiles > 0 && seg0 < S) {
-    const int64_t e = seg1 < S ? seg1 : S;
-    ws0 = ((seg0 + 1) * W - 1) / S;
-    nstat = (e * W - 1) / S - ws0 + 1;
+  // The schedule's quantities for this segment, derived by one thread and
+  // shared (64-bit divisions are long instruction sequences).
+  __shared__ int64_t s_sched[6];
+  if (threadIdx.x == 0) {
+    const Sched sc = make_sched(U, W);
+    const int64_t S = sc.S, C = sc.C;
+    // static shares meeting [seg0, min(seg1, S)): warp w holds [w*S/W,
+    // (w+1)*S/W), so the owner of tile x < S is ceil((x+1)W/S) - 1
+    int64_t ws0 = 0, nstat = 0;
+    if (tiles > 0 && seg0 < S) {
+      const int64_t e = seg1 < S ? seg1 : S;
+      ws0 = ((seg0 + 1) * W - 1) / S;
+      nstat = (e * W - 1) / S - ws0 + 1;
+    }
+    // chunks meeting [max(seg0, S), seg1)
+    int64_t k0 = 0, ndyn = 0;
+    if (tiles > 0 && seg1 > S) {
+      const int64_t a = seg0 > S ? seg0 : S;
+      k0 = (a - S) / C;
+      ndyn = (seg1 - 1 - S) / C - k0 + 1;
+    }
+    s_sched[0] = S;
+    s_sched[1] = C;
+    s_sched[2] = ws0;
+    s_sched[3] = nstat;
+    s_sched[4] = k0;
+    s_sched[5] = ndyn;
   }
-  // chunks meeting [max(seg0, S), seg1)
-  int64_t k0 = 0, ndyn = 0;
-  if (tiles > 0 && seg1 > S) {
-    const int64_t a = seg0 > S ? seg0 : S;
-    k0 = (a - S) / C;
-    ndyn = (seg1 - 1 - S) / C - k0 + 1;
-  }
-  const int ndec = static_cast<int>(nstat + ndyn);
+  __syncthreads();
+  const int64_t S = s_sched[0], C = s_sched[1], ws0 = s_sched[2], nstat = s_sched[3], k0 = s_sched[4];
+  const int ndec = static_cast<int>(nstat + s_sched[5]);
   if (ndec == 1 && npre == 0) return;  // one range held the whole segment and wrote the rows
   const int nc = ndec + npre;
   // a whole segment of a sequence with a shared prefix left its state in the

@@ -516,6 +516,32 @@ class DeviceDecode:
                        partition_size=self.part, workspace=self.ws, debug_err=self.err)
 
 
+class PackedH2D:
+    """One pinned host staging buffer and one device buffer that hold several
+    input tensors, each at a 256-byte boundary: a step's inputs cross the host
+    link in a single copy, and the library's calls read device views into it."""
+
+    def __init__(self, tensors, device):
+        offs, n = [], 0
+        for t in tensors:
+            offs.append(n)
+            n += (t.numel() * t.element_size() + 255) // 256 * 256
+        self.host = torch.empty(max(n, 256), dtype=torch.uint8).pin_memory()
+        self.dev = torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+        self.views = []
+        for t, o in zip(tensors, offs):
+            nb = t.numel() * t.element_size()
+            self.host[o:o + nb].copy_(t.detach().cpu().contiguous().view(-1).view(torch.uint8))
+            self.views.append(self.dev[o:o + nb].view(t.dtype).view(t.shape))
+
+    @property
+    def nbytes(self):
+        return self.dev.numel()
+
+    def h2d(self):
+        self.dev.copy_(self.host, non_blocking=True)
+
+
 def make_flush(device):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
 
@@ -749,15 +775,13 @@ def run_ours(args, world, rank, local):
     if dd.err.item() != 0:
         raise RuntimeError(f"device error word {dd.err.item():#x}")
 
-    # end to end through the public API with host buffers: inputs H2D, output D2H
-    q, nk, nv, slots, tables, lens = dd.q, dd.nk, dd.nv, dd.slots, dd.tables, dd.lens
-    pin = lambda t: t.cpu().pin_memory()  # noqa: E731
-    h_q, h_nk, h_nv, h_slots = pin(q), pin(nk), pin(nv), pin(slots)
-    h_tables, h_lens = pin(tables), pin(lens)
+    # end to end through the public API with host buffers: the step's inputs
+    # (q, the new token's K/V, its slots, the tables, the lengths) cross in one
+    # copy from a pinned staging buffer, the output comes back
+    packed = PackedH2D([dd.q, dd.nk, dd.nv, dd.slots, dd.tables, dd.lens], device)
+    d_q, d_nk, d_nv, d_slots, d_tables, d_lens = packed.views
     h_out = torch.empty(dd.out.shape, dtype=dd.out.dtype).pin_memory()
-    d_q, d_nk, d_nv = torch.empty_like(q), torch.empty_like(nk), torch.empty_like(nv)
-    d_slots, d_tables, d_lens = torch.empty_like(slots), torch.empty_like(tables), torch.empty_like(lens)
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_nk, h_nv, h_slots, h_tables, h_lens))
+    h2d = packed.nbytes
     d2h = h_out.numel() * h_out.element_size()
     Ke = max(1, min(K, 200))
     eev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Ke)]
@@ -766,9 +790,7 @@ def run_ours(args, world, rank, local):
     for k in range(Ke):
         flush_l2()
         eev[k][0].record(stream)
-        for dst, src in ((d_q, h_q), (d_nk, h_nk), (d_nv, h_nv), (d_slots, h_slots),
-                         (d_tables, h_tables), (d_lens, h_lens)):
-            dst.copy_(src, non_blocking=True)
+        packed.h2d()
         dd.write(d_nk, d_nv, d_slots)
         dd.decode(q=d_q, tables=d_tables, lens=d_lens)
         h_out.copy_(dd.out, non_blocking=True)

@@ -51,17 +51,18 @@ constexpr int kMaxG = 8;       // MMA N
 constexpr uint32_t kFull = 0xffffffffu;
 
 // A tile is TT tokens (16 or 32, one or two MMA row tiles) of one
-// (sequence, KV head): TT rows of K and TT rows of V in one ring slot.
-template <typename KT, int D, int TT>
+// (sequence, KV unit): TT rows of K and TT rows of V of each of the unit's HP
+// KV heads in one ring slot (head h's rows after head h-1's).
+template <typename KT, int D, int TT, int HP = 1>
 struct Geom {
   static constexpr int kElem = int(sizeof(KT));
   static constexpr int kRowBytes = D * kElem;
   static constexpr int kBoxW = 128 / kElem;        // elements in one 128-byte box row
   static constexpr int kBoxes = kRowBytes / 128;   // boxes across a row
-  static constexpr int kBoxBytes = TT * 128;       // one 128-byte column of the tile
-  static constexpr int kRowTiles = TT / kRowTile;
+  static constexpr int kBoxBytes = TT * HP * 128;  // one 128-byte column of the tile
+  static constexpr int kRowTiles = TT / kRowTile * HP;  // 16-row tiles of K (or V) in a slot
   static constexpr uint32_t kFullMask = TT == 32 ? 0xffffffffu : 0xffffu;
-  static constexpr int kTileBytes = TT * kRowBytes;
+  static constexpr int kTileBytes = TT * HP * kRowBytes;
   static constexpr int kSlotBytes = 2 * kTileBytes;
   // E4M3 tiles carry more conversion work per byte, so an SM runs more of
   // their warps (each with a shorter ring) to hide its latencies
@@ -203,14 +204,15 @@ __device__ __forceinline__ void cursor_next(Cursor& c, const int* prefT, int B, 
   if (c.seq < B) c.tiles = prefT[c.seq + 1] - prefT[c.seq];
 }
 
-template <typename QT, typename KT, int D, int TT>
-__global__ void __launch_bounds__(Geom<KT, D, TT>::kWarps * 32, 1)
+template <typename QT, typename KT, int D, int TT, int HP>
+__global__ void __launch_bounds__(Geom<KT, D, TT, HP>::kWarps * 32, 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                  const __grid_constant__ CUtensorMap tmap_v, const TcParams tp) {
-  using Gm = Geom<KT, D, TT>;
+  using Gm = Geom<KT, D, TT, HP>;
   constexpr int kWarps = Gm::kWarps;
   constexpr int kThreads = kWarps * 32;
-  constexpr int RT = Gm::kRowTiles;
+  constexpr int RT = Gm::kRowTiles;   // 16-row tiles of K (or V) in a slot
+  constexpr int RS = TT / kRowTile;   // 16-token tiles of S
   constexpr bool kFp8 = is_fp8<KT>::value;
   constexpr int NS = Gm::kSlots;
   const DecodeParams& p = tp.p;
@@ -221,6 +223,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2;   // MMA group id: accumulator row, B-operand column
   const int tig = lane & 3;  // thread in group
+  // HP = 2: a unit is two KV heads of G / 2 query heads each; MMA column c
+  // belongs to the unit's KV head c / (G / 2). This lane's B-operand column
+  // is g, its accumulator columns 2 tig and 2 tig + 1 (one KV head: G / 2 is
+  // 2 or 4).
+  const int hd_b = HP == 2 ? g / (G >> 1) : 0;
+  const int hd_c = HP == 2 ? min((2 * tig) / (G >> 1), 1) : 0;
 
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -376,8 +384,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
   // block-table window: lane l holds entry win_base + l of sequence win_seq
   // and, for E4M3 caches, that block's K and V scales for KV head win_kvh
   int win_seq = -1, win_base = 0, win_val = -1, win_kvh = -1;
-  float win_ks = 1.f, win_vs = 1.f;
-  auto table_entry = [&](int seq, int kvh, int j, float& ksc, float& vsc) -> int {
+  float win_ks = 1.f, win_vs = 1.f, win_ks1 = 1.f, win_vs1 = 1.f;  // (HP = 2: ks1, vs1 of the second head)
+  auto table_entry = [&](int seq, int kvh, int j, float& ksc, float& vsc, float& ksc1, float& vsc1) -> int {
     if (seq != win_seq || j < win_base || j >= win_base + 32) {
       win_seq = seq;
       win_base = j;
@@ -389,12 +397,21 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
       if (kvh != win_kvh) {
         win_kvh = kvh;
         const bool ok = win_val >= 0 && win_val < p.num_blocks;
-        const int64_t si = static_cast<int64_t>(ok ? win_val : 0) * p.kv_heads_phys + kv_head_of(p, kvh);
+        const int64_t si = static_cast<int64_t>(ok ? win_val : 0) * p.kv_heads_phys +
+                           (HP == 2 ? 2 * kvh : kv_head_of(p, kvh));
         win_ks = ok ? p.k_scale[si] : 1.f;
         win_vs = ok ? p.v_scale[si] : 1.f;
+        if constexpr (HP == 2) {
+          win_ks1 = ok ? p.k_scale[si + 1] : 1.f;
+          win_vs1 = ok ? p.v_scale[si + 1] : 1.f;
+        }
       }
       ksc = __shfl_sync(kFull, win_ks, j - win_base);
       vsc = __shfl_sync(kFull, win_vs, j - win_base);
+      if constexpr (HP == 2) {
+        ksc1 = __shfl_sync(kFull, win_ks1, j - win_base);
+        vsc1 = __shfl_sync(kFull, win_vs1, j - win_base);
+      }
     }
     return __shfl_sync(kFull, win_val, j - win_base);
   };
@@ -418,27 +435,37 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     uint32_t mask = 0, tx = 0;
     int phys[kMaxSub];
     float ks[kMaxSub], vs[kMaxSub];
+    float ks1 = 1.f, vs1 = 1.f;  // HP = 2: the second head's scales (the tile lies in one block)
     const int off = tok0 & (bs - 1);  // 0 when the tile spans blocks
 #pragma unroll
     for (int h = 0; h < kMaxSub; ++h) {
       phys[h] = -1;
       ks[h] = vs[h] = 1.f;
+      float k1 = 1.f, v1 = 1.f;
       const int first = h * bh;
       if (h >= nsub || first >= valid || first < skip) continue;  // skip is a multiple of bh
-      phys[h] = table_entry(c.seq, c.kvh, (tok0 >> lbs) + h, ks[h], vs[h]);
+      phys[h] = table_entry(c.seq, c.kvh, (tok0 >> lbs) + h, ks[h], vs[h], k1, v1);
+      if (HP == 2 && h == 0) {
+        ks1 = k1;
+        vs1 = v1;
+      }
       if (phys[h] < 0 || phys[h] >= p.num_blocks) {
         if (lane == 0) flag_error(p.debug_err, PA_DEVERR_BLOCK_RANGE);
         phys[h] = -1;
         continue;
       }
       mask |= bit_range(first, min(bh, valid - first));
-      tx += 2u * bh * Gm::kRowBytes;
+      tx += 2u * HP * bh * Gm::kRowBytes;
     }
     // lane 0: the slot's token mask and, for E4M3 caches, the scales of its
     // 8-token groups (vector stores), then the expected bytes
     if (lane == 0) {
       SlotMeta& m = my_meta[s];
-      if constexpr (kFp8) {
+      if constexpr (kFp8 && HP == 2) {
+        // the tile's block: each head's scales
+        *reinterpret_cast<float4*>(m.ks) = make_float4(ks[0], ks1, 1.f, 1.f);
+        *reinterpret_cast<float4*>(m.vs) = make_float4(vs[0], vs1, 1.f, 1.f);
+      } else if constexpr (kFp8) {
         float k4[4], v4[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -470,7 +497,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
       for (int q = 1; q < kMaxSub; ++q)
         if (h == q) ph = phys[q];
       if (ph >= 0) {
-        const int z = ph * p.kv_heads_phys + kv_head_of(p, c.kvh);
+        // HP = 2: one box holds both heads' rows (heads 2u, 2u + 1 are adjacent)
+        const int z = ph * p.kv_heads_phys + (HP == 2 ? 2 * c.kvh : kv_head_of(p, c.kvh));
         const uint32_t at = b * Gm::kBoxBytes + h * bh * 128;  // boxes of later blocks sit after earlier ones
         if (r & 1)
           tma_load_3d(vdst + at, &tmap_v, b * Gm::kBoxW, off, z, bar);
@@ -690,53 +718,65 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const uint32_t kbase = slot_base0 + s * Gm::kSlotBytes;
     const uint32_t vbase = kbase + Gm::kTileBytes;
 
-    // S^T = K Q^T per 16-token row tile: rows = tokens, columns = query heads
-    float sv[RT][4];
+    // S^T = K Q^T per 16-token row tile: rows = tokens, columns = query heads.
+    // HP = 2: the two heads' K rows meet q with the other head's columns
+    // zeroed (a block-diagonal q), both into the same accumulators.
+    float sv[RS][4];
 #pragma unroll
-    for (int rt = 0; rt < RT; ++rt) {
+    for (int rs = 0; rs < RS; ++rs) {
       float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-      const int row = rt * kRowTile + (lane & 15);
-      if constexpr (!kFp8) {
 #pragma unroll
-        for (int k = 0; k < Gm::kSteps; ++k) {
-          uint32_t a[4];
-          ldsm_x4(tile_addr<Gm::kBoxBytes>(kbase, row, 2 * k + (lane >> 4)), a[0], a[1], a[2], a[3]);
-          if constexpr (std::is_same<KT, bf16>::value) mma_bf16((k & 1) ? sb : sa, a, qb[k][0], qb[k][1]);
-          else mma_f16((k & 1) ? sb : sa, a, qb[k][0], qb[k][1]);
-        }
-      } else {
+      for (int hh = 0; hh < HP; ++hh) {
+        const int rt = hh * RS + rs;
+        const int row = rt * kRowTile + (lane & 15);
+        [[maybe_unused]] const bool qon = HP == 1 || hd_b == hh;
+        if constexpr (!kFp8) {
 #pragma unroll
-        for (int k = 0; k < Gm::kSteps; k += 2) {
-          uint32_t r[4];
-          ldsm_x4(tile_addr<Gm::kBoxBytes>(kbase, row, k + (lane >> 4)), r[0], r[1], r[2], r[3]);
-          // a lane's four bytes of a row are d = 16c + 4tig .. +3: the low pair
-          // feeds contraction slots 2tig, 2tig+1, the high pair 2tig+8, 2tig+9
-          uint32_t a0[4], a1[4];
-          e4m3x4_to_f16x2x2(r[0], a0[0], a0[2]);
-          e4m3x4_to_f16x2x2(r[1], a0[1], a0[3]);
-          e4m3x4_to_f16x2x2(r[2], a1[0], a1[2]);
-          e4m3x4_to_f16x2x2(r[3], a1[1], a1[3]);
-          mma_f16(sa, a0, qb[k][0], qb[k][1]);
-          mma_f16(sb, a1, qb[k + 1][0], qb[k + 1][1]);
+          for (int k = 0; k < Gm::kSteps; ++k) {
+            uint32_t a[4];
+            ldsm_x4(tile_addr<Gm::kBoxBytes>(kbase, row, 2 * k + (lane >> 4)), a[0], a[1], a[2], a[3]);
+            if constexpr (std::is_same<KT, bf16>::value) mma_bf16((k & 1) ? sb : sa, a, qb[k][0], qb[k][1]);
+            else mma_f16((k & 1) ? sb : sa, a, qb[k][0], qb[k][1]);
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < Gm::kSteps; k += 2) {
+            uint32_t r[4];
+            ldsm_x4(tile_addr<Gm::kBoxBytes>(kbase, row, k + (lane >> 4)), r[0], r[1], r[2], r[3]);
+            // a lane's four bytes of a row are d = 16c + 4tig .. +3: the low pair
+            // feeds contraction slots 2tig, 2tig+1, the high pair 2tig+8, 2tig+9
+            uint32_t a0[4], a1[4];
+            e4m3x4_to_f16x2x2(r[0], a0[0], a0[2]);
+            e4m3x4_to_f16x2x2(r[1], a0[1], a0[3]);
+            e4m3x4_to_f16x2x2(r[2], a1[0], a1[2]);
+            e4m3x4_to_f16x2x2(r[3], a1[1], a1[3]);
+            mma_f16(sa, a0, qon ? qb[k][0] : 0u, qon ? qb[k][1] : 0u);
+            mma_f16(sb, a1, qon ? qb[k + 1][0] : 0u, qon ? qb[k + 1][1] : 0u);
+          }
         }
       }
       // the block's K scale for E4M3 caches (the slot's scales are only
-      // written for them)
-      const float sc0 = kFp8 ? p.scale_log2 * mt.ks[2 * rt] : p.scale_log2;
-      const float sc1 = kFp8 ? p.scale_log2 * mt.ks[2 * rt + 1] : p.scale_log2;
-      sv[rt][0] = (sa[0] + sb[0]) * sc0;
-      sv[rt][1] = (sa[1] + sb[1]) * sc0;
-      sv[rt][2] = (sa[2] + sb[2]) * sc1;
-      sv[rt][3] = (sa[3] + sb[3]) * sc1;
+      // written for them): per 8-token group, or (HP = 2) per head
+      float sc0 = p.scale_log2, sc1 = p.scale_log2;
+      if constexpr (kFp8 && HP == 2) {
+        sc0 = sc1 = p.scale_log2 * (hd_c ? mt.ks[1] : mt.ks[0]);
+      } else if constexpr (kFp8) {
+        sc0 = p.scale_log2 * mt.ks[2 * rs];
+        sc1 = p.scale_log2 * mt.ks[2 * rs + 1];
+      }
+      sv[rs][0] = (sa[0] + sb[0]) * sc0;
+      sv[rs][1] = (sa[1] + sb[1]) * sc0;
+      sv[rs][2] = (sa[2] + sb[2]) * sc1;
+      sv[rs][3] = (sa[3] + sb[3]) * sc1;
     }
     const uint32_t mask = mt.mask;
     float x0 = -INFINITY, x1 = -INFINITY;
 #pragma unroll
-    for (int rt = 0; rt < RT; ++rt) {
-      if (!((mask >> (rt * kRowTile + g)) & 1u)) sv[rt][0] = sv[rt][1] = -INFINITY;
-      if (!((mask >> (rt * kRowTile + g + 8)) & 1u)) sv[rt][2] = sv[rt][3] = -INFINITY;
-      x0 = fmaxf(x0, fmaxf(sv[rt][0], sv[rt][2]));
-      x1 = fmaxf(x1, fmaxf(sv[rt][1], sv[rt][3]));
+    for (int rs = 0; rs < RS; ++rs) {
+      if (!((mask >> (rs * kRowTile + g)) & 1u)) sv[rs][0] = sv[rs][1] = -INFINITY;
+      if (!((mask >> (rs * kRowTile + g + 8)) & 1u)) sv[rs][2] = sv[rs][3] = -INFINITY;
+      x0 = fmaxf(x0, fmaxf(sv[rs][0], sv[rs][2]));
+      x1 = fmaxf(x1, fmaxf(sv[rs][1], sv[rs][3]));
     }
 
     // online softmax (log2 units), per head column
@@ -762,37 +802,43 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     }
     const float b0 = m0 == -INFINITY ? 0.f : m0, b1 = m1 == -INFINITY ? 0.f : m1;
     // P^T of each row tile as B operands: transpose the accumulator-layout rows
-    uint32_t pb[RT][2];
+    uint32_t pb[RS][2];
 #pragma unroll
-    for (int rt = 0; rt < RT; ++rt) {
-      const float p0 = exp2f(sv[rt][0] - b0), p1 = exp2f(sv[rt][1] - b1);
-      const float p2 = exp2f(sv[rt][2] - b0), p3 = exp2f(sv[rt][3] - b1);
+    for (int rs = 0; rs < RS; ++rs) {
+      const float p0 = exp2f(sv[rs][0] - b0), p1 = exp2f(sv[rs][1] - b1);
+      const float p2 = exp2f(sv[rs][2] - b0), p3 = exp2f(sv[rs][3] - b1);
       l0 += p0 + p2;
       l1 += p1 + p3;
       if constexpr (std::is_same<KT, bf16>::value) {
-        pb[rt][0] = movmatrix_trans(pack_bf16(p0, p1));
-        pb[rt][1] = movmatrix_trans(pack_bf16(p2, p3));
+        pb[rs][0] = movmatrix_trans(pack_bf16(p0, p1));
+        pb[rs][1] = movmatrix_trans(pack_bf16(p2, p3));
       } else if constexpr (!kFp8) {
-        pb[rt][0] = movmatrix_trans(pack_f16(p0, p1));
-        pb[rt][1] = movmatrix_trans(pack_f16(p2, p3));
+        pb[rs][0] = movmatrix_trans(pack_f16(p0, p1));
+        pb[rs][1] = movmatrix_trans(pack_f16(p2, p3));
       } else {
-        const float v0 = mt.vs[2 * rt], v1 = mt.vs[2 * rt + 1];
-        pb[rt][0] = movmatrix_trans(pack_f16(p0 * v0, p1 * v0));
-        pb[rt][1] = movmatrix_trans(pack_f16(p2 * v1, p3 * v1));
+        const float v0 = HP == 2 ? (hd_c ? mt.vs[1] : mt.vs[0]) : mt.vs[2 * rs];
+        const float v1 = HP == 2 ? v0 : mt.vs[2 * rs + 1];
+        pb[rs][0] = movmatrix_trans(pack_f16(p0 * v0, p1 * v0));
+        pb[rs][1] = movmatrix_trans(pack_f16(p2 * v1, p3 * v1));
       }
     }
 
     // O^T += V^T P^T: each row tile is one 16-token contraction step,
     // one 16-row step of d at a time
+    // HP = 2: head h's V rows meet P^T with the other head's columns zeroed
     const bool partial = mask != Gm::kFullMask;
 #pragma unroll
     for (int rt = 0; rt < RT; ++rt) {
-      const int t0 = rt * kRowTile;
+      const int rs = rt % RS, hh = rt / RS;
+      const int t0 = rs * kRowTile;     // the row tile's first token
+      const int r0 = rt * kRowTile;     // its first row in the slot
+      const bool pon = HP == 1 || hd_b == hh;
+      const uint32_t pb0 = pon ? pb[rs][0] : 0u, pb1 = pon ? pb[rs][1] : 0u;
       if constexpr (!kFp8) {
 #pragma unroll
         for (int k = 0; k < Gm::kSteps; ++k) {
           uint32_t a[4];
-          ldsm_x4_trans(tile_addr<Gm::kBoxBytes>(vbase, t0 + (lane & 7) + ((lane >> 4) << 3),
+          ldsm_x4_trans(tile_addr<Gm::kBoxBytes>(vbase, r0 + (lane & 7) + ((lane >> 4) << 3),
                                                  2 * k + ((lane >> 3) & 1)),
                         a[0], a[1], a[2], a[3]);
           if (partial) {
@@ -801,14 +847,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
             a[2] = keep_tokens(a[2], mask, t0 + 2 * tig + 8);
             a[3] = keep_tokens(a[3], mask, t0 + 2 * tig + 8);
           }
-          if constexpr (std::is_same<KT, bf16>::value) mma_bf16(o[k], a, pb[rt][0], pb[rt][1]);
-          else mma_f16(o[k], a, pb[rt][0], pb[rt][1]);
+          if constexpr (std::is_same<KT, bf16>::value) mma_bf16(o[k], a, pb0, pb1);
+          else mma_f16(o[k], a, pb0, pb1);
         }
       } else {
 #pragma unroll
         for (int k = 0; k < Gm::kSteps; k += 2) {
           uint32_t r[4];
-          ldsm_x4_trans(tile_addr<Gm::kBoxBytes>(vbase, t0 + (lane & 15), k + (lane >> 4)),
+          ldsm_x4_trans(tile_addr<Gm::kBoxBytes>(vbase, r0 + (lane & 15), k + (lane >> 4)),
                         r[0], r[1], r[2], r[3]);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
@@ -823,7 +869,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
               a[2] = keep_tokens(a[2], mask, t0 + 2 * tig + 8);
               a[3] = keep_tokens(a[3], mask, t0 + 2 * tig + 8);
             }
-            mma_f16(o[k + h], a, pb[rt][0], pb[rt][1]);
+            mma_f16(o[k + h], a, pb0, pb1);
           }
         }
       }
@@ -1185,7 +1231,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // 3-D view of a cache: (d, token in block, block x KV head), boxes of 128
 // bytes x min(block_size, 16) rows x 1, 128-byte swizzle.
 bool make_cache_map(CUtensorMap* map, const void* base, int head_dim, int elem, int block_size,
-                    int tile_tokens, int64_t blocks_x_heads) {
+                    int tile_tokens, int64_t blocks_x_heads, int heads_per_box) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(block_size),
@@ -1193,7 +1239,8 @@ bool make_cache_map(CUtensorMap* map, const void* base, int head_dim, int elem, 
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * elem,
                            static_cast<cuuint64_t>(head_dim) * elem * block_size};
   cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elem),
-                       static_cast<cuuint32_t>(block_size < tile_tokens ? block_size : tile_tokens), 1};
+                       static_cast<cuuint32_t>(block_size < tile_tokens ? block_size : tile_tokens),
+                       static_cast<cuuint32_t>(heads_per_box)};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, elem == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 3,
                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -1204,28 +1251,28 @@ bool make_cache_map(CUtensorMap* map, const void* base, int head_dim, int elem, 
 
 namespace {
 
-template <typename QT, typename KT, int D, int TT>
+template <typename QT, typename KT, int D, int TT, int HP>
 size_t smem_bytes(int num_seqs) {
-  using Gm = Geom<KT, D, TT>;
+  using Gm = Geom<KT, D, TT, HP>;
   return 1024 + static_cast<size_t>(Gm::kWarps) * Gm::kSlots * (Gm::kSlotBytes + sizeof(SlotMeta) + 8) +
          (3 * static_cast<size_t>(num_seqs) + 2) * sizeof(int);
 }
 
-template <typename QT, typename KT, int D, int TT>
+template <typename QT, typename KT, int D, int TT, int HP = 1>
 cudaError_t launch_typed(const TcParams& tp, const void* k_cache, const void* v_cache, int num_sms,
                          cudaStream_t stream) {
   const DecodeParams& p = tp.p;
   CUtensorMap mk, mv;
   const int64_t bxh = static_cast<int64_t>(p.num_blocks) * p.kv_heads_phys;
-  if (!make_cache_map(&mk, k_cache, D, int(sizeof(KT)), p.block_size, TT, bxh) ||
-      !make_cache_map(&mv, v_cache, D, int(sizeof(KT)), p.block_size, TT, bxh))
+  if (!make_cache_map(&mk, k_cache, D, int(sizeof(KT)), p.block_size, TT, bxh, HP) ||
+      !make_cache_map(&mv, v_cache, D, int(sizeof(KT)), p.block_size, TT, bxh, HP))
     return cudaErrorInvalidValue;
-  auto kernel = decode_tc_kernel<QT, KT, D, TT>;
+  auto kernel = decode_tc_kernel<QT, KT, D, TT, HP>;
   static std::atomic<unsigned long long> attr_set{0};
   cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(kernel),
-                                      static_cast<int>(smem_bytes<QT, KT, D, TT>(kTcMaxSeqs)), attr_set);
+                                      static_cast<int>(smem_bytes<QT, KT, D, TT, HP>(kTcMaxSeqs)), attr_set);
   if (e != cudaSuccess) return e;
-  constexpr int kWarps = Geom<KT, D, TT>::kWarps;
+  constexpr int kWarps = Geom<KT, D, TT, HP>::kWarps;
   const int grid = (tp.num_warps + kWarps - 1) / kWarps;
   if (tp.pg.group_start != nullptr) {
     // the shared prefixes first, on the whole GPU; the decode grid that
@@ -1239,7 +1286,7 @@ cudaError_t launch_typed(const TcParams& tp, const void* k_cache, const void* v_
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kWarps * 32);
-  cfg.dynamicSmemBytes = smem_bytes<QT, KT, D, TT>(p.num_seqs);
+  cfg.dynamicSmemBytes = smem_bytes<QT, KT, D, TT, HP>(p.num_seqs);
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
@@ -1296,26 +1343,36 @@ int tc_num_warps(int num_sms, int64_t max_units, pa_dtype kv_dtype) {
 
 size_t tc_auto_workspace_bytes(int num_seqs, int head_dim, int group, int num_sms) {
   (void)num_seqs;
-  // two partial states per static share and per chunk (at most 2W chunks)
+  // two partial states per static share and per chunk (at most 2W chunks);
+  // E4M3 calls with 2 or 4 query heads per KV head run units of two KV heads,
+  // whose states hold twice the query heads
   const size_t W = static_cast<size_t>(num_sms) * kMaxWarps;
-  const size_t slots = 6 * W * static_cast<size_t>(state_floats(group, head_dim)) * sizeof(float);
+  const int sg = (group == 2 || group == 4) ? 2 * group : group;
+  const size_t slots = 6 * W * static_cast<size_t>(state_floats(sg, head_dim)) * sizeof(float);
   return slots;
 }
 
 cudaError_t launch_decode_tc(const DecodeParams& p, int head_dim, pa_dtype q_dtype,
                              pa_dtype kv_dtype, int partition_size, void* workspace, int num_sms,
                              cudaStream_t stream, const PrefixGroups* groups) {
-  const int tt = tc_tile_tokens(kv_dtype);
+  // E4M3 caches with 2 or 4 query heads per KV head: a unit is two adjacent
+  // KV heads (their query heads fill the MMA's 8 columns), its tiles 16
+  // tokens of both heads, one box per block for K and one for V
+  const int gkv = p.num_heads / p.num_kv_heads;
+  const bool pairs = kv_dtype == PA_FP8_E4M3 && head_dim == 128 && groups == nullptr && p.kv_div == 1 &&
+                     (gkv == 2 || gkv == 4) && p.num_kv_heads % 2 == 0 && p.block_size >= 16;
+  const int tt = pairs ? 16 : tc_tile_tokens(kv_dtype);
   const int part_tiles = partition_size / tt;
   TcParams tp{};
   tp.p = p;
-  tp.group = p.num_heads / p.num_kv_heads;
+  if (pairs) tp.p.num_kv_heads = p.num_kv_heads / 2;  // units
+  tp.group = p.num_heads / tp.p.num_kv_heads;
   tp.part_tiles = part_tiles;
   const int64_t tiles_max = (static_cast<int64_t>(p.max_context_len) + tt - 1) / tt;
   if (part_tiles == 0) {
     tp.claim = next_claim_counter();
     if (tp.claim == nullptr) return cudaErrorInvalidDevice;
-    tp.num_warps = tc_num_warps(num_sms, static_cast<int64_t>(p.num_seqs) * p.num_kv_heads * tiles_max, kv_dtype);
+    tp.num_warps = tc_num_warps(num_sms, static_cast<int64_t>(p.num_seqs) * tp.p.num_kv_heads * tiles_max, kv_dtype);
     tp.ws_slots = static_cast<float*>(workspace);
     if (groups != nullptr) {
       // the shared-prefix states follow the 6W decode states
@@ -1324,7 +1381,7 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int head_dim, pa_dtype q_dty
     }
   } else {
     const int64_t parts_max = (tiles_max + part_tiles - 1) / part_tiles;
-    tp.num_warps = tc_num_warps(num_sms, static_cast<int64_t>(p.num_seqs) * p.num_kv_heads * parts_max, kv_dtype);
+    tp.num_warps = tc_num_warps(num_sms, static_cast<int64_t>(p.num_seqs) * tp.p.num_kv_heads * parts_max, kv_dtype);
     // the tail of the partitions is claimed from a counter the reduce rearms
     tp.claim = next_claim_counter();
     if (tp.claim == nullptr) return cudaErrorInvalidDevice;
@@ -1339,6 +1396,10 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int head_dim, pa_dtype q_dty
   if (kv_dtype == PA_F16) {
     if (head_dim == 128) return launch_typed<f16, f16, 128, 16>(tp, kc, vc, num_sms, stream);
     return launch_typed<f16, f16, 64, 16>(tp, kc, vc, num_sms, stream);
+  }
+  if (pairs) {
+    if (q_dtype == PA_BF16) return launch_typed<bf16, fp8, 128, 16, 2>(tp, kc, vc, num_sms, stream);
+    return launch_typed<f16, fp8, 128, 16, 2>(tp, kc, vc, num_sms, stream);
   }
   if (q_dtype == PA_BF16) return launch_typed<bf16, fp8, 128, 32>(tp, kc, vc, num_sms, stream);
   return launch_typed<f16, fp8, 128, 32>(tp, kc, vc, num_sms, stream);

@@ -34,9 +34,10 @@ inline cudaError_t set_smem_limit_once(const void* fn, int bytes, std::atomic<un
 
 // 3-D TMA view of a cache [blocks, KV heads, block_size, head_dim] as (d, token
 // in block, block x KV head), boxes of 128 bytes x min(block_size,
-// tile_tokens) rows x 1, 128-byte swizzle (decode_tc.cu).
+// tile_tokens) rows x heads_per_box adjacent KV heads, 128-byte swizzle
+// (decode_tc.cu).
 bool make_cache_map(CUtensorMap* map, const void* base, int head_dim, int elem, int block_size,
-                    int tile_tokens, int64_t blocks_x_heads);
+                    int tile_tokens, int64_t blocks_x_heads, int heads_per_box = 1);
 
 // Sets the message pa_last_error_message() returns on this thread.
 void set_last_error(const char* fmt, ...);

@@ -296,6 +296,31 @@ def test_fp8_kv_decode(q_dtype, bs):
     assert np.array_equal(host_bits(dc.k_cache), kc)
 
 
+@pytest.mark.parametrize("Hq,Hkv", [(8, 4), (12, 3), (16, 8), (4, 4)])
+def test_fp8_kv_head_pairs(Hq, Hkv):
+    """E4M3 caches with 2 or 4 query heads per KV head and an even number of
+    KV heads run units of two adjacent KV heads (8 KV heads: 4 units; 4 KV
+    heads of 2 query heads each: units of 4 query heads); an odd number of KV
+    heads, or one query head per KV head, keeps units of one KV head. Every
+    layout matches the oracle, on the library's schedule and the split path."""
+    lengths = [1, 15, 16, 17, 100, 333, 1024, 1500]
+    case = workloads.fp8_layer(990 + Hq + Hkv, lengths, num_heads=Hq, num_kv_heads=Hkv, head_dim=128,
+                               block_size=16, src_dtype=BF16, name=f"fp8_pairs_{Hq}_{Hkv}")
+    dc = DeviceCase(case)
+    pa.reshape_and_cache(dc.new_key, dc.new_value, dc.k_cache, dc.v_cache, dc.slot_mapping,
+                         k_scale=dc.k_scale, v_scale=dc.v_scale, debug_err=dc.debug_err)
+    kc, vc = case.k_cache.copy(), case.v_cache.copy()
+    oracle.reshape_and_cache(case.new_key, case.new_value, kc, vc, case.slot_mapping, 16, BF16,
+                             FP8_E4M3, case.k_scale, case.v_scale)
+    ref = oracle_decode(case, k_cache=kc, v_cache=vc)
+    for part in (0, 32, 512):
+        out = run_decode(pa, dc, partition_size=part)
+        torch.cuda.synchronize()
+        max_abs, _ = assert_close(out, ref, BF16, FP8_E4M3, f"fp8 pairs part={part}")
+        assert max_abs <= 3e-2, max_abs
+    assert dc.debug_err.item() == 0
+
+
 def test_fp8_q_beyond_f16_range_is_flagged():
     """With an 8-bit cache q is multiplied in f16: a bf16 q value above 65504
     has no f16 counterpart, and the call reports it through debug_err."""

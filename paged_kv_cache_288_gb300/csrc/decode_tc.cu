@@ -947,7 +947,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) tc_merge_kernel(const TcParams 
   constexpr int kMergeThreads = NT;
   constexpr int kMergeChunk = NT >= 512 ? 256 : 128;  // contributors taken at a time
   const DecodeParams& p = tp.p;
-  if (blockIdx.x == 0 && blockIdx.y == 0) {
+  if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) {
     // the decode grid is complete: rearm its chunk counter for the next call
     griddep_wait();
     if (threadIdx.x == 0) *tp.claim = 0;
@@ -1064,10 +1064,14 @@ __global__ void __launch_bounds__(NT, 1024 / NT) tc_merge_kernel(const TcParams 
   __shared__ float4 s_part[kMergeThreads];
   const float* slots = tp.ws_slots;
   const int stride = state_floats(G, D);
-  const int ne4 = G * D / 4;                 // float4 elements in the block: 32..256
-  const int ngrp = kMergeThreads / ne4;      // contributor groups
-  const int e4 = threadIdx.x % ne4;
-  const int grp = threadIdx.x / ne4;
+  // the block's float4 elements (32..256); with gridDim.z > 1 this CTA takes
+  // the z-th of gridDim.z equal slices of them (few pairs with many
+  // contributors: more CTAs share each pair)
+  const int nes = G * D / 4 / static_cast<int>(gridDim.z);
+  const int ngrp = kMergeThreads / nes;      // contributor groups
+  const int el = threadIdx.x % nes;          // this thread's element within the slice
+  const int e4 = static_cast<int>(blockIdx.z) * nes + el;
+  const int grp = threadIdx.x / nes;
   const int he = (4 * e4) / D;               // head of this thread's elements
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x < kMaxG) {
@@ -1172,7 +1176,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) tc_merge_kernel(const TcParams 
   if (grp == 0) {
     float4 t = acc;
     for (int gi = 1; gi < ngrp; ++gi) {
-      const float4 u = s_part[gi * ne4 + e4];
+      const float4 u = s_part[gi * nes + el];
       t.x += u.x;
       t.y += u.y;
       t.z += u.z;
@@ -1309,9 +1313,16 @@ cudaError_t launch_typed(const TcParams& tp, const void* k_cache, const void* v_
   }
   cudaLaunchConfig_t mcfg = cfg;
   mcfg.gridDim = dim3(p.num_kv_heads, p.num_seqs);
+  // few pairs: each is split over up to 4 CTAs by element slices (slices of
+  // at least 32 float4s) so that more SMs share the merge
+  const int64_t npairs = static_cast<int64_t>(p.num_seqs) * p.num_kv_heads;
+  int zs = 1;
+  while (zs < 4 && npairs * zs * 2 <= num_sms && (tp.group * D / 4) % (zs * 2) == 0 && tp.group * D / 4 / (zs * 2) >= 32)
+    zs *= 2;
   mcfg.dynamicSmemBytes = 0;
   if (static_cast<int64_t>(p.num_seqs) * p.num_kv_heads <= num_sms) {
     mcfg.blockDim = dim3(kMergeThreadsFew);
+    mcfg.gridDim.z = zs;
     err = cudaLaunchKernelEx(&mcfg, tc_merge_kernel<QT, D, TT, kMergeThreadsFew>, tp);
   } else if (tp.group <= 4 && tp.group * D <= 4 * kMergeThreadsSmall &&
              tp.num_warps < 2 * static_cast<int64_t>(p.num_seqs) * p.num_kv_heads) {

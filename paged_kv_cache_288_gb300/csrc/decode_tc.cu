@@ -49,6 +49,8 @@ constexpr int kMaxWarps = 12;   // the most of either (sizes the workspace)
 constexpr int kRowTile = 16;   // MMA M: tokens per row tile
 constexpr int kMaxG = 8;       // MMA N
 constexpr uint32_t kFull = 0xffffffffu;
+// inputs larger than this are not warmed into the L2 at the start of a call
+constexpr int64_t kWarmBytes = 16ll << 20;
 
 // A tile is TT tokens (16 or 32, one or two MMA row tiles) of one
 // (sequence, KV unit): TT rows of K and TT rows of V of each of the unit's HP
@@ -256,8 +258,31 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
   __shared__ int64_t s_queue[kWarps][NS + 1][3];  // claimed ranges waiting: start, end, first slot
 
   if (threadIdx.x < kWarps * NS) mbar_init(smem_u32(&bars[threadIdx.x]), 1);
+  if (threadIdx.x == 0) {
+    prefetch_tensormap(&tmap_k);
+    prefetch_tensormap(&tmap_v);
+  }
   mbar_init_fence();
   griddep_wait();
+  // Warm the L2 with the call's small inputs: q, the block tables and the
+  // E4M3 scales, a 128-byte line per thread of the grid at a time. Every
+  // warp's first tiles and q rows need them at once, and from HBM those
+  // loads would queue behind the first tiles' own traffic.
+  {
+    const int64_t nthr = static_cast<int64_t>(gridDim.x) * kThreads;
+    const int64_t me = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+    auto warm = [&](const void* base, int64_t bytes) {
+      if (base == nullptr || bytes > kWarmBytes) return;
+      const char* b = static_cast<const char*>(base);
+      for (int64_t l = me; l * 128 < bytes; l += nthr) prefetch_l2(b + l * 128);
+    };
+    warm(p.q, static_cast<int64_t>(B) * p.num_heads * D * static_cast<int64_t>(sizeof(QT)));
+    warm(p.block_tables, static_cast<int64_t>(B) * p.max_blocks_per_seq * 4);
+    if constexpr (kFp8) {
+      warm(p.k_scale, static_cast<int64_t>(p.num_blocks) * p.kv_heads_phys * 4);
+      warm(p.v_scale, static_cast<int64_t>(p.num_blocks) * p.kv_heads_phys * 4);
+    }
+  }
 
   // ---- per-sequence tile and partition counts, and their exclusive prefix --
   const int per = (B + kThreads - 1) / kThreads;
@@ -519,8 +544,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
   // q of one (sequence, KV head) as MMA B fragments: column g = query head
   // kvh*G + g (zero for g >= G); 16-bit caches contract d in order, E4M3
   // caches in the permuted order their K fragments arrive in.
+  // fetch_q issues the loads (E4M3: the four q elements of a step raw, as
+  // two 16-bit pairs) and convert_q turns them into f16 fragments, so the
+  // first q rows can be in flight while the first tiles are issued.
   uint32_t qb[Gm::kSteps][2];
-  auto load_q = [&](int seq, int kvh) {
+  auto fetch_q = [&](int seq, int kvh) {
     const QT* qrow = static_cast<const QT*>(p.q) + (static_cast<int64_t>(seq) * Hq + kvh * G + g) * D;
 #pragma unroll
     for (int k = 0; k < Gm::kSteps; ++k) {
@@ -530,15 +558,29 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
         qb[k][0] = *reinterpret_cast<const uint32_t*>(qrow + 16 * k + 2 * tig);
         qb[k][1] = *reinterpret_cast<const uint32_t*>(qrow + 16 * k + 8 + 2 * tig);
       } else {
-        float f[4];
-        load_float<QT, 4>(qrow + 16 * k + 4 * tig, f);
-        qb[k][0] = pack_f16(f[0], f[1]);
-        qb[k][1] = pack_f16(f[2], f[3]);
+        const uint2 r = *reinterpret_cast<const uint2*>(qrow + 16 * k + 4 * tig);
+        qb[k][0] = r.x;
+        qb[k][1] = r.y;
+      }
+    }
+  };
+  auto convert_q = [&]() {
+    if constexpr (kFp8) {
+#pragma unroll
+      for (int k = 0; k < Gm::kSteps; ++k) {
+        const float2 a = pair_to_float2(qb[k][0], static_cast<QT*>(nullptr));
+        const float2 b = pair_to_float2(qb[k][1], static_cast<QT*>(nullptr));
+        qb[k][0] = pack_f16(a.x, a.y);
+        qb[k][1] = pack_f16(b.x, b.y);
         // beyond the f16 range q turns infinite: report it
-        if (fmaxf(fmaxf(fabsf(f[0]), fabsf(f[1])), fmaxf(fabsf(f[2]), fabsf(f[3]))) > 65504.f)
+        if (fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(b.x), fabsf(b.y))) > 65504.f)
           flag_error(p.debug_err, PA_DEVERR_Q_RANGE);
       }
     }
+  };
+  auto load_q = [&](int seq, int kvh) {
+    fetch_q(seq, kvh);
+    convert_q();
   };
 
   // online-softmax state of the current piece: this lane's two heads
@@ -700,13 +742,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
       }
     }
   };
+  fetch_q(cc.seq, cc.kvh);  // in flight while the first tiles are issued
   int pending = 0;
   for (int s = 0; s < NS && !prod_done; ++s) {
     issue(pc, s);
     advance_producer();
     ++pending;
   }
-  load_q(cc.seq, cc.kvh);
+  convert_q();
   reset();
   int piece_t0 = cc.t;
   bool first_piece = true;

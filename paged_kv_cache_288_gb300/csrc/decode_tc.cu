@@ -454,6 +454,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
   // one block when the block holds at least TT tokens, else it spans
   // TT / block_size blocks).
   constexpr int kMaxSub = TT / 8;
+  // K and V are read once: their lines leave the L2 first, so the partial
+  // states the merge reads, q and the tables stay there
+  const uint64_t kv_policy = l2_evict_first_policy();
   auto issue = [&](const Cursor& c, int s) {
     const int ctx = s_ctx[c.seq];
     const int st = start_of(c.seq);
@@ -534,9 +537,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
         const int z = ph * p.kv_heads_phys + (HP == 2 ? 2 * c.kvh : kv_head_of(p, c.kvh));
         const uint32_t at = b * Gm::kBoxBytes + h * bh * 128;  // boxes of later blocks sit after earlier ones
         if (r & 1)
-          tma_load_3d(vdst + at, &tmap_v, b * Gm::kBoxW, off, z, bar);
+          tma_load_3d_hint(vdst + at, &tmap_v, b * Gm::kBoxW, off, z, bar, kv_policy);
         else
-          tma_load_3d(kdst + at, &tmap_k, b * Gm::kBoxW, off, z, bar);
+          tma_load_3d_hint(kdst + at, &tmap_k, b * Gm::kBoxW, off, z, bar, kv_policy);
       }
     }
   };

@@ -88,30 +88,33 @@ struct TcParams {
   int32_t num_warps;   // warps that share the work
   int32_t part_tiles;  // tiles per partition (split path); 0 = auto schedule
   int32_t group;       // query heads per KV head
-  int32_t small_rule;  // 16-bit caches, one unit per KV head: short lists keep a smaller static share
+  int32_t head_units;  // every unit is one KV head or an E4M3 head pair (not MQA's split units)
 };
 
-// The auto schedule: the first kStatic256/256 of the U tiles are split
-// evenly over the W warps (warp w: [w*S/W, (w+1)*S/W)); the rest are chunks
-// of C >= kMinChunk tiles that warps claim from a counter when their share is
-// done, so SMs that stream faster take more of them. At most 2W chunks.
-// Calls with 16-bit caches, one unit per KV head and fewer than kSmallShare
-// tiles per warp keep only kStatic256Small/256 static (measured: the
-// Llama-8B-shaped batch 92.8 against 94.5 us, the shared-prefix batch 82.1
-// against 84.7; longer lists, E4M3 tiles and MQA units, whose four units
-// of a KV head gain from running side by side, were faster with 192).
+// The auto schedule: the first S of the U tiles are split evenly over the W
+// warps (warp w: [w*S/W, (w+1)*S/W)); the rest are chunks of C >= kMinChunk
+// tiles that warps claim from a counter when their share is done, so SMs
+// that stream faster take more of them. At most 2W chunks.
+// S is kStatic256/256 of U. When every unit is one KV head (or an E4M3 head
+// pair) it is kStatic256Short/256 for lists of fewer than kShortShare tiles
+// per warp and kStatic256Long/256 for longer ones. Measured against 192:
+// with 160, the Llama-8B-shaped batch 92.8 against 94.5 us, the
+// shared-prefix batch 82.1 against 84.7, the E4M3 layer 70.7 against 72.0;
+// with 224, long context bs 16 167.1 against 168.9. MQA's units of 8 query
+// heads keep 192: the four units of a KV head gain from running side by side.
 constexpr int kStatic256 = 192;
-constexpr int kStatic256Small = 160;
-constexpr int64_t kSmallShare = 64;
+constexpr int kStatic256Short = 160;
+constexpr int kStatic256Long = 224;
+constexpr int64_t kShortShare = 64;
 constexpr int64_t kMinChunk = 8;
 
 struct Sched {
   int64_t S, C, K;
 };
 
-__device__ __forceinline__ Sched make_sched(int64_t U, int64_t W, bool small_rule) {
+__device__ __forceinline__ Sched make_sched(int64_t U, int64_t W, bool head_units) {
   Sched sc;
-  sc.S = U * (small_rule && U < kSmallShare * W ? kStatic256Small : kStatic256) / 256;
+  sc.S = U * (!head_units ? kStatic256 : U < kShortShare * W ? kStatic256Short : kStatic256Long) / 256;
   const int64_t rest = U - sc.S;
   int64_t c = (rest + 2 * W - 1) / (2 * W);
   sc.C = c < kMinChunk ? kMinChunk : c;
@@ -370,7 +373,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
   };
   int64_t SP = 0;  // split path: partitions shared out statically
   if (tp.part_tiles == 0) {
-    const Sched sc = make_sched(U, W, tp.small_rule != 0);
+    const Sched sc = make_sched(U, W, tp.head_units != 0);
     S = sc.S;
     C = sc.C;
     K = sc.K;
@@ -969,13 +972,22 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
 }
 
 // Combine the partial states of every (sequence, KV head) that several
-// ranges shared (launched as a programmatic dependent of the decode grid): with M = max_c m_c, out = sum_c 2^(m_c-M) acc_c / sum_c
-// 2^(m_c-M) l_c. Sequences with no context get zero rows here. Contributors
-// are taken 128 at a time (one per thread for their slots, maxima and sums);
-// the rows are float4 elements of the G x D block, and when the block has
-// fewer than 256 float4s the threads split the contributors into groups, so
-// a step issues the loads of many contributors at once. A running maximum
-// carries the online softmax across chunks of contributors.
+// ranges shared (launched as a programmatic dependent of the decode grid):
+// with M = max_c m_c, out = sum_c 2^(m_c-M) acc_c / sum_c 2^(m_c-M) l_c.
+// Sequences with no context get zero rows here. The rows are float4 elements
+// of the G x D block, EPT per thread; when the block has fewer elements than
+// the CTA has threads, the threads split the contributors into groups, so a
+// step issues the loads of many contributors at once. Contributor slots are
+// listed in shared memory 128 (or 256) at a time.
+// - Up to 256 threads: the (max, sum) of every contributor in the list are
+//   loaded by a thread each, a warp per head derives the weights, and a
+//   running maximum carries the softmax across lists.
+// - 1024 threads (long contributor lists): each thread keeps its own online
+//   softmax (running maximum, denominator, weighted rows) over its group's
+//   contributors, loading a contributor's rows with its maximum and sum, and
+//   group 0 combines the groups at the end; no barrier stands between the
+//   decode grid's completion and the loads (long context bs 16: 169.7 ->
+//   168.2 us; slower on the E4M3 layer's short lists, 72.4 against 74.2).
 // Threads of a merge CTA: 256, or 1024 when there are few pairs (their
 // contributor lists are then long, and more threads keep more rows in flight),
 // or 128 when most pairs have at most two contributors (fewer warps than twice
@@ -983,15 +995,19 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
 // fits on an SM beside the persistent decode CTA, so the first of them are
 // resident, past their prologue, when the decode grid completes. (Measured:
 // 128 threads were faster on batches of short pairs, 256 on the Llama-8B-
-// shaped batch, about 2.4 contributors per pair.)
+// shaped batch, about 2.4 contributors per pair.) Blocks of more than 128
+// float4s with more pairs than one wave of 256-thread CTAs holds take 128
+// threads of two elements each, so that one wave holds them all (the E4M3
+// layer's head-pair blocks: 73.1 -> 72.4 us).
 constexpr int kMergeThreads = 256;
 constexpr int kMergeThreadsFew = 1024;
 constexpr int kMergeThreadsSmall = 128;
 
-template <typename QT, int D, int TT, int NT>
+template <typename QT, int D, int TT, int NT, int EPT = 1>
 __global__ void __launch_bounds__(NT, 1024 / NT) tc_merge_kernel(const TcParams tp) {
   constexpr int kMergeThreads = NT;
   constexpr int kMergeChunk = NT >= 512 ? 256 : 128;  // contributors taken at a time
+  constexpr bool kOnline = NT >= 512;  // long contributor lists: an online softmax per thread
   const DecodeParams& p = tp.p;
   if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) {
     // the decode grid is complete: rearm its chunk counter for the next call
@@ -1051,7 +1067,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) tc_merge_kernel(const TcParams 
   // shared (64-bit divisions are long instruction sequences).
   __shared__ int64_t s_sched[6];
   if (threadIdx.x == 0) {
-    const Sched sc = make_sched(U, W, tp.small_rule != 0);
+    const Sched sc = make_sched(U, W, tp.head_units != 0);
     const int64_t S = sc.S, C = sc.C;
     // static shares meeting [seg0, min(seg1, S)): warp w holds [w*S/W,
     // (w+1)*S/W), so the owner of tile x < S is ceil((x+1)W/S) - 1
@@ -1103,142 +1119,265 @@ __global__ void __launch_bounds__(NT, 1024 / NT) tc_merge_kernel(const TcParams 
     return static_cast<int>(2 * W + 2 * k + ((c == nstat && st < seg0) ? 1 : 0));
   };
 
-  __shared__ float s_w[kMergeChunk][kMaxG];  // max of each contributor, then its weight
-  __shared__ float s_l[kMergeChunk][kMaxG];
   __shared__ int s_slot[kMergeChunk];
-  __shared__ float s_run[kMaxG], s_den[kMaxG], s_scale[kMaxG];
-  __shared__ float4 s_part[kMergeThreads];
   const float* slots = tp.ws_slots;
   const int stride = state_floats(G, D);
   // the block's float4 elements (32..256); with gridDim.z > 1 this CTA takes
   // the z-th of gridDim.z equal slices of them (few pairs with many
-  // contributors: more CTAs share each pair)
+  // contributors: more CTAs share each pair). A thread holds EPT elements of
+  // the slice, nth apart.
   const int nes = G * D / 4 / static_cast<int>(gridDim.z);
-  const int ngrp = kMergeThreads / nes;      // contributor groups
-  const int el = threadIdx.x % nes;          // this thread's element within the slice
-  const int e4 = static_cast<int>(blockIdx.z) * nes + el;
-  const int grp = threadIdx.x / nes;
-  const int he = (4 * e4) / D;               // head of this thread's elements
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x < kMaxG) {
-    s_run[threadIdx.x] = -INFINITY;
-    s_den[threadIdx.x] = 0.f;
+  const int nth = nes / EPT;                 // threads that cover the slice once
+  const int ngrp = kMergeThreads / nth;      // contributor groups
+  const int el = threadIdx.x % nth;          // this thread's first element within the slice
+  const int grp = threadIdx.x / nth;
+  int e4[EPT], he[EPT];                      // this thread's elements and their heads
+#pragma unroll
+  for (int e = 0; e < EPT; ++e) {
+    e4[e] = static_cast<int>(blockIdx.z) * nes + el + e * nth;
+    he[e] = (4 * e4[e]) / D;
   }
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (threadIdx.x < min(kMergeChunk, nc)) s_slot[threadIdx.x] = slot_of(threadIdx.x);
-  __syncthreads();
-  griddep_wait();  // the decode grid's partial states are complete from here on
-  constexpr int kBatch = 4;  // row loads a thread keeps in flight
-  for (int cb = 0; cb < nc; cb += kMergeChunk) {
-    const int nin = min(kMergeChunk, nc - cb);
-    if (cb > 0) {
-      if (threadIdx.x < nin) s_slot[threadIdx.x] = slot_of(cb + threadIdx.x);
+  if constexpr (kOnline) {
+    // each thread carries its own online softmax over the contributors of its
+    // group: running maximum, denominator and weighted rows, per element
+    float run[EPT], den[EPT];
+    float4 acc[EPT];
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) {
+      run[e] = -INFINITY;
+      den[e] = 0.f;
+      acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (threadIdx.x < min(kMergeChunk, nc)) s_slot[threadIdx.x] = slot_of(threadIdx.x);
+    __syncthreads();
+    griddep_wait();  // the decode grid's partial states are complete from here on
+    constexpr int kBatch = 4 / EPT;  // contributors a thread loads at a time (4 rows in flight)
+    for (int cb = 0; cb < nc; cb += kMergeChunk) {
+      const int nin = min(kMergeChunk, nc - cb);
+      if (cb > 0) {
+        __syncthreads();  // every thread is done with the previous chunk's slots
+        if (threadIdx.x < nin) s_slot[threadIdx.x] = slot_of(cb + threadIdx.x);
+        __syncthreads();
+      }
+      for (int j0 = grp; j0 < nin; j0 += kBatch * ngrp) {
+        // one round of loads: each contributor's row elements, maximum and sum
+        float4 v[kBatch][EPT];
+        float m[kBatch][EPT], l[kBatch][EPT];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int j = j0 + u * ngrp;
+          const int sl = j < nin ? s_slot[j] : -1;
+          const float* st = slots + int64_t(sl) * stride;
+#pragma unroll
+          for (int e = 0; e < EPT; ++e) {
+            v[u][e] = sl >= 0 ? __ldcg(reinterpret_cast<const float4*>(st) + e4[e]) : make_float4(0.f, 0.f, 0.f, 0.f);
+            m[u][e] = sl >= 0 ? __ldcg(st + G * D + he[e]) : -INFINITY;
+            l[u][e] = sl >= 0 ? __ldcg(st + G * D + G + he[e]) : 0.f;
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+#pragma unroll
+          for (int e = 0; e < EPT; ++e) {
+            const float mj = m[u][e];
+            if (mj > run[e]) {
+              const float a = exp2f(run[e] - mj);  // 0 while the running maximum is -inf
+              den[e] *= a;
+              acc[e].x *= a;
+              acc[e].y *= a;
+              acc[e].z *= a;
+              acc[e].w *= a;
+              run[e] = mj;
+            }
+            const float w = mj == -INFINITY ? 0.f : exp2f(mj - run[e]);
+            den[e] += w * l[u][e];
+            acc[e].x += w * v[u][e].x;
+            acc[e].y += w * v[u][e].y;
+            acc[e].z += w * v[u][e].z;
+            acc[e].w += w * v[u][e].w;
+          }
+        }
+      }
+    }
+    // the groups' states, combined by group 0
+    __shared__ float4 s_acc[kMergeThreads * EPT];
+    __shared__ float2 s_md[kMergeThreads * EPT];
+    if (ngrp > 1) {
+#pragma unroll
+      for (int e = 0; e < EPT; ++e) {
+        s_acc[threadIdx.x * EPT + e] = acc[e];
+        s_md[threadIdx.x * EPT + e] = make_float2(run[e], den[e]);
+      }
       __syncthreads();
     }
-    // one round of loads: each contributor's (max, sum) per head, and this
-    // thread's first kBatch rows
-    if (threadIdx.x < nin) {
-      const int sl = s_slot[threadIdx.x];
+    if (grp == 0) {
 #pragma unroll
-      for (int h = 0; h < kMaxG; ++h) {
-        const bool ok = sl >= 0 && h < G;
-        s_w[threadIdx.x][h] = ok ? __ldcg(slots + int64_t(sl) * stride + G * D + h) : -INFINITY;
-        s_l[threadIdx.x][h] = ok ? __ldcg(slots + int64_t(sl) * stride + G * D + G + h) : 0.f;
+      for (int e = 0; e < EPT; ++e) {
+        float mx = run[e];
+        for (int gi = 1; gi < ngrp; ++gi) mx = fmaxf(mx, s_md[(gi * nth + el) * EPT + e].x);
+        const float a0 = run[e] == -INFINITY ? 0.f : exp2f(run[e] - mx);
+        float4 t = make_float4(a0 * acc[e].x, a0 * acc[e].y, a0 * acc[e].z, a0 * acc[e].w);
+        float d = a0 * den[e];
+        for (int gi = 1; gi < ngrp; ++gi) {
+          const int k = (gi * nth + el) * EPT + e;
+          const float2 md = s_md[k];
+          const float a = md.x == -INFINITY ? 0.f : exp2f(md.x - mx);
+          const float4 u = s_acc[k];
+          t.x += a * u.x;
+          t.y += a * u.y;
+          t.z += a * u.z;
+          t.w += a * u.w;
+          d += a * md.y;
+        }
+        const float inv = d > 0.f ? 1.f / d : 0.f;
+        uint2 pk;
+        if constexpr (std::is_same<QT, bf16>::value) {
+          pk.x = pack_bf16(t.x * inv, t.y * inv);
+          pk.y = pack_bf16(t.z * inv, t.w * inv);
+        } else {
+          pk.x = pack_f16(t.x * inv, t.y * inv);
+          pk.y = pack_f16(t.z * inv, t.w * inv);
+        }
+        *reinterpret_cast<uint2*>(out + 4 * e4[e]) = pk;
       }
     }
-    float4 v[kBatch];
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int j = grp + u * ngrp;
-      const int sl = j < nin ? s_slot[j] : -1;
-      v[u] = sl >= 0 ? __ldcg(reinterpret_cast<const float4*>(slots + int64_t(sl) * stride) + e4)
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
+  } else {
+    __shared__ float s_w[kMergeChunk][kMaxG];  // max of each contributor, then its weight
+    __shared__ float s_l[kMergeChunk][kMaxG];
+    __shared__ float s_run[kMaxG], s_den[kMaxG], s_scale[kMaxG];
+    __shared__ float4 s_part[kMergeThreads * EPT];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x < kMaxG) {
+      s_run[threadIdx.x] = -INFINITY;
+      s_den[threadIdx.x] = 0.f;
     }
+    float4 acc[EPT];
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (threadIdx.x < min(kMergeChunk, nc)) s_slot[threadIdx.x] = slot_of(threadIdx.x);
     __syncthreads();
-    // per head (warp h): new running max, rescale factor, weights, sum
-    if (warp < G) {
-      const int h = warp;
-      float cm = -INFINITY;
-      for (int j = lane; j < nin; j += 32) cm = fmaxf(cm, s_w[j][h]);
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, off));
-      const float old = s_run[h];
-      const float nm = fmaxf(old, cm);
-      float d = 0.f;
-      for (int j = lane; j < nin; j += 32) {
-        const float m = s_w[j][h];
-        const float w = m == -INFINITY ? 0.f : exp2f(m - nm);
-        s_w[j][h] = w;
-        d += w * s_l[j][h];
+    griddep_wait();  // the decode grid's partial states are complete from here on
+    constexpr int kBatch = 4 / EPT;  // rows a thread loads at a time (4 float4s in flight)
+    for (int cb = 0; cb < nc; cb += kMergeChunk) {
+      const int nin = min(kMergeChunk, nc - cb);
+      if (cb > 0) {
+        if (threadIdx.x < nin) s_slot[threadIdx.x] = slot_of(cb + threadIdx.x);
+        __syncthreads();
       }
+      // one round of loads: each contributor's (max, sum) per head, and this
+      // thread's first kBatch rows
+      if (threadIdx.x < nin) {
+        const int sl = s_slot[threadIdx.x];
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
-      __syncwarp();
-      if (lane == 0) {
-        const float scale = old == -INFINITY ? 0.f : exp2f(old - nm);
-        s_scale[h] = scale;
-        s_den[h] = s_den[h] * scale + d;
-        s_run[h] = nm;
+        for (int h = 0; h < kMaxG; ++h) {
+          const bool ok = sl >= 0 && h < G;
+          s_w[threadIdx.x][h] = ok ? __ldcg(slots + int64_t(sl) * stride + G * D + h) : -INFINITY;
+          s_l[threadIdx.x][h] = ok ? __ldcg(slots + int64_t(sl) * stride + G * D + G + h) : 0.f;
+        }
       }
-    }
-    __syncthreads();
-    const float sc_e = s_scale[he];
-    acc.x *= sc_e;
-    acc.y *= sc_e;
-    acc.z *= sc_e;
-    acc.w *= sc_e;
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int j = grp + u * ngrp;
-      const float wt = j < nin ? s_w[j][he] : 0.f;
-      acc.x += wt * v[u].x;
-      acc.y += wt * v[u].y;
-      acc.z += wt * v[u].z;
-      acc.w += wt * v[u].w;
-    }
-    // contributors beyond the first batch of this thread
-    for (int j0 = grp + kBatch * ngrp; j0 < nin; j0 += kBatch * ngrp) {
+      float4 v[kBatch][EPT];
 #pragma unroll
       for (int u = 0; u < kBatch; ++u) {
-        const int j = j0 + u * ngrp;
+        const int j = grp + u * ngrp;
         const int sl = j < nin ? s_slot[j] : -1;
-        v[u] = sl >= 0 ? __ldcg(reinterpret_cast<const float4*>(slots + int64_t(sl) * stride) + e4)
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int j = j0 + u * ngrp;
-        const float wt = j < nin ? s_w[j][he] : 0.f;
-        acc.x += wt * v[u].x;
-        acc.y += wt * v[u].y;
-        acc.z += wt * v[u].z;
-        acc.w += wt * v[u].w;
+        for (int e = 0; e < EPT; ++e)
+          v[u][e] = sl >= 0 ? __ldcg(reinterpret_cast<const float4*>(slots + int64_t(sl) * stride) + e4[e])
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      __syncthreads();
+      // per head (warps take heads h, h + warps, ...): new running max,
+      // rescale factor, weights, sum
+      for (int h = warp; h < G; h += kMergeThreads / 32) {
+        float cm = -INFINITY;
+        for (int j = lane; j < nin; j += 32) cm = fmaxf(cm, s_w[j][h]);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, off));
+        const float old = s_run[h];
+        const float nm = fmaxf(old, cm);
+        float d = 0.f;
+        for (int j = lane; j < nin; j += 32) {
+          const float m = s_w[j][h];
+          const float w = m == -INFINITY ? 0.f : exp2f(m - nm);
+          s_w[j][h] = w;
+          d += w * s_l[j][h];
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+        __syncwarp();
+        if (lane == 0) {
+          const float scale = old == -INFINITY ? 0.f : exp2f(old - nm);
+          s_scale[h] = scale;
+          s_den[h] = s_den[h] * scale + d;
+          s_run[h] = nm;
+        }
+      }
+      __syncthreads();
+      auto accumulate = [&](int j0) {
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int j = j0 + u * ngrp;
+#pragma unroll
+          for (int e = 0; e < EPT; ++e) {
+            const float wt = j < nin ? s_w[j][he[e]] : 0.f;
+            acc[e].x += wt * v[u][e].x;
+            acc[e].y += wt * v[u][e].y;
+            acc[e].z += wt * v[u][e].z;
+            acc[e].w += wt * v[u][e].w;
+          }
+        }
+      };
+#pragma unroll
+      for (int e = 0; e < EPT; ++e) {
+        const float sc_e = s_scale[he[e]];
+        acc[e].x *= sc_e;
+        acc[e].y *= sc_e;
+        acc[e].z *= sc_e;
+        acc[e].w *= sc_e;
+      }
+      accumulate(grp);
+      // contributors beyond the first batch of this thread
+      for (int j0 = grp + kBatch * ngrp; j0 < nin; j0 += kBatch * ngrp) {
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int j = j0 + u * ngrp;
+          const int sl = j < nin ? s_slot[j] : -1;
+#pragma unroll
+          for (int e = 0; e < EPT; ++e)
+            v[u][e] = sl >= 0 ? __ldcg(reinterpret_cast<const float4*>(slots + int64_t(sl) * stride) + e4[e])
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        accumulate(j0);
+      }
+      __syncthreads();
+    }
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) s_part[threadIdx.x * EPT + e] = acc[e];
+    __syncthreads();
+    if (grp == 0) {
+#pragma unroll
+      for (int e = 0; e < EPT; ++e) {
+        float4 t = acc[e];
+        for (int gi = 1; gi < ngrp; ++gi) {
+          const float4 u = s_part[(gi * nth + el) * EPT + e];
+          t.x += u.x;
+          t.y += u.y;
+          t.z += u.z;
+          t.w += u.w;
+        }
+        const float d = s_den[he[e]];
+        const float inv = d > 0.f ? 1.f / d : 0.f;
+        uint2 pk;
+        if constexpr (std::is_same<QT, bf16>::value) {
+          pk.x = pack_bf16(t.x * inv, t.y * inv);
+          pk.y = pack_bf16(t.z * inv, t.w * inv);
+        } else {
+          pk.x = pack_f16(t.x * inv, t.y * inv);
+          pk.y = pack_f16(t.z * inv, t.w * inv);
+        }
+        *reinterpret_cast<uint2*>(out + 4 * e4[e]) = pk;
       }
     }
-    __syncthreads();
-  }
-  s_part[threadIdx.x] = acc;
-  __syncthreads();
-  if (grp == 0) {
-    float4 t = acc;
-    for (int gi = 1; gi < ngrp; ++gi) {
-      const float4 u = s_part[gi * nes + el];
-      t.x += u.x;
-      t.y += u.y;
-      t.z += u.z;
-      t.w += u.w;
-    }
-    const float d = s_den[he];
-    const float inv = d > 0.f ? 1.f / d : 0.f;
-    uint2 pk;
-    if constexpr (std::is_same<QT, bf16>::value) {
-      pk.x = pack_bf16(t.x * inv, t.y * inv);
-      pk.y = pack_bf16(t.z * inv, t.w * inv);
-    } else {
-      pk.x = pack_f16(t.x * inv, t.y * inv);
-      pk.y = pack_f16(t.z * inv, t.w * inv);
-    }
-    *reinterpret_cast<uint2*>(out + 4 * e4) = pk;
   }
 }
 
@@ -1366,10 +1505,21 @@ cudaError_t launch_typed(const TcParams& tp, const void* k_cache, const void* v_
   while (zs < 4 && npairs * zs * 2 <= num_sms && (tp.group * D / 4) % (zs * 2) == 0 && tp.group * D / 4 / (zs * 2) >= 32)
     zs *= 2;
   mcfg.dynamicSmemBytes = 0;
+  // more pairs than one wave of kMergeThreads-thread CTAs holds, each of more
+  // than kMergeThreadsSmall float4s: kMergeThreadsSmall-thread CTAs of two
+  // elements per thread, so that all of them are resident at once
+  bool wide = false;
+  if constexpr (D == 128)
+    wide = tp.group * D / 4 > kMergeThreadsSmall && npairs > static_cast<int64_t>(num_sms) * (1024 / kMergeThreads);
   if (static_cast<int64_t>(p.num_seqs) * p.num_kv_heads <= num_sms) {
     mcfg.blockDim = dim3(kMergeThreadsFew);
     mcfg.gridDim.z = zs;
     err = cudaLaunchKernelEx(&mcfg, tc_merge_kernel<QT, D, TT, kMergeThreadsFew>, tp);
+  } else if (wide) {
+    if constexpr (D == 128) {
+      mcfg.blockDim = dim3(kMergeThreadsSmall);
+      err = cudaLaunchKernelEx(&mcfg, tc_merge_kernel<QT, D, TT, kMergeThreadsSmall, 2>, tp);
+    }
   } else if (tp.group <= 4 && tp.group * D <= 4 * kMergeThreadsSmall &&
              tp.num_warps < 2 * static_cast<int64_t>(p.num_seqs) * p.num_kv_heads) {
     mcfg.blockDim = dim3(kMergeThreadsSmall);
@@ -1430,7 +1580,7 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int head_dim, pa_dtype q_dty
   const int part_tiles = partition_size / tt;
   TcParams tp{};
   tp.p = p;
-  tp.small_rule = kv_dtype != PA_FP8_E4M3 && p.kv_div == 1;
+  tp.head_units = p.kv_div == 1;
   if (pairs) tp.p.num_kv_heads = p.num_kv_heads / 2;  // units
   tp.group = p.num_heads / tp.p.num_kv_heads;
   tp.part_tiles = part_tiles;

@@ -321,6 +321,24 @@ def test_fp8_kv_head_pairs(Hq, Hkv):
     assert dc.debug_err.item() == 0
 
 
+def test_merge_of_eight_head_units_over_many_pairs():
+    """Units of 8 query heads (a 256-float4 block per pair) with more pairs
+    than one wave of 256-thread merge CTAs holds: the merge runs 128-thread
+    CTAs of two elements per thread, whose four warps derive the weights of
+    all eight heads. Short random lengths leave most pairs split over two or
+    three ranges."""
+    g = np.random.default_rng(4242)
+    lengths = g.integers(1, 400, size=100)
+    for dtype in (BF16, F16):
+        case = workloads.paged_case(4243, lengths, 64, 8, 128, 16, dtype, name="wide_merge")
+        dc = DeviceCase(case)
+        out = run_decode(pa, dc)
+        ref = oracle_decode(case)
+        torch.cuda.synchronize()
+        assert_close(out, ref, dtype, dtype, f"wide merge {dtype}")
+        assert dc.debug_err.item() == 0
+
+
 def test_fp8_q_beyond_f16_range_is_flagged():
     """With an 8-bit cache q is multiplied in f16: a bf16 q value above 65504
     has no f16 counterpart, and the call reports it through debug_err."""

@@ -88,7 +88,7 @@ struct TcParams {
   int32_t num_warps;   // warps that share the work
   int32_t part_tiles;  // tiles per partition (split path); 0 = auto schedule
   int32_t group;       // query heads per KV head
-  int32_t head_units;  // every unit is one KV head or an E4M3 head pair (not MQA's split units)
+  int32_t short_share;  // static share /256 of short lists; 0 for MQA's split units
 };
 
 // The auto schedule: the first S of the U tiles are split evenly over the W
@@ -96,14 +96,20 @@ struct TcParams {
 // tiles that warps claim from a counter when their share is done, so SMs
 // that stream faster take more of them. At most 2W chunks.
 // S is kStatic256/256 of U. When every unit is one KV head (or an E4M3 head
-// pair) it is kStatic256Short/256 for lists of fewer than kShortShare tiles
-// per warp and kStatic256Long/256 for longer ones. Measured against 192:
-// with 160, the Llama-8B-shaped batch 92.8 against 94.5 us, the
-// shared-prefix batch 82.1 against 84.7, the E4M3 layer 70.7 against 72.0;
-// with 224, long context bs 16 167.1 against 168.9. MQA's units of 8 query
-// heads keep 192: the four units of a KV head gain from running side by side.
+// pair) it is a shorter share for lists of fewer than kShortShare tiles per
+// warp (kStatic256Short16/256 for 16-bit caches, kStatic256ShortFp8/256 for
+// E4M3) and kStatic256Long/256 for longer ones. Measured:
+// - 16-bit, short lists: the Llama-8B-shaped batch 92.8 us with 160 against
+//   94.5 with 192; later 87.9 with 144, 89.5 with 160, 90.7 with 128; the
+//   shared-prefix batch's suffixes 55.2 with 144 against 56.0 with 160.
+// - E4M3 head pairs (about 18 tiles per warp): 70.9 with 160, 72.0 with 192,
+//   77.0 with 144, 79.3 with 128.
+// - long context bs 16 (108 tiles per warp): 167.1 with 224, 168.9 with 192.
+// MQA's units of 8 query heads keep 192: the four units of a KV head gain
+// from running side by side.
 constexpr int kStatic256 = 192;
-constexpr int kStatic256Short = 160;
+constexpr int kStatic256Short16 = 144;
+constexpr int kStatic256ShortFp8 = 160;
 constexpr int kStatic256Long = 224;
 constexpr int64_t kShortShare = 64;
 constexpr int64_t kMinChunk = 8;
@@ -112,9 +118,10 @@ struct Sched {
   int64_t S, C, K;
 };
 
-__device__ __forceinline__ Sched make_sched(int64_t U, int64_t W, bool head_units) {
+// short_share: the static share /256 of short lists, 0 for MQA's split units
+__device__ __forceinline__ Sched make_sched(int64_t U, int64_t W, int short_share) {
   Sched sc;
-  sc.S = U * (!head_units ? kStatic256 : U < kShortShare * W ? kStatic256Short : kStatic256Long) / 256;
+  sc.S = U * (short_share == 0 ? kStatic256 : U < kShortShare * W ? short_share : kStatic256Long) / 256;
   const int64_t rest = U - sc.S;
   int64_t c = (rest + 2 * W - 1) / (2 * W);
   sc.C = c < kMinChunk ? kMinChunk : c;
@@ -373,7 +380,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
   };
   int64_t SP = 0;  // split path: partitions shared out statically
   if (tp.part_tiles == 0) {
-    const Sched sc = make_sched(U, W, tp.head_units != 0);
+    const Sched sc = make_sched(U, W, tp.short_share);
     S = sc.S;
     C = sc.C;
     K = sc.K;
@@ -460,6 +467,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
   // K and V are read once: their lines leave the L2 first, so the partial
   // states the merge reads, q and the tables stay there
   const uint64_t kv_policy = l2_evict_first_policy();
+  const uint64_t state_policy = l2_evict_last_policy();
   auto issue = [&](const Cursor& c, int s) {
     const int ctx = s_ctx[c.seq];
     const int st = start_of(c.seq);
@@ -688,27 +696,34 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
       }
     } else {
       // part of a (sequence, KV head) shared with other warps
+      // (16-bit caches: stored under an L2 evict-last policy for the merge;
+      // measured on the Llama-8B-shaped batch 88.5 against 89.5 us, while
+      // the E4M3 layer was 0.8 us slower with it)
       float* base = tp.ws_slots + slot_index * state_floats(G, D);
+      auto put = [&](float* a, float v) {
+        if constexpr (kFp8) *a = v;
+        else st_global_hint(a, v, state_policy);
+      };
 #pragma unroll
       for (int k = 0; k < Gm::kSteps; ++k) {
         const int da = d_of(k, 0), db = d_of(k, 1);
         if (h0 < G) {
-          base[h0 * D + da] = o[k][0];
-          base[h0 * D + db] = o[k][2];
+          put(base + h0 * D + da, o[k][0]);
+          put(base + h0 * D + db, o[k][2]);
         }
         if (h1 < G) {
-          base[h1 * D + da] = o[k][1];
-          base[h1 * D + db] = o[k][3];
+          put(base + h1 * D + da, o[k][1]);
+          put(base + h1 * D + db, o[k][3]);
         }
       }
       if (g == 0) {
         if (h0 < G) {
-          base[G * D + h0] = m0;
-          base[G * D + G + h0] = l0;
+          put(base + G * D + h0, m0);
+          put(base + G * D + G + h0, l0);
         }
         if (h1 < G) {
-          base[G * D + h1] = m1;
-          base[G * D + G + h1] = l1;
+          put(base + G * D + h1, m1);
+          put(base + G * D + G + h1, l1);
         }
       }
     }
@@ -1067,7 +1082,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) tc_merge_kernel(const TcParams 
   // shared (64-bit divisions are long instruction sequences).
   __shared__ int64_t s_sched[6];
   if (threadIdx.x == 0) {
-    const Sched sc = make_sched(U, W, tp.head_units != 0);
+    const Sched sc = make_sched(U, W, tp.short_share);
     const int64_t S = sc.S, C = sc.C;
     // static shares meeting [seg0, min(seg1, S)): warp w holds [w*S/W,
     // (w+1)*S/W), so the owner of tile x < S is ceil((x+1)W/S) - 1
@@ -1580,7 +1595,7 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int head_dim, pa_dtype q_dty
   const int part_tiles = partition_size / tt;
   TcParams tp{};
   tp.p = p;
-  tp.head_units = p.kv_div == 1;
+  tp.short_share = p.kv_div != 1 ? 0 : kv_dtype == PA_FP8_E4M3 ? kStatic256ShortFp8 : kStatic256Short16;
   if (pairs) tp.p.num_kv_heads = p.num_kv_heads / 2;  // units
   tp.group = p.num_heads / tp.p.num_kv_heads;
   tp.part_tiles = part_tiles;

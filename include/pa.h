@@ -46,7 +46,7 @@ extern "C" {
 typedef enum {
   PA_OK = 0,
   PA_ERR_INVALID = 1,     /* a host-checked argument is wrong */
-  PA_ERR_UNSUPPORTED = 2, /* valid, but not a shape/type this build runs */
+  PA_ERR_UNSUPPORTED = 2, /* valid, but not a shape/type the library runs */
   PA_ERR_CUDA = 3,        /* the CUDA runtime reported an error */
   PA_ERR_WORKSPACE = 4    /* the workspace given is too small */
 } pa_status;
